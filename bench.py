@@ -1,0 +1,348 @@
+"""Benchmark: decode MoE-layer tokens/s and expert-weight HBM GB/s.
+
+Workload (default): the 35B-like decode stack -- d_model 2048, E=256 routed
+experts, K=4, expert ffn 512, one always-on shared expert, unfused LoRA r=16
+on the shared expert, prerouter heads 2560->512->256, 40 layers, batch 1 --
+on seeded synthetic weights and inputs.  One step = one decode token through
+all 40 layers: per layer the routed + shared expert FFN, the fused combine +
+residual (+ RMS for the next layer's input), the prerouter head of the next
+layer and its top-K router (layer 0 routes with its own router).  Steady-state
+steps are replayed from captured CUDA graphs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 35b]
+    python bench.py --impl reference ...   # the CPU oracle, same metric
+
+Prints one JSON line (rank 0).  N > 1 runs N independent replicas (the layer
+does not shard across GPUs in this build), one per GPU, launched by torchrun.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode MoE-layer tokens/s and expert-weight HBM GB/s vs GB300 peak (1 GPU)"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="35b")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-layers", type=int, default=40,
+                    help="layer samples the oracle baseline times (native arm)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle
+def oracle_layer_sampler(cfg, n_layers: int):
+    """Host data for n_layers distinct layers and a function timing one layer
+    of the oracle (head + top-K + experts + combine) on it."""
+    import numpy as np
+
+    import oracle as orc
+    from int4_expert_gemv_gb300 import synth
+
+    data = []
+    for r in range(min(n_layers, cfg.L)):
+        x = synth.step_input(cfg, 10_000 + r)[0].astype(np.float64)
+        router = synth.router_host(cfg, r)
+        idx, w, _ = orc.topk(orc.head_logits(router, x), cfg.K)
+        prev, _, _ = orc.topk(orc.head_logits(router, -x), cfg.K)
+        exps = {e: synth.expert_host(cfg, r, e) for e in idx.tolist()}
+        any_e = next(iter(exps.values()))
+        data.append(dict(x=x, idx=idx, w=w, prev=prev,
+                         experts=[exps.get(e, any_e) for e in range(cfg.E)],
+                         shared=synth.expert_host(cfg, r, synth.SHARED_EXPERT) if cfg.shared else None,
+                         head=synth.head_host(cfg, r)))
+
+    def run_layer(i: int):
+        dd = data[i % len(data)]
+        z = orc.head_logits(dd["head"], dd["x"], dd["idx"], dd["prev"], cfg.K)
+        orc.topk(z, cfg.K)
+        y = orc.expert_ffn(dd["experts"], dd["shared"], dd["x"][None], dd["idx"][None])[0]
+        orc.combine(y, dd["w"], cfg.shared, dd["x"])
+
+    return run_layer
+
+
+def cpu_baseline(cfg, layer_samples: int):
+    run_layer = oracle_layer_sampler(cfg, 4)
+    run_layer(0)
+    t0 = time.perf_counter()
+    for i in range(layer_samples):
+        run_layer(i)
+    dt = time.perf_counter() - t0
+    per_layer = dt / layer_samples
+    return {"value": 1.0 / (per_layer * cfg.depth), "unit": "tokens/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{layer_samples} layer passes (head, top-K, {cfg.slots} experts, combine) "
+                      f"on 4 distinct layers, {dt:.1f} s, extrapolated to a {cfg.depth}-layer token"}
+
+
+def run_reference(args, cfg):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    run_layer = oracle_layer_sampler(cfg, 4)
+    for i in range(args.warmup):
+        run_layer(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run_layer(i)
+    dt = time.perf_counter() - t0
+    v = args.steps / (dt * cfg.depth)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": 1, "layers": cfg.depth},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                             "sample": f"each step = one layer pass of the plain C oracle "
+                                       f"(head, top-K, {cfg.slots} experts, combine); "
+                                       f"tokens/s = steps / (time * {cfg.depth} layers)"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- native
+def kernels_per_step(cfg, stack) -> int:
+    """Kernel launches of one steady-state step (counted from the calls the
+    driver makes; the kernels per call are fixed by the library)."""
+    ed = stack.m.layers[0]["experts_desc"]
+    gu_lora = any(ed.lora[i].r for i in range(2)) or any(ed.shared_lora[i].r for i in range(2))
+    ffn = 2 + (1 if gu_lora else 0)
+    head = 1 + (1 if cfg.H else 0)
+    n = 0
+    for N in range(cfg.depth):
+        if N == 0 and not cfg.self_predict:
+            n += 1 + 1                      # router (H = 0 head) + top-K
+        n += ffn + 1                        # experts + combine
+        if N + 1 < cfg.depth or cfg.self_predict:
+            n += head + 1                   # head + top-K
+    return n
+
+
+def run_native(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    from int4_expert_gemv_gb300 import synth
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    import __graft_entry__
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    __graft_entry__.build()
+
+    dm = DeviceModel(cfg)
+    st = DecodeStack(dm)
+    total = args.warmup + args.steps
+    xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
+                                       (total + 64, cfg.d), 1.0)).cuda()
+
+    # step 0 (routers everywhere) eagerly, then capture the steady state
+    st.step(xin[0])
+    st.capture()
+    for t in range(1, args.warmup):
+        st.step(xin[t])
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for t in range(args.warmup, total):
+            st.step(xin[t])
+        stop.record(stream)
+        barrier()
+    ms = start.elapsed_time(stop)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    tok_s = world * args.steps / (ms / 1000.0)
+    ms_step = ms / args.steps
+
+    # ---- per-call kernel durations (instrumented replay of further steps)
+    ev = []
+    t_next = total
+    inst = {}
+    for rot in range(3):
+        g = torch.cuda.CUDAGraph()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(cfg.depth)]
+        with torch.cuda.graph(g):
+            st.enqueue_step(rot if rot else 3, ffn_events=evs)
+        inst[rot] = (g, evs)
+    ffn_ms = []
+    n_inst = min(args.steps, 48)
+    for i in range(n_inst):
+        t = t_next + i
+        st.xin.copy_(xin[t % xin.shape[0]])
+        g, evs = inst[t % 3]
+        g.replay()
+        torch.cuda.synchronize()
+        ffn_ms += [a.elapsed_time(b) for a, b in evs]
+    st.t = t_next + n_inst
+    ffn_avg_ms = statistics.mean(ffn_ms)
+    ffn_bytes = cfg.expert_bytes_per_layer()
+
+    # ---- end to end: host input -> device, step, result -> host, per step
+    pin_in = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 1),
+                                          (args.steps, cfg.d), 1.0)).pin_memory()
+    pin_out = torch.empty((args.steps, cfg.d), dtype=torch.float32).pin_memory()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        st.xin.copy_(pin_in[i], non_blocking=True)
+        g = st.graphs[st.t % 3]
+        g.replay()
+        st.t += 1
+        pin_out[i].copy_(st.stream, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    if rank == 0:
+        hbm, hbm_kind = peaks()
+        expert_gbs = ffn_bytes * cfg.depth / (ms_step / 1000.0) / 1e9
+        achieved = ffn_bytes / (ffn_avg_ms / 1000.0) / 1e9
+        head_bytes = dm.head_bytes_per_token()
+        line = {
+            "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {
+                "workload": cfg.name, "batch": 1, "layers": cfg.depth, "d_model": cfg.d,
+                "experts": cfg.E, "top_k": cfg.K, "expert_ffn": cfg.F,
+                "shared_expert": cfg.shared, "weight_bits": cfg.bits, "group": cfg.group,
+                "head_hidden": cfg.H, "head_prec": cfg.head_prec,
+                "lora": f"r{cfg.lora_r} alpha{cfg.lora_alpha:g} {cfg.lora_on}" if cfg.lora_r else "none",
+                "l2": f"no flush: each step reads {cfg.depth * (ffn_bytes + head_bytes) / 1e6:.0f} MB "
+                      f"of weights (> {L2_BYTES / 1e6:.0f} MB L2); routed experts change every step",
+                "graphs": "steady-state steps replayed from captured CUDA graphs",
+            },
+            "expert_weight_gbs": expert_gbs,
+            "expert_weight_frac_of_hbm": expert_gbs / hbm,
+            "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn_int4 (gate/up+SwiGLU, down)",
+                         "achieved": achieved, "peak": hbm, "peak_kind": hbm_kind,
+                         "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                         "bytes_per_launch": ffn_bytes, "avg_launch_us": ffn_avg_ms * 1000.0,
+                         "timing": f"CUDA events around each layer's call in {n_inst} "
+                                   f"instrumented graph replays after the timed region"},
+            "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+                    "h2d_bytes_per_step": cfg.d * 4, "d2h_bytes_per_step": cfg.d * 4},
+            "gpu_launches": kernels_per_step(cfg, st) * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_layers)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from int4_expert_gemv_gb300.configs import ALL
+    cfg = ALL[args.config]
+    if args.impl == "reference":
+        import oracle
+        oracle.build()
+        run_reference(args, cfg)
+    else:
+        run_native(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

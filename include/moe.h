@@ -1,0 +1,228 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) decode MoE layer with routing
+ * predicted a token ahead.
+ *
+ * One decode step of a fine-grained Mixture-of-Experts FFN layer is split into
+ * four calls, in the order a decoder issues them:
+ *
+ *   moe_prerouter_head    head(x) = fc2(erf-GELU(fc1(f))) + l(f) on the
+ *                         features f = [x ; K-hot(cur) ; K-hot(prev)] of width
+ *                         d_model + 2E; predicts the next layer's routing.
+ *                         Source: "La otra mitad del muro de la memoria:
+ *                         Servir MoEs de 35B desde SSD con prediccion de
+ *                         enrutamiento entrenada" (xyznot.com/es/paper/
+ *                         2609.18063), section "Arquitectura del cabezal
+ *                         Prerouter" (dim = d_model + 2E; head equation; l is
+ *                         a linear path started from the next layer's router).
+ *   moe_topk_route        top-K of the logits with softmax weights
+ *                         renormalised over the K kept experts.  The same page,
+ *                         "Ideas clave": the prediction is used as the real
+ *                         routing (no fallback, no dropped tokens).
+ *   moe_expert_ffn_int4   per selected expert (and the shared expert) the
+ *                         group-quantised affine int4 / 2-bit gate/up GEMV with
+ *                         SwiGLU, then the down GEMV, each with an optional
+ *                         unfused LoRA delta y = W x + (alpha/r) B A x.
+ *                         Sources: "Inferencia de LLM MoE en MacBook Pro:
+ *                         Streaming de Expertos desde SSD con Metal"
+ *                         (kerneldigest.dev), section "Arquitectura del
+ *                         Sistema" (4-/2-bit dequant matvec, fused SwiGLU) and
+ *                         its Metal fragment (w = nibble*scale + bias, taken as
+ *                         fma(nibble, scale*x, bias*x)); the LoRA form is the
+ *                         xyznot page, "Ejecucion del adaptador no fusionado".
+ *   moe_combine_residual  out = residual + sum_k w_k y_k + y_shared, with an
+ *                         optional RMS-normalised copy of out (kerneldigest
+ *                         page, "Arquitectura del Sistema": fused expert
+ *                         combine + residual, RMS normalisation).
+ *
+ * Conventions shared by every call
+ *  - Memory: every pointer argument is a DEVICE pointer unless stated
+ *    otherwise; the caller owns all memory.  The library never allocates,
+ *    frees or synchronises.  Scratch memory comes from a caller-provided
+ *    workspace whose size the matching *_workspace_bytes() call returns.
+ *  - Alignment: device pointers must be 16-byte aligned; expert pools and
+ *    packed matrices 256-byte aligned.
+ *  - Streams: every call only enqueues work on `stream` (asynchronous).
+ *    Descriptors are read during the call and not retained.
+ *  - Errors: calls return a moe_status.  Arguments are validated before any
+ *    work is enqueued; a rejected call enqueues nothing.  moe_last_error()
+ *    returns a human-readable detail of the last failure on the calling host
+ *    thread.  Launch failures are reported as MOE_ECUDA.
+ *  - Determinism: no floating-point atomics; reductions run in a fixed order,
+ *    so results are bitwise reproducible run to run.
+ *
+ * Packed weight format ("records").  A weight matrix [rows][cols] of affine
+ * group-quantised weights is stored as `rows` records of
+ * moe_record_bytes(cols, bits) bytes each: first the row's packed codes
+ * (cols*bits/8 bytes, uint32 words little-endian, element j of a word at bits
+ * [bits*j, bits*j+bits)), then one {fp16 scale, fp16 bias} pair per group of
+ * 64 columns, then zero padding to a multiple of 16 bytes.  Decoded weight:
+ * w = code*scale + bias.
+ *
+ * Expert blob.  One expert is one contiguous blob of
+ * moe_pool_expert_bytes(d, F, bits, 64) bytes: a gate/up section of 2F
+ * records of d columns (record 2f is gate row f, record 2f+1 is up row f),
+ * then a down section of d records of F columns; each section starts on a
+ * 256-byte boundary.  An expert pool is E blobs, expert_stride bytes apart.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+typedef enum {
+    MOE_OK = 0,
+    MOE_EINVAL = 1,         /* an argument is out of range, null or misaligned */
+    MOE_EUNSUPPORTED = 2,   /* valid, but a shape this build has no kernel for */
+    MOE_ECUDA = 3,          /* a CUDA runtime call or kernel launch failed     */
+    MOE_ETIMEOUT = 4,       /* a bounded device-side wait expired              */
+    MOE_ENOSPACE = 5        /* the workspace is smaller than required          */
+} moe_status;
+
+/* Static string naming a status code ("MOE_OK", ...). */
+const char *moe_status_string(int status);
+/* Detail of the last failing call on this host thread ("" if none).  The
+ * string stays valid until the next failing call on the same thread. */
+const char *moe_last_error(void);
+
+/* ---------------------------------------------------------------- enums */
+enum {
+    MOE_DTYPE_F32 = 0,      /* activations in fp32                             */
+    MOE_DTYPE_BF16 = 1      /* activations in bfloat16                         */
+};
+
+enum {
+    MOE_PREC_AFFINE4 = 4,   /* affine int4, group 64, packed records           */
+    MOE_PREC_FP16 = 16      /* plain fp16 row-major [rows][cols]               */
+};
+
+/* ---------------------------------------------------------------- sizes */
+/* Bytes of one packed record (one row of `cols` weights); 0 if invalid. */
+size_t moe_record_bytes(int cols, int bits);
+/* Bytes of a packed matrix: rows * moe_record_bytes(cols, bits). */
+size_t moe_packed_matrix_bytes(int rows, int cols, int bits);
+/* Bytes of one expert blob (gate/up and down sections, see above); 0 if the
+ * shape is invalid (bits not in {2,4}, group != 64, d or F not multiples of
+ * 64).  At d=4096, F=1024, bits=4 this is 7,077,888 bytes (6.75 MiB). */
+size_t moe_pool_expert_bytes(int d, int F, int bits, int group);
+
+/* ---------------------------------------------------------------- packing */
+/* Packs one logical matrix into records.  q: uint32 [rows][cols*bits/32],
+ * s, b: fp16 bit patterns [rows][cols/64]; out: moe_packed_matrix_bytes()
+ * bytes.  All device pointers; enqueued on `stream`. */
+int moe_pack_matrix(const uint32_t *q, const uint16_t *s, const uint16_t *b,
+                    int rows, int cols, int bits, void *out,
+                    cudaStream_t stream);
+
+/* Packs E experts into a pool.  Logical inputs, contiguous per expert:
+ * gate_q/up_q [E][F][d*bits/32], gate_s/b, up_s/b [E][F][d/64],
+ * down_q [E][d][F*bits/32], down_s/b [E][d][F/64].  pool: E blobs,
+ * expert_stride bytes apart (>= moe_pool_expert_bytes, multiple of 256). */
+int moe_pack_experts(int d, int F, int E, int bits,
+                     const uint32_t *gate_q, const uint16_t *gate_s,
+                     const uint16_t *gate_b, const uint32_t *up_q,
+                     const uint16_t *up_s, const uint16_t *up_b,
+                     const uint32_t *down_q, const uint16_t *down_s,
+                     const uint16_t *down_b, void *pool, size_t expert_stride,
+                     cudaStream_t stream);
+
+/* Test hook: decodes matrix `which` (0 gate [F][d], 1 up [F][d], 2 down
+ * [d][F]) of one expert blob into fp32 out[rows][cols] as
+ * fmaf(code, scale, bias), the same decode the GEMV kernels use. */
+int moe_debug_dequant(const void *blob, int d, int F, int bits, int which,
+                      float *out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- head */
+typedef struct {
+    int d;                    /* d_model                                      */
+    int E;                    /* experts of the predicted layer               */
+    int H;                    /* head hidden size; 0 = plain router l(x) only  */
+    int prec;                 /* MOE_PREC_AFFINE4 or MOE_PREC_FP16 for the
+                                 dense matrices fc1x, fc2, lx                 */
+    const void *fc1x;         /* [H][d]  fc1 columns that multiply x          */
+    const uint16_t *fc1_tab;  /* [2E][H] fp16: fc1 columns of the two K-hot
+                                 vectors, transposed (row c = column d+c)     */
+    const uint16_t *b1;       /* [H] fp16, or NULL (zero)                     */
+    const void *fc2;          /* [E][H]                                       */
+    const uint16_t *b2;       /* [E] fp16, or NULL                            */
+    const void *lx;           /* [E][d]  l columns that multiply x            */
+    const uint16_t *l_tab;    /* [2E][E] fp16, or NULL (zero)                 */
+    const uint16_t *bl;       /* [E] fp16, or NULL                            */
+} moe_head_desc;
+
+size_t moe_prerouter_head_workspace_bytes(const moe_head_desc *hd, int T);
+
+/* Logits of the prerouter head for T tokens.
+ * x: [T][d] in x_dtype.  cur_idx / prev_idx: int32 [T][K] expert indices in
+ * [0, E) of the current / previous token's route (the K-hot vectors); either
+ * may be NULL (an all-zero vector).  logits: fp32 [T][E].
+ *   a = fc1x x + sum_{c in cur} fc1_tab[c] + sum_{c in prev} fc1_tab[E+c] + b1
+ *   logits = fc2 gelu_erf(a) + b2 + lx x + sum l_tab rows (same rule) + bl
+ * With H == 0 only the l branch is computed (a plain linear router). */
+int moe_prerouter_head(const moe_head_desc *hd, const void *x, int x_dtype,
+                       const int32_t *cur_idx, const int32_t *prev_idx, int K,
+                       int T, float *logits, void *ws, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* ---------------------------------------------------------------- route */
+/* Top-K of logits [T][E] ordered by (value descending, index ascending).
+ * idx: int32 [T][K]; w: fp32 [T][K], w_k = exp(z_k - z_1) / sum_j exp(z_j - z_1)
+ * over the kept K; margin: fp32 [T] (may be NULL), z_(K) - z_(K+1) (+inf if
+ * K == E).  1 <= K <= 16, K <= E <= 1024. */
+int moe_topk_route(const float *logits, int T, int E, int K, int32_t *idx,
+                   float *w, float *margin, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- experts */
+typedef struct {
+    int r;                    /* rank; 0 = no adapter                         */
+    float scale;              /* alpha / r                                    */
+    const uint16_t *A;        /* fp16 [r][in]  (expert e: A + e*a_stride)     */
+    const uint16_t *B;        /* fp16 [out][r] (expert e: B + e*b_stride)     */
+    size_t a_stride;          /* elements between experts' A (routed only)    */
+    size_t b_stride;          /* elements between experts' B (routed only)    */
+} moe_lora_desc;
+
+typedef struct {
+    int d;                    /* d_model (multiple of 64)                     */
+    int F;                    /* expert SwiGLU hidden size (multiple of 64)   */
+    int E;                    /* routed experts in the pool                   */
+    int bits;                 /* 4 or 2                                       */
+    const void *pool;         /* E expert blobs                               */
+    size_t expert_stride;     /* bytes between blobs (multiple of 256)        */
+    const void *shared;       /* blob of the always-on shared expert, or NULL */
+    moe_lora_desc lora[3];    /* routed experts: gate, up, down               */
+    moe_lora_desc shared_lora[3]; /* shared expert: gate, up, down            */
+} moe_experts_desc;
+
+size_t moe_expert_ffn_workspace_bytes(const moe_experts_desc *ed, int T, int K);
+
+/* Expert outputs for T tokens routed to idx [T][K] (int32, in [0, E)).
+ * x: [T][d] in x_dtype.  y_slots: fp32 [T][K + (shared != NULL)][d]; slot
+ * k < K holds expert idx[t][k]'s output y = W_d h (+ LoRA), the last slot the
+ * shared expert's.  h = silu(W_g x + LoRA) * (W_u x + LoRA) is kept in fp32
+ * for x_dtype == MOE_DTYPE_F32 and rounded to bf16 for MOE_DTYPE_BF16.
+ * T == 1 is the decode path; T > 1 groups tokens by expert first. */
+int moe_expert_ffn_int4(const moe_experts_desc *ed, const void *x, int x_dtype,
+                        const int32_t *idx, int T, int K, float *y_slots,
+                        void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------- combine */
+/* out[t] = residual[t] + sum_k w[t][k] * y_slots[t][k] (+ y_slots[t][K] if
+ * has_shared), all fp32, y_slots [T][K + has_shared][d].  If x_next is not
+ * NULL it receives out[t] / sqrt(mean(out[t]^2) + 1e-6).  out may alias
+ * residual. */
+int moe_combine_residual(const float *y_slots, const float *w, int T, int K,
+                         int has_shared, int d, const float *residual,
+                         float *out, float *x_next, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

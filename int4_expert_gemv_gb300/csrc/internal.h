@@ -1,0 +1,75 @@
+// internal.h -- launcher interfaces between the C ABI (abi.cu) and the kernel
+// translation units.  Every launcher assumes validated arguments and only
+// enqueues work; it returns a moe_status.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct LoraDev {
+    int r;
+    float scale;
+    const uint16_t *A;
+    const uint16_t *B;
+    size_t a_stride, b_stride;
+};
+
+struct FfnParams {
+    const uint8_t *pool;
+    size_t stride;
+    const uint8_t *shared;
+    const int32_t *idx;          // [T][K]
+    int T, K, slots, d, F, E, bits;
+    const void *x;               // [T][d]
+    int x_dtype;
+    int round_h_bf16;
+    float *h;                    // workspace [T*slots][F]
+    float *v;                    // workspace [T*slots][3][kMaxLoraRank]
+    float *y;                    // [T*slots][d]
+    LoraDev lora[3];
+    LoraDev shared_lora[3];
+    BlobLayout L;
+    int any_gu_lora;             // some slot carries a gate or up adapter
+    // grouped (T > 1) path
+    int32_t *counts;             // workspace [E+1]
+    int32_t *offsets;            // workspace [E+2]
+    int32_t *perm;               // workspace [T*K] (token*K + k), by expert
+};
+
+struct HeadParams {
+    int d, E, H, K, T, prec;
+    const uint8_t *fc1x;
+    const uint16_t *fc1_tab, *b1;
+    const uint8_t *fc2;
+    const uint16_t *b2;
+    const uint8_t *lx;
+    const uint16_t *l_tab, *bl;
+    const void *x;
+    int x_dtype;
+    const int32_t *cur, *prev;
+    float *g;                    // workspace [T][H]
+    float *zl;                   // workspace [T][E]
+    float *logits;               // [T][E]
+};
+
+int launch_expert_ffn(const FfnParams &p, cudaStream_t st);
+int launch_prerouter_head(const HeadParams &p, cudaStream_t st);
+int launch_topk(const float *logits, int T, int E, int K, int32_t *idx, float *w,
+                float *margin, cudaStream_t st);
+int launch_combine(const float *y, const float *w, int T, int K, int has_shared, int d,
+                   const float *res, float *out, float *xn, cudaStream_t st);
+int launch_pack_rows(const uint32_t *q, const uint16_t *s, const uint16_t *b, int rows,
+                     int cols, int bits, int nmat, size_t src_q_stride,
+                     size_t src_sb_stride, uint8_t *dst, size_t dst_mat_stride,
+                     size_t first_record, size_t record_step, cudaStream_t st);
+int launch_debug_dequant(const uint8_t *sec, size_t rec, size_t first_record,
+                         size_t record_step, int rows, int cols, int bits, float *out,
+                         cudaStream_t st);
+
+int num_sms();
+
+}  // namespace moe

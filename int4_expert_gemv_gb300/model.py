@@ -1,0 +1,265 @@
+"""Device-resident synthetic model and the decode-stack driver.
+
+DeviceModel draws every weight of a configuration on the GPU with the seeded
+generator (synth.py / csrc/synth.cu), packs experts into per-expert blobs and
+head matrices into records through the C ABI, and keeps descriptors for the
+four calls.  DecodeStack runs decode steps of the layer stack through those
+four calls only, and can capture one step as a CUDA graph.
+
+Stack semantics (one decode step at token t; x_0 is the step's input):
+  layer 0 routes with its own router (a head with H = 0) on x_0;
+  layer N >= 1 uses the route head N-1 predicted at t-1 (at t = 0, when no
+  prediction exists yet, its own router);
+  y = experts(x_N); out_N = stream_N + combine(y); x_{N+1} = rms(out_N);
+  head N runs on x_N with cur = layer N's route at t and prev = layer N's
+  route at t-1 and predicts layer N+1's route for t+1.
+A single-layer stack whose head predicts its own next route (self_predict)
+routes with the head's prediction from step 1 on.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import moe, synth
+from .configs import MoEConfig
+
+
+def _align(n: int, a: int = 256) -> int:
+    return (n + a - 1) // a * a
+
+
+def _u16(shape, device):
+    return torch.empty(shape, dtype=torch.int16, device=device)
+
+
+class DeviceModel:
+    def __init__(self, cfg: MoEConfig, device="cuda", heads: bool = True):
+        self.cfg = cfg
+        self.device = torch.device(device)
+        self.blob_bytes = moe.moe_pool_expert_bytes(cfg.d, cfg.F, cfg.bits, cfg.group)
+        if self.blob_bytes == 0:
+            raise ValueError(f"unsupported expert shape {cfg}")
+        self.stride = _align(self.blob_bytes)
+        self.layers = []
+        self._build(heads)
+
+    # -------------------------------------------------------------- tensors
+    def _affine_packed(self, tg: int, rows: int, cols: int, bits: int, sigma: float):
+        dev = self.device
+        q = torch.empty((rows, cols * bits // 32), dtype=torch.int32, device=dev)
+        s = _u16((rows, cols // 64), dev)
+        b = _u16((rows, cols // 64), dev)
+        synth.gpu_affine(self.cfg.seed, tg, rows, cols, bits, sigma, q, s, b)
+        out = torch.empty(_align(moe.moe_packed_matrix_bytes(rows, cols, bits)),
+                          dtype=torch.uint8, device=dev)
+        moe.moe_pack_matrix(q, s, b, rows, cols, bits, out)
+        return out
+
+    def _head_matrix(self, tg: int, rows: int, cols: int):
+        c = self.cfg
+        if c.head_prec == "fp16":
+            return synth.gpu_gauss(c.seed, tg, _u16((rows, cols), self.device), c.sigma_w)
+        return self._affine_packed(tg, rows, cols, 4, c.sigma_w)
+
+    def _f16(self, tg: int, shape, sigma: float):
+        return synth.gpu_gauss(self.cfg.seed, tg, _u16(shape, self.device), sigma)
+
+    def _pool(self, layer: int, experts: list[int]):
+        """Blobs of the given experts, packed; returns a uint8 tensor."""
+        c, dev = self.cfg, self.device
+        n, d, F, bits = len(experts), c.d, c.F, c.bits
+        gq = torch.empty((n, F, d * bits // 32), dtype=torch.int32, device=dev)
+        uq = torch.empty_like(gq)
+        dq = torch.empty((n, d, F * bits // 32), dtype=torch.int32, device=dev)
+        gs, gb, us, ub = (_u16((n, F, d // 64), dev) for _ in range(4))
+        ds, db = (_u16((n, d, F // 64), dev) for _ in range(2))
+        for i, e in enumerate(experts):
+            synth.gpu_affine(c.seed, synth.tag(synth.GATE, layer, e), F, d, bits, c.sigma_w,
+                             gq[i], gs[i], gb[i])
+            synth.gpu_affine(c.seed, synth.tag(synth.UP, layer, e), F, d, bits, c.sigma_w,
+                             uq[i], us[i], ub[i])
+            synth.gpu_affine(c.seed, synth.tag(synth.DOWN, layer, e), d, F, bits, c.sigma_w,
+                             dq[i], ds[i], db[i])
+        pool = torch.empty(n * self.stride, dtype=torch.uint8, device=dev)
+        moe.moe_pack_experts(d, F, n, bits, gq, gs, gb, uq, us, ub, dq, ds, db, pool,
+                             self.stride)
+        return pool
+
+    def _lora(self, layer: int, e: int, ka: int, kb: int, din: int, dout: int):
+        c = self.cfg
+        A = self._f16(synth.tag(ka, layer, e), (c.lora_r, din), c.sigma_lora)
+        B = self._f16(synth.tag(kb, layer, e), (dout, c.lora_r), c.sigma_lora)
+        return A, B
+
+    # -------------------------------------------------------------- build
+    def _build(self, heads: bool):
+        c = self.cfg
+        routers = []
+        for r in range(c.L):
+            routers.append(self._head_matrix(synth.tag(synth.ROUTER, r), c.E, c.d))
+        for r in range(c.L):
+            ly = dict(keep=[])
+            ly["pool"] = self._pool(r, list(range(c.E)))
+            ly["shared"] = self._pool(r, [synth.SHARED_EXPERT]) if c.shared else None
+            ed = moe.ExpertsDesc()
+            ed.d, ed.F, ed.E, ed.bits = c.d, c.F, c.E, c.bits
+            ed.pool = ly["pool"].data_ptr()
+            ed.expert_stride = self.stride
+            ed.shared = ly["shared"].data_ptr() if c.shared else None
+            if c.lora_r and c.lora_on == "routed_down":
+                A = _u16((c.E, c.lora_r, c.F), self.device)
+                B = _u16((c.E, c.d, c.lora_r), self.device)
+                for e in range(c.E):
+                    synth.gpu_gauss(c.seed, synth.tag(synth.LORA_DOWN_A, r, e), A[e], c.sigma_lora)
+                    synth.gpu_gauss(c.seed, synth.tag(synth.LORA_DOWN_B, r, e), B[e], c.sigma_lora)
+                ly["keep"] += [A, B]
+                ed.lora[2] = moe.LoraDesc(c.lora_r, c.lora_scale, A.data_ptr(), B.data_ptr(),
+                                          c.lora_r * c.F, c.d * c.lora_r)
+            if c.lora_r and c.lora_on == "shared_all" and c.shared:
+                S = synth.SHARED_EXPERT
+                for i, (ka, kb, din, dout) in enumerate(
+                        [(synth.LORA_GATE_A, synth.LORA_GATE_B, c.d, c.F),
+                         (synth.LORA_UP_A, synth.LORA_UP_B, c.d, c.F),
+                         (synth.LORA_DOWN_A, synth.LORA_DOWN_B, c.F, c.d)]):
+                    A, B = self._lora(r, S, ka, kb, din, dout)
+                    ly["keep"] += [A, B]
+                    ed.shared_lora[i] = moe.LoraDesc(c.lora_r, c.lora_scale, A.data_ptr(),
+                                                     B.data_ptr(), 0, 0)
+            ly["experts_desc"] = ed
+            prec = moe.MOE_PREC_FP16 if c.head_prec == "fp16" else moe.MOE_PREC_AFFINE4
+            rd = moe.HeadDesc()
+            rd.d, rd.E, rd.H, rd.prec = c.d, c.E, 0, prec
+            rd.lx = routers[r].data_ptr()
+            ly["router_desc"] = rd
+            ly["router"] = routers[r]
+            if heads:
+                tgt = synth.head_target(c, r)
+                hd = moe.HeadDesc()
+                hd.d, hd.E, hd.H, hd.prec = c.d, c.E, c.H, prec
+                t = dict(lx=routers[tgt],
+                         l_tab=self._f16(synth.tag(synth.L_TAB, r), (2 * c.E, c.E), c.sigma_w),
+                         bl=self._f16(synth.tag(synth.BL, r), (c.E,), c.sigma_bias))
+                if c.H:
+                    t.update(fc1x=self._head_matrix(synth.tag(synth.FC1X, r), c.H, c.d),
+                             fc1_tab=self._f16(synth.tag(synth.FC1_TAB, r), (2 * c.E, c.H), c.sigma_w),
+                             b1=self._f16(synth.tag(synth.B1, r), (c.H,), c.sigma_bias),
+                             fc2=self._head_matrix(synth.tag(synth.FC2, r), c.E, c.H),
+                             b2=self._f16(synth.tag(synth.B2, r), (c.E,), c.sigma_bias))
+                for k, v in t.items():
+                    setattr(hd, k, v.data_ptr())
+                ly["head"] = t
+                ly["head_desc"] = hd
+            self.layers.append(ly)
+        torch.cuda.current_stream().synchronize()
+
+    # -------------------------------------------------------------- sizes
+    def head_bytes_per_token(self) -> int:
+        """Bytes one decode token reads in one head call (dense matrices,
+        2K gathered table rows per table, biases)."""
+        c = self.cfg
+        if c.head_prec == "fp16":
+            dense = 2 * (c.H * c.d + c.E * c.H + c.E * c.d)
+        else:
+            dense = (moe.moe_packed_matrix_bytes(c.H, c.d, 4) if c.H else 0) + \
+                (moe.moe_packed_matrix_bytes(c.E, c.H, 4) if c.H else 0) + \
+                moe.moe_packed_matrix_bytes(c.E, c.d, 4)
+        tables = 2 * c.K * 2 * (c.H + c.E)
+        return dense + tables + 2 * (c.H + 2 * c.E)
+
+
+class DecodeStack:
+    """Batch-1 decode over `depth` layers (resident layers cycled)."""
+
+    def __init__(self, model: DeviceModel):
+        self.m = model
+        c = self.cfg = model.cfg
+        dev = model.device
+        D = c.depth
+        f32 = dict(dtype=torch.float32, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.xin = torch.zeros(c.d, **f32)             # the step's input x_0
+        self.xs = torch.zeros((D + 1, c.d), **f32)     # x_N, layer inputs
+        self.stream = torch.zeros(c.d, **f32)          # residual stream
+        self.y = torch.zeros((c.slots, c.d), **f32)
+        self.logits = torch.zeros((D, c.E), **f32)
+        # three rotating route sets: used at t, predicted for t+1, used at t-1
+        self.r_idx = torch.zeros((3, D, c.K), **i32)
+        self.r_w = torch.zeros((3, D, c.K), **f32)
+        self.r_margin = torch.zeros((3, D), **f32)
+        ed = model.layers[0]["experts_desc"]
+        self.ffn_ws = torch.empty(moe.moe_expert_ffn_workspace_bytes(ed, 1, c.K),
+                                  dtype=torch.uint8, device=dev)
+        hd = model.layers[0].get("head_desc", model.layers[0]["router_desc"])
+        self.head_ws = torch.empty(max(256, moe.moe_prerouter_head_workspace_bytes(hd, 1)),
+                                   dtype=torch.uint8, device=dev)
+        self.t = 0
+        self.graphs = {}
+
+    def _layer(self, N: int):
+        return self.m.layers[N % self.cfg.L]
+
+    def _route_own(self, N: int, use: int):
+        c = self.cfg
+        ly = self._layer(N)
+        moe.moe_prerouter_head(ly["router_desc"], self.xs[N], None, None, c.K, 1,
+                               self.logits[N], self.head_ws)
+        moe.moe_topk_route(self.logits[N], 1, c.E, c.K, self.r_idx[use, N], self.r_w[use, N],
+                           self.r_margin[use, N])
+
+    def enqueue_step(self, t: int, ffn_events=None):
+        """Enqueue one decode step (input already in self.xin) for token t.
+        ffn_events: optional per-layer (start, end) CUDA events recorded
+        around each layer's expert FFN call."""
+        c = self.cfg
+        D = c.depth
+        use, nxt, prv = t % 3, (t + 1) % 3, (t - 1) % 3
+        self.xs[0].copy_(self.xin)
+        self.stream.copy_(self.xin)
+        for N in range(D):
+            ly = self._layer(N)
+            own = (N == 0 and not c.self_predict) or t == 0
+            if own:
+                self._route_own(N, use)
+            if ffn_events is not None:
+                ffn_events[N][0].record()
+            moe.moe_expert_ffn_int4(ly["experts_desc"], self.xs[N], self.r_idx[use, N], 1, c.K,
+                                    self.y, self.ffn_ws)
+            if ffn_events is not None:
+                ffn_events[N][1].record()
+            moe.moe_combine_residual(self.y, self.r_w[use, N], 1, c.K, c.shared, c.d,
+                                     self.stream, self.stream, self.xs[N + 1])
+            tgt = N + 1 if N + 1 < D else (0 if c.self_predict else -1)
+            if tgt >= 0:
+                prev = self.r_idx[prv, N] if t > 0 else None
+                moe.moe_prerouter_head(ly["head_desc"], self.xs[N], self.r_idx[use, N], prev,
+                                       c.K, 1, self.logits[N], self.head_ws)
+                moe.moe_topk_route(self.logits[N], 1, c.E, c.K, self.r_idx[nxt, tgt],
+                                   self.r_w[nxt, tgt], self.r_margin[nxt, tgt])
+
+    def step(self, x0: torch.Tensor):
+        """Run step self.t eagerly (or through its captured graph)."""
+        self.xin.copy_(x0)
+        t = self.t
+        g = self.graphs.get(t % 3) if t >= 1 else None
+        if g is not None:
+            g.replay()
+        else:
+            self.enqueue_step(t)
+        self.t += 1
+
+    def capture(self):
+        """Capture the steady-state step (t >= 1) once per route rotation."""
+        for rot in range(3):
+            t = rot if rot >= 1 else 3
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.enqueue_step(t)
+            self.graphs[rot] = g
+
+    def used_routes(self, t: int):
+        """(idx [depth][K], w, margin) the layers used at step t (valid right
+        after step t, before step t+2 overwrites the rotation)."""
+        u = t % 3
+        return self.r_idx[u].clone(), self.r_w[u].clone(), self.r_margin[u].clone()

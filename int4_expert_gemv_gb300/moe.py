@@ -1,0 +1,194 @@
+"""Thin Python binding of the C ABI in include/moe.h (ctypes).
+
+Argument marshalling only: every function forwards device pointers, sizes and
+the current CUDA stream to libmoe.so, which does all of the work.  Tensors are
+PyTorch CUDA tensors (PyTorch supplies device memory and streams); raw integer
+pointers are accepted wherever a tensor is.  A non-zero status raises
+MoEError.  There is no fallback: if libmoe.so is missing the import of the
+library fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe.so")
+
+MOE_OK, MOE_EINVAL, MOE_EUNSUPPORTED, MOE_ECUDA, MOE_ETIMEOUT, MOE_ENOSPACE = range(6)
+MOE_DTYPE_F32, MOE_DTYPE_BF16 = 0, 1
+MOE_PREC_AFFINE4, MOE_PREC_FP16 = 4, 16
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        super().__init__(f"{where}: {status_string(status)}: {detail}")
+        self.status = status
+
+
+# ------------------------------------------------------------------ structs
+class HeadDesc(C.Structure):
+    _fields_ = [("d", C.c_int), ("E", C.c_int), ("H", C.c_int), ("prec", C.c_int),
+                ("fc1x", C.c_void_p), ("fc1_tab", C.c_void_p), ("b1", C.c_void_p),
+                ("fc2", C.c_void_p), ("b2", C.c_void_p),
+                ("lx", C.c_void_p), ("l_tab", C.c_void_p), ("bl", C.c_void_p)]
+
+
+class LoraDesc(C.Structure):
+    _fields_ = [("r", C.c_int), ("scale", C.c_float), ("A", C.c_void_p), ("B", C.c_void_p),
+                ("a_stride", C.c_size_t), ("b_stride", C.c_size_t)]
+
+
+class ExpertsDesc(C.Structure):
+    _fields_ = [("d", C.c_int), ("F", C.c_int), ("E", C.c_int), ("bits", C.c_int),
+                ("pool", C.c_void_p), ("expert_stride", C.c_size_t), ("shared", C.c_void_p),
+                ("lora", LoraDesc * 3), ("shared_lora", LoraDesc * 3)]
+
+
+# ------------------------------------------------------------------ loading
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with "
+                                  "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = C.CDLL(LIB_PATH)
+            P, I, S = C.c_void_p, C.c_int, C.c_size_t
+            sigs = {
+                "moe_status_string": (C.c_char_p, [I]),
+                "moe_last_error": (C.c_char_p, []),
+                "moe_record_bytes": (S, [I, I]),
+                "moe_packed_matrix_bytes": (S, [I, I, I]),
+                "moe_pool_expert_bytes": (S, [I, I, I, I]),
+                "moe_pack_matrix": (I, [P, P, P, I, I, I, P, P]),
+                "moe_pack_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, S, P]),
+                "moe_debug_dequant": (I, [P, I, I, I, I, P, P]),
+                "moe_prerouter_head_workspace_bytes": (S, [C.POINTER(HeadDesc), I]),
+                "moe_prerouter_head": (I, [C.POINTER(HeadDesc), P, I, P, P, I, I, P, P, S, P]),
+                "moe_topk_route": (I, [P, I, I, I, P, P, P, P]),
+                "moe_expert_ffn_workspace_bytes": (S, [C.POINTER(ExpertsDesc), I, I]),
+                "moe_expert_ffn_int4": (I, [C.POINTER(ExpertsDesc), P, I, P, I, I, P, P, S, P]),
+                "moe_combine_residual": (I, [P, P, I, I, I, I, P, P, P, P]),
+            }
+            for name, (res, args) in sigs.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(status).decode()
+
+
+def last_error() -> str:
+    return lib().moe_last_error().decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoEError(rc, where, last_error())
+
+
+def _nbytes(t):
+    return 0 if t is None else (t.numel() * t.element_size() if not isinstance(t, int) else 0)
+
+
+def _dtype_code(x) -> int:
+    import torch
+    if x.dtype == torch.float32:
+        return MOE_DTYPE_F32
+    if x.dtype == torch.bfloat16:
+        return MOE_DTYPE_BF16
+    raise TypeError(f"activations must be float32 or bfloat16, got {x.dtype}")
+
+
+# ------------------------------------------------------------------ sizes
+def moe_record_bytes(cols: int, bits: int) -> int:
+    return lib().moe_record_bytes(cols, bits)
+
+
+def moe_packed_matrix_bytes(rows: int, cols: int, bits: int) -> int:
+    return lib().moe_packed_matrix_bytes(rows, cols, bits)
+
+
+def moe_pool_expert_bytes(d: int, F: int, bits: int, group: int = 64) -> int:
+    return lib().moe_pool_expert_bytes(d, F, bits, group)
+
+
+def moe_prerouter_head_workspace_bytes(hd: HeadDesc, T: int) -> int:
+    return lib().moe_prerouter_head_workspace_bytes(C.byref(hd), T)
+
+
+def moe_expert_ffn_workspace_bytes(ed: ExpertsDesc, T: int, K: int) -> int:
+    return lib().moe_expert_ffn_workspace_bytes(C.byref(ed), T, K)
+
+
+# ------------------------------------------------------------------ calls
+def moe_pack_matrix(q, s, b, rows: int, cols: int, bits: int, out, stream=None):
+    _check(lib().moe_pack_matrix(_ptr(q), _ptr(s), _ptr(b), rows, cols, bits, _ptr(out),
+                                 _stream(stream)), "moe_pack_matrix")
+
+
+def moe_pack_experts(d, F, E, bits, gate_q, gate_s, gate_b, up_q, up_s, up_b, down_q, down_s,
+                     down_b, pool, expert_stride: int, stream=None):
+    _check(lib().moe_pack_experts(d, F, E, bits, _ptr(gate_q), _ptr(gate_s), _ptr(gate_b),
+                                  _ptr(up_q), _ptr(up_s), _ptr(up_b), _ptr(down_q),
+                                  _ptr(down_s), _ptr(down_b), _ptr(pool), expert_stride,
+                                  _stream(stream)), "moe_pack_experts")
+
+
+def moe_debug_dequant(blob, d: int, F: int, bits: int, which: int, out, stream=None):
+    _check(lib().moe_debug_dequant(_ptr(blob), d, F, bits, which, _ptr(out), _stream(stream)),
+           "moe_debug_dequant")
+
+
+def moe_prerouter_head(hd: HeadDesc, x, cur_idx, prev_idx, K: int, T: int, logits, ws,
+                       stream=None, x_dtype: int | None = None):
+    xd = _dtype_code(x) if x_dtype is None else x_dtype
+    _check(lib().moe_prerouter_head(C.byref(hd), _ptr(x), xd, _ptr(cur_idx), _ptr(prev_idx), K,
+                                    T, _ptr(logits), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "moe_prerouter_head")
+
+
+def moe_topk_route(logits, T: int, E: int, K: int, idx, w, margin=None, stream=None):
+    _check(lib().moe_topk_route(_ptr(logits), T, E, K, _ptr(idx), _ptr(w), _ptr(margin),
+                                _stream(stream)), "moe_topk_route")
+
+
+def moe_expert_ffn_int4(ed: ExpertsDesc, x, idx, T: int, K: int, y_slots, ws, stream=None,
+                        x_dtype: int | None = None):
+    xd = _dtype_code(x) if x_dtype is None else x_dtype
+    _check(lib().moe_expert_ffn_int4(C.byref(ed), _ptr(x), xd, _ptr(idx), T, K, _ptr(y_slots),
+                                     _ptr(ws), _nbytes(ws), _stream(stream)),
+           "moe_expert_ffn_int4")
+
+
+def moe_combine_residual(y_slots, w, T: int, K: int, has_shared: bool, d: int, residual, out,
+                         x_next=None, stream=None):
+    _check(lib().moe_combine_residual(_ptr(y_slots), _ptr(w), T, K, int(has_shared), d,
+                                      _ptr(residual), _ptr(out), _ptr(x_next),
+                                      _stream(stream)), "moe_combine_residual")

@@ -205,3 +205,57 @@ def head_host(cfg, layer: int) -> dict:
 def step_input(cfg, step: int) -> np.ndarray:
     """Layer-0 hidden state of decode step `step` (fp32 [T][d], N(0,1))."""
     return gauss(cfg.seed, tag(X_INPUT, step), (cfg.T, cfg.d), 1.0)
+
+
+# ------------------------------------------------------------ GPU twin
+_gpu_lib = None
+
+
+def _gpu():
+    """libmoe_synth.so (csrc/synth.cu), the bit-exact CUDA twin of this module."""
+    global _gpu_lib
+    if _gpu_lib is None:
+        import ctypes as C
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_synth.so")
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: run __graft_entry__.build()")
+        L = C.CDLL(path)
+        L.synth_gauss_f32.argtypes = [C.c_uint64, C.c_uint64, C.c_float, C.c_void_p, C.c_void_p]
+        L.synth_gauss_f16.argtypes = [C.c_uint64, C.c_uint64, C.c_float, C.c_void_p, C.c_void_p]
+        L.synth_affine.argtypes = [C.c_uint64, C.c_int, C.c_int, C.c_int, C.c_float,
+                                   C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
+        for f in (L.synth_gauss_f32, L.synth_gauss_f16, L.synth_affine):
+            f.restype = C.c_int
+        _gpu_lib = L
+    return _gpu_lib
+
+
+def _cur_stream():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def gpu_gauss(seed: int, tg: int, out, sigma: float):
+    """Fill a CUDA tensor (float32, or float16/uint16 for fp16) like gauss()."""
+    import torch
+    n = out.numel()
+    k = stream_key(seed, tg)
+    sc = float(sigma_scale(sigma))
+    if out.dtype == torch.float32:
+        rc = _gpu().synth_gauss_f32(k, n, sc, out.data_ptr(), _cur_stream())
+    else:
+        assert out.element_size() == 2
+        rc = _gpu().synth_gauss_f16(k, n, sc, out.data_ptr(), _cur_stream())
+    if rc:
+        raise RuntimeError(f"synth_gauss failed ({rc})")
+    return out
+
+
+def gpu_affine(seed: int, tg: int, rows: int, cols: int, bits: int, sigma: float, q, s, b):
+    """Fill CUDA tensors q (int32/uint32 [rows][cols*bits/32]), s, b (16-bit
+    [rows][cols/64]) like affine()."""
+    rc = _gpu().synth_affine(stream_key(seed, tg), rows, cols, bits, float(sigma_scale(sigma)),
+                             q.data_ptr(), s.data_ptr(), b.data_ptr(), _cur_stream())
+    if rc:
+        raise RuntimeError(f"synth_affine failed ({rc})")

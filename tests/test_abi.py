@@ -1,0 +1,168 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the header
+declares, sizes its buffers correctly and rejects bad arguments before it
+enqueues anything (these calls never reach the device)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from int4_expert_gemv_gb300 import build as nbuild
+from int4_expert_gemv_gb300.configs import ALL, MOE35B, TINY
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def m():
+    nbuild.build()
+    from int4_expert_gemv_gb300 import moe
+    moe.lib()
+    return moe
+
+
+def _declared(header):
+    text = open(os.path.join(ROOT, "include", header)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(m):
+    names = _declared("moe.h")
+    assert "moe_expert_ffn_int4" in names and "moe_prerouter_head" in names
+    assert len(names) >= 14
+    lib = C.CDLL(m.LIB_PATH)
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(m):
+    assert m.status_string(0) == "MOE_OK"
+    assert m.status_string(1) == "MOE_EINVAL"
+    assert m.status_string(4) == "MOE_ETIMEOUT"
+    assert m.status_string(99) == "MOE_UNKNOWN"
+
+
+def test_pool_expert_bytes_matches_the_page(m):
+    vals = {}
+    for line in open(os.path.join(GOLDEN, "page_values.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            k, v = line.split("=")
+            vals[k.strip()] = float(v)
+    n = m.moe_pool_expert_bytes(int(vals["expert_bytes.d_model"]), int(vals["expert_bytes.ffn"]),
+                                int(vals["expert_bytes.bits"]), int(vals["expert_bytes.group"]))
+    assert n == 7_077_888 == vals["expert_bytes.value_mib"] * 2 ** 20
+
+
+def test_sizes(m):
+    assert m.moe_record_bytes(2048, 4) == 1024 + 128
+    assert m.moe_record_bytes(512, 4) == 256 + 32
+    assert m.moe_record_bytes(128, 4) == 80           # 64 + 8, padded to 16
+    assert m.moe_record_bytes(4096, 2) == 1024 + 256
+    assert m.moe_record_bytes(100, 4) == 0 and m.moe_record_bytes(128, 3) == 0
+    assert m.moe_pool_expert_bytes(2048, 512, 4, 64) == MOE35B.expert_bytes()
+    assert m.moe_pool_expert_bytes(4096, 1024, 2, 64) == ALL["wide-int2"].expert_bytes()
+    assert m.moe_pool_expert_bytes(256, 128, 4, 64) >= TINY.expert_bytes()
+    assert m.moe_pool_expert_bytes(256, 128, 4, 32) == 0
+    assert m.moe_packed_matrix_bytes(3, 2048, 4) == 3 * 1152
+
+
+def _experts_desc(m, **kw):
+    ed = m.ExpertsDesc()
+    ed.d, ed.F, ed.E, ed.bits = 2048, 512, 256, 4
+    ed.pool = 1 << 20
+    ed.expert_stride = m.moe_pool_expert_bytes(2048, 512, 4, 64)
+    for k, v in kw.items():
+        setattr(ed, k, v)
+    return ed
+
+
+def _ffn(m, ed, T=1, K=4, x=1 << 20, idx=1 << 20, y=1 << 20, ws=1 << 20, ws_bytes=1 << 30,
+         x_dtype=0):
+    return m.lib().moe_expert_ffn_int4(C.byref(ed), x, x_dtype, idx, T, K, y, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,call", [
+    (dict(d=2000), {}), (dict(F=500), {}), (dict(bits=3), {}), (dict(E=0), {}),
+    (dict(pool=None), {}), (dict(pool=(1 << 20) + 16), {}), (dict(expert_stride=1024), {}),
+    ({}, dict(K=0)), ({}, dict(K=17)), ({}, dict(T=-1)), ({}, dict(x=None)),
+    ({}, dict(x=(1 << 20) + 4)), ({}, dict(idx=None)), ({}, dict(x_dtype=7)),
+])
+def test_expert_ffn_rejects_bad_arguments(m, kw, call):
+    assert _ffn(m, _experts_desc(m, **kw), **call) == m.MOE_EINVAL
+    assert m.last_error() != ""
+
+
+def test_expert_ffn_rejects_small_workspace(m):
+    ed = _experts_desc(m)
+    need = m.moe_expert_ffn_workspace_bytes(ed, 1, 4)
+    assert need > 0
+    assert _ffn(m, ed, ws_bytes=need - 1) == m.MOE_ENOSPACE
+    assert _ffn(m, ed, ws=None) == m.MOE_ENOSPACE
+
+
+def test_expert_ffn_rejects_bad_lora(m):
+    ed = _experts_desc(m)
+    ed.lora[2] = m.LoraDesc(65, 1.0, 1 << 20, 1 << 20, 0, 0)
+    assert _ffn(m, ed) == m.MOE_EINVAL
+    ed.lora[2] = m.LoraDesc(8, 1.0, None, 1 << 20, 0, 0)
+    assert _ffn(m, ed) == m.MOE_EINVAL
+
+
+def test_empty_batch_is_a_no_op(m):
+    # T == 0 returns before touching any pointer or the device
+    assert _ffn(m, _experts_desc(m), T=0, x=None, idx=None, y=None, ws=None) == m.MOE_OK
+    assert m.lib().moe_topk_route(None, 0, 256, 4, None, None, None, None) == m.MOE_OK
+    assert m.lib().moe_combine_residual(None, None, 0, 4, 1, 2048, None, None, None, None) == m.MOE_OK
+
+
+def _head_desc(m, **kw):
+    hd = m.HeadDesc()
+    hd.d, hd.E, hd.H, hd.prec = 2048, 256, 512, m.MOE_PREC_AFFINE4
+    hd.fc1x = hd.fc2 = hd.lx = 1 << 20
+    for k, v in kw.items():
+        setattr(hd, k, v)
+    return hd
+
+
+@pytest.mark.parametrize("kw", [dict(d=100), dict(E=0), dict(E=2000), dict(H=100),
+                                dict(prec=8), dict(lx=None), dict(fc1x=None), dict(fc2=None)])
+def test_head_rejects_bad_descriptors(m, kw):
+    hd = _head_desc(m, **kw)
+    rc = m.lib().moe_prerouter_head(C.byref(hd), 1 << 20, 0, None, None, 4, 1, 1 << 20,
+                                    1 << 20, 1 << 30, None)
+    assert rc == m.MOE_EINVAL
+
+
+def test_head_workspace_and_k_checks(m):
+    hd = _head_desc(m)
+    need = m.moe_prerouter_head_workspace_bytes(hd, 3)
+    assert need == (3 * 512 * 4 + 255) // 256 * 256 + (3 * 256 * 4 + 255) // 256 * 256
+    rc = m.lib().moe_prerouter_head(C.byref(hd), 1 << 20, 0, None, None, 4, 3, 1 << 20,
+                                    1 << 20, need - 1, None)
+    assert rc == m.MOE_ENOSPACE
+    rc = m.lib().moe_prerouter_head(C.byref(hd), 1 << 20, 0, 1 << 20, None, 0, 3, 1 << 20,
+                                    1 << 20, need, None)
+    assert rc == m.MOE_EINVAL
+
+
+@pytest.mark.parametrize("T,E,K", [(1, 0, 1), (1, 2000, 4), (1, 256, 0), (1, 256, 17), (1, 4, 5)])
+def test_topk_rejects_bad_shapes(m, T, E, K):
+    assert m.lib().moe_topk_route(1 << 20, T, E, K, 1 << 20, 1 << 20, None, None) == m.MOE_EINVAL
+
+
+def test_combine_rejects_bad_arguments(m):
+    L = m.lib()
+    assert L.moe_combine_residual(1 << 20, 1 << 20, 1, 4, 1, 0, 1 << 20, 1 << 20, None, None) == m.MOE_EINVAL
+    assert L.moe_combine_residual(1 << 20, None, 1, 4, 1, 64, 1 << 20, 1 << 20, None, None) == m.MOE_EINVAL
+    assert L.moe_combine_residual(1 << 20, None, 1, 0, 0, 64, 1 << 20, 1 << 20, None, None) == m.MOE_EINVAL
+
+
+def test_pack_rejects_bad_arguments(m):
+    L = m.lib()
+    assert L.moe_pack_matrix(1 << 20, 1 << 20, 1 << 20, 4, 100, 4, 1 << 20, None) == m.MOE_EINVAL
+    assert L.moe_pack_matrix(1 << 20, 1 << 20, 1 << 20, 4, 128, 4, (1 << 20) + 16, None) == m.MOE_EINVAL
+    assert L.moe_pack_experts(2048, 512, 4, 4, *([1 << 20] * 9), 1 << 20, 4096, None) == m.MOE_EINVAL
+    assert L.moe_debug_dequant(1 << 20, 2048, 512, 4, 3, 1 << 20, None) == m.MOE_EINVAL

@@ -1,0 +1,105 @@
+"""Decode-stack parity: the CUDA path (four C-ABI calls per layer, steady-state
+steps replayed from captured CUDA graphs, exactly as bench.py times them)
+against the oracle's stack step, on the full-size configurations.
+
+Routes: compared as index sets per layer wherever the oracle's K-th/(K+1)-th
+logit margin exceeds 1e-4; at nearer ties the oracle adopts the GPU's route
+(teacher forcing) and recomputes its own weights there.  Weights are compared
+per index, outputs as the MoE delta (final stream minus the step input)."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from int4_expert_gemv_gb300 import synth
+from int4_expert_gemv_gb300.configs import ALL, TINY
+from _util import TIE, assert_close, host_expert_from_gpu, zero_expert
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from int4_expert_gemv_gb300 import build
+    build.build()
+
+
+def run_gpu(cfg, steps):
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    dm = DeviceModel(cfg)
+    st = DecodeStack(dm)
+    rec = []
+    for t in range(steps):
+        x0 = torch.from_numpy(synth.step_input(cfg, t)[0]).cuda()
+        st.step(x0)
+        if t == 0:
+            st.capture()
+        idx, w, mg = st.used_routes(t)
+        torch.cuda.synchronize()
+        rec.append(dict(idx=idx.cpu().numpy(), w=w.cpu().double().numpy(),
+                        margin=mg.cpu().double().numpy(), out=st.stream.cpu().double().numpy()))
+    del st, dm
+    torch.cuda.empty_cache()
+    return rec
+
+
+def oracle_layers(cfg, rec):
+    used = {r: set() for r in range(cfg.L)}
+    for r_ in rec:
+        for N in range(cfg.depth):
+            used[N % cfg.L].update(r_["idx"][N].tolist())
+    zero = zero_expert(cfg)
+    res = []
+    for r in range(cfg.L):
+        exps = {e: host_expert_from_gpu(cfg, r, e) for e in sorted(used[r])}
+        res.append(dict(experts=[exps.get(e, zero) for e in range(cfg.E)],
+                        shared=host_expert_from_gpu(cfg, r, synth.SHARED_EXPERT) if cfg.shared else None,
+                        router=synth.router_host(cfg, r), head=synth.head_host(cfg, r)))
+    return [res[N % cfg.L] for N in range(cfg.depth)]
+
+
+def check_stack(cfg, steps):
+    rec = run_gpu(cfg, steps)
+    run = orc.StackRunner(oracle_layers(cfg, rec), cfg.d, cfg.E, cfg.K,
+                          single_layer_self_predict=cfg.self_predict)
+    forced = 0
+    for t, g in enumerate(rec):
+        x0 = synth.step_input(cfg, t)[0].astype(np.float64)
+        r = run.step(x0, ext_idx=g["idx"], tie_margin=TIE)
+        for N in range(cfg.depth):
+            if r["forced"][N]:
+                forced += 1
+                assert r["margin"][N] <= TIE
+                continue
+            assert set(g["idx"][N].tolist()) == set(r["idx"][N].tolist()), (t, N)
+            gw = dict(zip(g["idx"][N].tolist(), g["w"][N]))
+            rw = dict(zip(r["idx"][N].tolist(), r["w"][N]))
+            keys = sorted(rw)
+            assert_close([gw[k] for k in keys], [rw[k] for k in keys], f"weights t{t} N{N}")
+        assert_close(g["out"] - x0, r["out"] - x0, f"{cfg.name} step {t} output delta")
+    return forced
+
+
+def test_tiny_stack_all_steps():
+    forced = check_stack(TINY, TINY.steps)
+    assert forced <= TINY.steps // 8           # near-ties are rare
+
+
+def test_35b_stack_full_size():
+    check_stack(ALL["35b"], 4)
+
+
+def test_8b_stack_full_size():
+    check_stack(ALL["8b"], 2)
+
+
+@pytest.mark.parametrize("name", ["wide-int4", "wide-int2"])
+def test_wide_stack_full_size(name):
+    check_stack(ALL[name], 2)
+
+
+def test_k_sweep_stack():
+    for K in (2, 8):
+        check_stack(replace(ALL[f"35b-K{K}"], L=4, depth=4), 3)
