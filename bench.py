@@ -233,10 +233,12 @@ def run_native(args, cfg):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     with ClockSampler(local) as clk:
+        torch.cuda.nvtx.range_push("timed")
         start.record(stream)
         for t in range(args.warmup, total):
             st.step(xin[t])
         stop.record(stream)
+        torch.cuda.nvtx.range_pop()
         barrier()
     ms = start.elapsed_time(stop)
     if world > 1:
@@ -252,7 +254,9 @@ def run_native(args, cfg):
     inst = {}
     for rot in range(3):
         g = torch.cuda.CUDAGraph()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        # external events become timing record nodes inside the graph
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
                for _ in range(cfg.depth)]
         with torch.cuda.graph(g):
             st.enqueue_step(rot if rot else 3, ffn_events=evs)
