@@ -213,6 +213,34 @@ int moe_expert_ffn_int4(const moe_experts_desc *ed, const void *x, int x_dtype,
                         const int32_t *idx, int T, int K, float *y_slots,
                         void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Bytes of the static device scratch behind moe_expert_ffn_int4_noalloc. */
+#define MOE_FFN_STATIC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/* moe_expert_ffn_int4 without a workspace argument.  The pages have no
+ * counterpart to this call; it exists for callers that are handed only their
+ * input and output buffers and cannot allocate device memory or carve a
+ * workspace -- for example a plugin or custom operator hosted by a framework
+ * that owns the device allocator, or a fixed-budget real-time loop that
+ * forbids allocation once it has started.
+ *
+ * Arguments and results are those of moe_expert_ffn_int4.  The scratch the
+ * call needs comes from one fixed array of MOE_FFN_STATIC_SCRATCH_BYTES
+ * (4 MiB) in the library's device memory, which every GPU that loads the
+ * library holds until the process exits.  Calls whose scratch need
+ * (moe_expert_ffn_workspace_bytes(ed, T, K)) exceeds it return MOE_ENOSPACE.
+ * The call allocates and frees nothing.
+ *
+ * The first call on a device (with that device current) looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture on the device.  All calls on a device share the
+ * one array, which keeps the last call's contents: calls that may overlap on
+ * the GPU (e.g. issued on different streams without ordering) race with each
+ * other and must be serialised by the caller.  No scratch needs clearing
+ * between calls. */
+int moe_expert_ffn_int4_noalloc(const moe_experts_desc *ed, const void *x,
+                                int x_dtype, const int32_t *idx, int T, int K,
+                                float *y_slots, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- combine */
 /* out[t] = residual[t] + sum_k w[t][k] * y_slots[t][k] (+ y_slots[t][K] if
  * has_shared), all fp32, y_slots [T][K + has_shared][d].  If x_next is not

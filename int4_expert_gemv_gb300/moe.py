@@ -74,6 +74,7 @@ def lib():
                 "moe_expert_ffn_workspace_bytes": (S, [C.POINTER(ExpertsDesc), I, I]),
                 "moe_expert_ffn_int4": (I, [C.POINTER(ExpertsDesc), P, I, P, I, I, P, P, S, P]),
                 "moe_combine_residual": (I, [P, P, I, I, I, I, P, P, P, P]),
+                "moe_expert_ffn_int4_noalloc": (I, [C.POINTER(ExpertsDesc), P, I, P, I, I, P, P]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -192,3 +193,16 @@ def moe_combine_residual(y_slots, w, T: int, K: int, has_shared: bool, d: int, r
     _check(lib().moe_combine_residual(_ptr(y_slots), _ptr(w), T, K, int(has_shared), d,
                                       _ptr(residual), _ptr(out), _ptr(x_next),
                                       _stream(stream)), "moe_combine_residual")
+
+
+MOE_FFN_STATIC_SCRATCH_BYTES = 4 << 20
+
+
+def moe_expert_ffn_int4_noalloc(ed: ExpertsDesc, x, idx, T: int, K: int, y_slots, stream=None,
+                                x_dtype: int | None = None):
+    """moe_expert_ffn_int4 for callers that cannot allocate: the library's
+    fixed static device scratch stands in for the workspace."""
+    xd = _dtype_code(x) if x_dtype is None else x_dtype
+    _check(lib().moe_expert_ffn_int4_noalloc(C.byref(ed), _ptr(x), xd, _ptr(idx), T, K,
+                                             _ptr(y_slots), _stream(stream)),
+           "moe_expert_ffn_int4_noalloc")
