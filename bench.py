@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--cpu-layers", type=int, default=40,
                     help="layer samples the oracle baseline times (native arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="fused", choices=["fused", "per-call"],
+                    help="fused: one persistent kernel per step; per-call: the four calls per layer")
     return ap.parse_args()
 
 
@@ -181,6 +183,8 @@ def run_reference(args, cfg):
 def kernels_per_step(cfg, stack) -> int:
     """Kernel launches of one steady-state step (counted from the calls the
     driver makes; the kernels per call are fixed by the library)."""
+    if stack.fused:
+        return 1
     ed = stack.m.layers[0]["experts_desc"]
     gu_lora = any(ed.lora[i].r for i in range(2)) or any(ed.shared_lora[i].r for i in range(2))
     ffn = 2 + (1 if gu_lora else 0)
@@ -212,7 +216,7 @@ def run_native(args, cfg):
     __graft_entry__.build()
 
     dm = DeviceModel(cfg)
-    st = DecodeStack(dm)
+    st = DecodeStack(dm, fused=args.path == "fused")
     total = args.warmup + args.steps
     xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
                                        (total + 64, cfg.d), 1.0)).cuda()
@@ -248,20 +252,23 @@ def run_native(args, cfg):
     tok_s = world * args.steps / (ms / 1000.0)
     ms_step = ms / args.steps
 
-    # ---- per-call kernel durations (instrumented replay of further steps)
-    ev = []
+    # ---- per-launch durations of the dominant kernel (instrumented replay of
+    # further steps; external events become timing nodes inside the graph)
     t_next = total
     inst = {}
     for rot in range(3):
         g = torch.cuda.CUDAGraph()
-        # external events become timing record nodes inside the graph
+        n_ev = 1 if st.fused else cfg.depth
         evs = [(torch.cuda.Event(enable_timing=True, external=True),
                 torch.cuda.Event(enable_timing=True, external=True))
-               for _ in range(cfg.depth)]
+               for _ in range(n_ev)]
         with torch.cuda.graph(g):
-            st.enqueue_step(rot if rot else 3, ffn_events=evs)
+            if st.fused:
+                st.enqueue_fused_step(rot if rot else 3, events=evs[0])
+            else:
+                st.enqueue_step(rot if rot else 3, ffn_events=evs)
         inst[rot] = (g, evs)
-    ffn_ms = []
+    launch_ms = []
     n_inst = min(args.steps, 48)
     for i in range(n_inst):
         t = t_next + i
@@ -269,10 +276,12 @@ def run_native(args, cfg):
         g, evs = inst[t % 3]
         g.replay()
         torch.cuda.synchronize()
-        ffn_ms += [a.elapsed_time(b) for a, b in evs]
+        launch_ms += [a.elapsed_time(b) for a, b in evs]
     st.t = t_next + n_inst
-    ffn_avg_ms = statistics.mean(ffn_ms)
-    ffn_bytes = cfg.expert_bytes_per_layer()
+    launch_avg_ms = statistics.mean(launch_ms)
+    # algorithmic bytes of one launch: the experts a launch reads
+    unit_layers = cfg.depth if st.fused else 1
+    launch_bytes = cfg.expert_bytes_per_layer() * unit_layers
 
     # ---- end to end: host input -> device, step, result -> host, per step
     pin_in = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 1),
@@ -297,9 +306,12 @@ def run_native(args, cfg):
 
     if rank == 0:
         hbm, hbm_kind = peaks()
+        ffn_bytes = cfg.expert_bytes_per_layer()
         expert_gbs = ffn_bytes * cfg.depth / (ms_step / 1000.0) / 1e9
-        achieved = ffn_bytes / (ffn_avg_ms / 1000.0) / 1e9
+        achieved = launch_bytes / (launch_avg_ms / 1000.0) / 1e9
         head_bytes = dm.head_bytes_per_token()
+        kname = ("decode_step_kernel (whole step: experts, combine, heads, top-K)" if st.fused
+                 else "moe_expert_ffn_int4 (gate/up+SwiGLU, down)")
         line = {
             "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -314,13 +326,16 @@ def run_native(args, cfg):
                 "l2": f"no flush: each step reads {cfg.depth * (ffn_bytes + head_bytes) / 1e6:.0f} MB "
                       f"of weights (> {L2_BYTES / 1e6:.0f} MB L2); routed experts change every step",
                 "graphs": "steady-state steps replayed from captured CUDA graphs",
+                "path": args.path,
             },
+            "total_weight_gbs": (ffn_bytes + head_bytes) * cfg.depth / (ms_step / 1000.0) / 1e9,
             "expert_weight_gbs": expert_gbs,
             "expert_weight_frac_of_hbm": expert_gbs / hbm,
-            "roofline": {"bound": "hbm", "kernel": "moe_expert_ffn_int4 (gate/up+SwiGLU, down)",
+            "roofline": {"bound": "hbm", "kernel": kname,
                          "achieved": achieved, "peak": hbm, "peak_kind": hbm_kind,
                          "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
-                         "bytes_per_launch": ffn_bytes, "avg_launch_us": ffn_avg_ms * 1000.0,
+                         "bytes_per_launch": launch_bytes,
+                         "avg_launch_us": launch_avg_ms * 1000.0,
                          "timing": f"CUDA events around each layer's call in {n_inst} "
                                    f"instrumented graph replays after the timed region"},
             "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "tokens/s",

@@ -250,6 +250,58 @@ int moe_combine_residual(const float *y_slots, const float *w, int T, int K,
                          int has_shared, int d, const float *residual,
                          float *out, float *x_next, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- stack */
+/* A decode stack: depth layers per step, layer N using resident layer
+ * N % n_layers (all of one shape).  Layer 0 routes with its own router every
+ * step (unless self_predict); layer N >= 1 uses the route head N-1 predicted
+ * at the previous step; head N (N < depth-1) runs on layer N's input with the
+ * K-hot routes of layer N at this and the previous step and predicts layer
+ * N+1's route for the next step.  self_predict (depth 1 only): the single
+ * layer's head predicts its own next route and the layer routes with it. */
+typedef struct {
+    const moe_experts_desc *experts;  /* [n_layers]                            */
+    const moe_head_desc *routers;     /* [n_layers] H == 0 heads (l = router)  */
+    const moe_head_desc *heads;       /* [n_layers] int4 heads, or NULL when no
+                                         head runs (depth 1, no self_predict)  */
+    int n_layers;                     /* resident layers (<= 48)               */
+    int depth;                        /* layers per decode step (<= 48)        */
+    int K;                            /* experts per token (<= 16)             */
+    int self_predict;
+    unsigned long long timeout_ns;    /* bound of every device-side wait;
+                                         0 = 1 second                          */
+    int debug_unset_wait;             /* test hook: 1 makes the kernel wait on
+                                         a flag nothing sets (-> MOE_ETIMEOUT) */
+} moe_stack_desc;
+
+/* Workspace bytes of moe_decode_step; 0 if the descriptor is invalid. */
+size_t moe_decode_step_workspace_bytes(const moe_stack_desc *sd);
+
+/* One decode step (token t >= 1) of the whole stack in one persistent kernel
+ * (one CTA per SM, cooperative launch): per layer the expert FFN, combine +
+ * residual + RMS, the prerouter head and its top-K -- the same operations as
+ * the four calls above, fused across layers.
+ * x0: fp32 [d] layer-0 input (also its residual); out: fp32 [d] final
+ * residual stream.  Route state (caller-owned, device): route_idx int32
+ * [3][depth][K], route_w fp32 [3][depth][K], route_margin fp32 [3][depth],
+ * rotating by t % 3: set t % 3 holds the routes used at t (written by the
+ * previous step, or by this one for layer 0's own route), set (t+1) % 3
+ * receives the predictions for t+1, set (t+2) % 3 holds the routes of t-1 (the
+ * "previous token" K-hot input of the heads).  Step 0 (every layer routing
+ * with its own router) is run with the per-call functions.
+ * ws: moe_decode_step_workspace_bytes() bytes, 256-byte aligned, ZEROED before
+ * the first call (never again, unless a call reports an error).  Device-side
+ * waits are bounded; a step that timed out or found a bad route records the
+ * status in the workspace (read it with moe_decode_step_status) and every
+ * later step on that workspace returns immediately until it is zeroed. */
+int moe_decode_step(const moe_stack_desc *sd, const float *x0, float *out,
+                    int32_t *route_idx, float *route_w, float *route_margin,
+                    int t, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Reads the status word of a decode-step workspace into *status (host):
+ * MOE_OK, MOE_ETIMEOUT (a bounded wait expired) or MOE_EINVAL (a route index
+ * out of range).  Synchronises `stream`. */
+int moe_decode_step_status(const void *ws, int *status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -170,9 +170,13 @@ class DeviceModel:
 
 
 class DecodeStack:
-    """Batch-1 decode over `depth` layers (resident layers cycled)."""
+    """Batch-1 decode over `depth` layers (resident layers cycled).
 
-    def __init__(self, model: DeviceModel):
+    fused=True runs steady-state steps (t >= 1) as one persistent kernel
+    (moe_decode_step); step 0, where every layer routes with its own router,
+    always runs through the four per-layer calls."""
+
+    def __init__(self, model: DeviceModel, fused: bool = False):
         self.m = model
         c = self.cfg = model.cfg
         dev = model.device
@@ -196,6 +200,18 @@ class DecodeStack:
                                    dtype=torch.uint8, device=dev)
         self.t = 0
         self.graphs = {}
+        self.fused = fused
+        if fused:
+            L = model.layers
+            self._ed = (moe.ExpertsDesc * c.L)(*[ly["experts_desc"] for ly in L])
+            self._rd = (moe.HeadDesc * c.L)(*[ly["router_desc"] for ly in L])
+            has_heads = all("head_desc" in ly for ly in L)
+            self._hd = (moe.HeadDesc * c.L)(*[ly["head_desc"] for ly in L]) if has_heads else None
+            self.sd = moe.StackDesc(C.cast(self._ed, C.c_void_p), C.cast(self._rd, C.c_void_p),
+                                    C.cast(self._hd, C.c_void_p) if has_heads else None,
+                                    c.L, c.depth, c.K, int(c.self_predict), 0, 0)
+            self.step_ws = torch.zeros(moe.moe_decode_step_workspace_bytes(self.sd),
+                                       dtype=torch.uint8, device=dev)
 
     def _layer(self, N: int):
         return self.m.layers[N % self.cfg.L]
@@ -207,6 +223,19 @@ class DecodeStack:
                                self.logits[N], self.head_ws)
         moe.moe_topk_route(self.logits[N], 1, c.E, c.K, self.r_idx[use, N], self.r_w[use, N],
                            self.r_margin[use, N])
+
+    def enqueue_fused_step(self, t: int, events=None):
+        """Enqueue step t >= 1 as one moe_decode_step launch."""
+        if events is not None:
+            events[0].record()
+        moe.moe_decode_step(self.sd, self.xin, self.stream, self.r_idx, self.r_w, self.r_margin,
+                            t, self.step_ws)
+        if events is not None:
+            events[1].record()
+
+    def status(self) -> int:
+        """Status word of the fused step's workspace (synchronises)."""
+        return moe.moe_decode_step_status(self.step_ws)
 
     def enqueue_step(self, t: int, ffn_events=None):
         """Enqueue one decode step (input already in self.xin) for token t.
@@ -245,6 +274,8 @@ class DecodeStack:
         g = self.graphs.get(t % 3) if t >= 1 else None
         if g is not None:
             g.replay()
+        elif self.fused and t >= 1:
+            self.enqueue_fused_step(t)
         else:
             self.enqueue_step(t)
         self.t += 1
@@ -255,7 +286,10 @@ class DecodeStack:
             t = rot if rot >= 1 else 3
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                self.enqueue_step(t)
+                if self.fused:
+                    self.enqueue_fused_step(t)
+                else:
+                    self.enqueue_step(t)
             self.graphs[rot] = g
 
     def used_routes(self, t: int):

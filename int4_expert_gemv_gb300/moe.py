@@ -49,6 +49,13 @@ class ExpertsDesc(C.Structure):
                 ("lora", LoraDesc * 3), ("shared_lora", LoraDesc * 3)]
 
 
+class StackDesc(C.Structure):
+    _fields_ = [("experts", C.c_void_p), ("routers", C.c_void_p), ("heads", C.c_void_p),
+                ("n_layers", C.c_int), ("depth", C.c_int), ("K", C.c_int),
+                ("self_predict", C.c_int), ("timeout_ns", C.c_ulonglong),
+                ("debug_unset_wait", C.c_int)]
+
+
 # ------------------------------------------------------------------ loading
 def lib():
     global _lib
@@ -75,6 +82,9 @@ def lib():
                 "moe_expert_ffn_int4": (I, [C.POINTER(ExpertsDesc), P, I, P, I, I, P, P, S, P]),
                 "moe_combine_residual": (I, [P, P, I, I, I, I, P, P, P, P]),
                 "moe_expert_ffn_int4_noalloc": (I, [C.POINTER(ExpertsDesc), P, I, P, I, I, P, P]),
+                "moe_decode_step_workspace_bytes": (S, [C.POINTER(StackDesc)]),
+                "moe_decode_step": (I, [C.POINTER(StackDesc), P, P, P, P, P, I, P, S, P]),
+                "moe_decode_step_status": (I, [P, C.POINTER(C.c_int), P]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -206,3 +216,22 @@ def moe_expert_ffn_int4_noalloc(ed: ExpertsDesc, x, idx, T: int, K: int, y_slots
     _check(lib().moe_expert_ffn_int4_noalloc(C.byref(ed), _ptr(x), xd, _ptr(idx), T, K,
                                              _ptr(y_slots), _stream(stream)),
            "moe_expert_ffn_int4_noalloc")
+
+
+# ------------------------------------------------------------------ stack
+def moe_decode_step_workspace_bytes(sd: StackDesc) -> int:
+    return lib().moe_decode_step_workspace_bytes(C.byref(sd))
+
+
+def moe_decode_step(sd: StackDesc, x0, out, route_idx, route_w, route_margin, t: int, ws,
+                    stream=None):
+    _check(lib().moe_decode_step(C.byref(sd), _ptr(x0), _ptr(out), _ptr(route_idx),
+                                 _ptr(route_w), _ptr(route_margin), t, _ptr(ws), _nbytes(ws),
+                                 _stream(stream)), "moe_decode_step")
+
+
+def moe_decode_step_status(ws, stream=None) -> int:
+    st = C.c_int(0)
+    _check(lib().moe_decode_step_status(_ptr(ws), C.byref(st), _stream(stream)),
+           "moe_decode_step_status")
+    return st.value

@@ -26,10 +26,10 @@ def built():
     build.build()
 
 
-def run_gpu(cfg, steps):
+def run_gpu(cfg, steps, fused=False):
     from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
     dm = DeviceModel(cfg)
-    st = DecodeStack(dm)
+    st = DecodeStack(dm, fused=fused)
     rec = []
     for t in range(steps):
         x0 = torch.from_numpy(synth.step_input(cfg, t)[0]).cuda()
@@ -40,6 +40,8 @@ def run_gpu(cfg, steps):
         torch.cuda.synchronize()
         rec.append(dict(idx=idx.cpu().numpy(), w=w.cpu().double().numpy(),
                         margin=mg.cpu().double().numpy(), out=st.stream.cpu().double().numpy()))
+    if fused:
+        assert st.status() == 0
     del st, dm
     torch.cuda.empty_cache()
     return rec
@@ -60,8 +62,8 @@ def oracle_layers(cfg, rec):
     return [res[N % cfg.L] for N in range(cfg.depth)]
 
 
-def check_stack(cfg, steps):
-    rec = run_gpu(cfg, steps)
+def check_stack(cfg, steps, fused=False):
+    rec = run_gpu(cfg, steps, fused)
     run = orc.StackRunner(oracle_layers(cfg, rec), cfg.d, cfg.E, cfg.K,
                           single_layer_self_predict=cfg.self_predict)
     forced = 0
@@ -82,24 +84,55 @@ def check_stack(cfg, steps):
     return forced
 
 
-def test_tiny_stack_all_steps():
-    forced = check_stack(TINY, TINY.steps)
+PATHS = [pytest.param(False, id="per-call"), pytest.param(True, id="fused")]
+
+
+@pytest.mark.parametrize("fused", PATHS)
+def test_tiny_stack_all_steps(fused):
+    forced = check_stack(TINY, TINY.steps, fused)
     assert forced <= TINY.steps // 8           # near-ties are rare
 
 
-def test_35b_stack_full_size():
-    check_stack(ALL["35b"], 4)
+@pytest.mark.parametrize("fused", PATHS)
+def test_35b_stack_full_size(fused):
+    check_stack(ALL["35b"], 4, fused)
 
 
-def test_8b_stack_full_size():
-    check_stack(ALL["8b"], 2)
+@pytest.mark.parametrize("fused", PATHS)
+def test_8b_stack_full_size(fused):
+    check_stack(ALL["8b"], 2, fused)
 
 
+@pytest.mark.parametrize("fused", PATHS)
 @pytest.mark.parametrize("name", ["wide-int4", "wide-int2"])
-def test_wide_stack_full_size(name):
-    check_stack(ALL[name], 2)
+def test_wide_stack_full_size(name, fused):
+    check_stack(ALL[name], 2, fused)
 
 
-def test_k_sweep_stack():
+@pytest.mark.parametrize("fused", PATHS)
+def test_k_sweep_stack(fused):
     for K in (2, 8):
-        check_stack(replace(ALL[f"35b-K{K}"], L=4, depth=4), 3)
+        check_stack(replace(ALL[f"35b-K{K}"], L=4, depth=4), 3, fused)
+
+
+def test_fused_bounded_wait_times_out_and_recovers():
+    """A wait on a flag nothing sets runs out after its short limit; the kernel
+    records MOE_ETIMEOUT and returns, the context stays usable, and a zeroed
+    workspace runs the next step normally."""
+    from int4_expert_gemv_gb300 import moe
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    cfg = TINY
+    st = DecodeStack(DeviceModel(cfg), fused=True)
+    st.step(torch.from_numpy(synth.step_input(cfg, 0)[0]).cuda())       # step 0: per-call
+    st.sd.timeout_ns = 50_000_000
+    st.sd.debug_unset_wait = 1
+    st.step(torch.from_numpy(synth.step_input(cfg, 1)[0]).cuda())
+    assert st.status() == moe.MOE_ETIMEOUT
+    torch.cuda.synchronize()                                               # context alive
+    st.sd.debug_unset_wait = 0
+    st.sd.timeout_ns = 0
+    st.step_ws.zero_()
+    st.t = 1
+    st.step(torch.from_numpy(synth.step_input(cfg, 1)[0]).cuda())
+    assert st.status() == moe.MOE_OK
+    assert torch.isfinite(st.stream).all()
