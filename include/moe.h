@@ -271,6 +271,10 @@ typedef struct {
                                          0 = 1 second                          */
     int debug_unset_wait;             /* test hook: 1 makes the kernel wait on
                                          a flag nothing sets (-> MOE_ETIMEOUT) */
+    unsigned long long *debug_trace;  /* profiling hook: NULL, or a device
+                                         buffer of n_SM * depth * 12 u64 that
+                                         receives %globaltimer stamps per CTA
+                                         and layer at phase boundaries        */
 } moe_stack_desc;
 
 /* Workspace bytes of moe_decode_step; 0 if the descriptor is invalid. */

@@ -79,107 +79,141 @@ __device__ __forceinline__ int ld_flag(const int *p) {
 }
 
 // ---------------------------------------------------------------- dequant dot
-// x is kept pre-scaled and transposed in shared memory so that codes can be
-// turned into floats without shifts: a code n at bit offset 4j (or 2j) of a
-// word, OR-ed into the mantissa of 2^23, is the float 2^23 + n*16^j (4^j);
-// subtracting 2^23 is exact, and multiplying by x*16^-j (4^-j) gives n*x with
-// one rounding, the same as n*x.  Codes are handled in pairs with the paired
-// fp32 instructions of sm_100+.
+// Integer dot products.  A vector x (x, h or gelu(a)) is staged per 16-byte
+// code chunk c (VALS = 128/BITS values) as 16-bit fixed point with one
+// power-of-two scale: xf = rint(x * 2^(15-e)), e the exponent of the chunk's
+// largest |x| (2^(e-1) <= max < 2^e), clamped to [-32767, 32767]; xf is split
+// into a signed high byte and an unsigned low byte (xf = 256 hi + lo).  A
+// packed code word is cut into byte vectors of 4 codes with one mask (and a
+// shift), and dp4a accumulates sum(code * hi) and sum(code * lo) exactly in
+// int32.  The chunk's sum(code * xf) = 256 HI + LO is below 2^24, so its float
+// and the product with 2^(e-15) are exact: the chunk dot is exactly
+// codes . x^ with |x - x^| <= 2^(e-16) <= max|x| * 2^-15.
 //
-// Pre-scaled layout of one vector of n floats split in 16-byte chunks c of
-// VALS = 128/BITS codes: float4 group q (0 .. VALS/4-1) of chunk c sits at
-// float4 index q*nch + c (nch = n / VALS), so the lanes of a warp, each on its
-// own chunk, read consecutive 16-byte words (no bank conflicts).
-//   int4: word i (0..3), pair slot jj (0..1):  float4 q = 2i + jj holds
-//         (x[8i+2jj]*16^-2jj, x[8i+2jj+4]*16^-2jj,
-//          x[8i+2jj+1]*16^-(2jj+1), x[8i+2jj+5]*16^-(2jj+1)).
-//   int2: word i (0..3), pair slot jj (0..3):  float4 q = 4i + jj holds
-//         (x[16i+2jj]*4^-2jj, x[16i+2jj+8]*4^-2jj,
-//          x[16i+2jj+1]*4^-(2jj+1), x[16i+2jj+9]*4^-(2jj+1)).
+// Layout of one staged vector (nch chunks): the 4-code byte vectors of word i
+// of a chunk are, for int4, A = positions 8i+{0,2,4,6} and B = 8i+{1,3,5,7};
+// for int2, group g (0..3) = positions 16i + 4b + g (b = 0..3).  Their
+// (hi, lo) words sit in uint4 slot k of chunk c at uint4 index k*nch + c
+// (k = i for int4 as (A_hi, A_lo, B_hi, B_lo); k = 2i + g/2 for int2 as
+// (G_hi, G_lo, G'_hi, G'_lo)), so lanes on consecutive chunks read consecutive
+// 16-byte words.  Per chunk also: scale 2^(e-15) and xhat = sum(x^).
 
-// float index of vector position `pos` in the pre-scaled layout
 template <int BITS>
-__device__ __forceinline__ int ps_index(int pos, int nch) {
-    constexpr int VALS = 128 / BITS;
-    const int c = pos / VALS, r = pos % VALS;
+struct Fix {
+    static constexpr int VALS = 128 / BITS;          // values per chunk
+    static constexpr int SLOTS = BITS == 4 ? 4 : 8;  // uint4 per chunk
+};
+
+// uint4 slot and byte offset (within the uint4) of position pos of a chunk,
+// for the high byte (the low byte is 4 bytes further).
+template <int BITS>
+__device__ __forceinline__ void fix_place(int pos, int &slot, int &byte) {
     if (BITS == 4) {
-        const int i = r / 8, p = r % 8;          // word, position in word
-        const int j = p & 3, hi = p >> 2;        // pair index j, second of pair
-        const int q = 2 * i + (j >> 1);
-        const int lane = (j & 1) * 2 + hi;       // (j even: x,y) (j odd: z,w)
-        return (q * nch + c) * 4 + lane;
+        const int i = pos >> 3, p = pos & 7;
+        slot = i;
+        byte = ((p & 1) ? 8 : 0) + (p >> 1);
     } else {
-        const int i = r / 16, p = r % 16;
-        const int j = p & 7, hi = p >> 3;
-        const int q = 4 * i + (j >> 1);
-        const int lane = (j & 1) * 2 + hi;
-        return (q * nch + c) * 4 + lane;
+        const int i = pos >> 4, p = pos & 15, g = p & 3, b = p >> 2;
+        slot = 2 * i + (g >> 1);
+        byte = ((g & 1) ? 8 : 0) + b;
     }
 }
 
+// Stages one chunk whose values are spread over the 32 lanes of a warp
+// (lane j holds positions j and, for int2, j + 32): writes the fixed-point
+// bytes into xf (uint4 array, chunk c of nch), the scale and xhat.
 template <int BITS>
-__device__ __forceinline__ float ps_scale(int pos) {
-    if (BITS == 4) return __uint_as_float((uint32_t)(127 - 4 * (pos % 8 & 3)) << 23);
-    return __uint_as_float((uint32_t)(127 - 2 * (pos % 16 & 7)) << 23);
+__device__ __forceinline__ void stage_chunk(const float *v, int lane, uint8_t *xf, int c, int nch,
+                                            float *scale, float *xhat) {
+    constexpr int PER = Fix<BITS>::VALS / 32;
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < PER; k++) m = fmaxf(m, fabsf(v[k]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    // e: 2^(e-1) <= m < 2^e; f = 2^(15-e) exactly
+    int e = 0;
+    if ((__float_as_uint(m) >> 23) == 0) m = 0.0f;          // zero or subnormal: treat as zero
+    if (m > 0.0f) e = (int)((__float_as_uint(m) >> 23) & 0xff) - 126;
+    const float f = m > 0.0f ? __uint_as_float((uint32_t)(127 + 15 - e) << 23) : 0.0f;
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < PER; k++) {
+        int q = (int)rintf(v[k] * f);
+        q = max(-32767, min(32767, q));
+        sum += q;
+        const int pos = lane + 32 * k;
+        int slot, byte;
+        fix_place<BITS>(pos, slot, byte);
+        uint8_t *w = xf + ((size_t)slot * nch + c) * 16;
+        w[byte] = (uint8_t)((q >> 8) & 0xff);
+        w[byte + 4] = (uint8_t)(q & 0xff);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane == 0) {
+        const float sc = m > 0.0f ? __uint_as_float((uint32_t)(127 + e - 15) << 23) : 0.0f;
+        scale[c] = sc;
+        xhat[c] = (float)sum * sc;
+    }
 }
 
-__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
-    return ((uint64_t)hi << 32) | lo;
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-    uint64_t r;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
 }
 
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
-
-__device__ __forceinline__ float f2_sum(uint64_t a) {
-    return __uint_as_float((uint32_t)a) + __uint_as_float((uint32_t)(a >> 32));
-}
-
-constexpr uint32_t kMagic = 0x4B000000u;                       // 2^23
-constexpr uint64_t kMagic2 = 0x4B0000004B000000ull;
-
-// Accumulates the dot products of two code chunks (two rows) with one
-// pre-scaled x chunk: acc0 += codes(q0) . x, acc1 += codes(q1) . x.
-// xq: float4 pointer to group 0 of this chunk; groups are nch apart.
+// Exact codes . x^ of NR code chunks (NR rows) against one staged chunk:
+// out[r] = (256 HI + LO) without the chunk scale.  xq: uint4 array of the
+// staged vector, indexed slot*nch + c (this lane's chunk c).
 template <int BITS, int NR>
-__device__ __forceinline__ void chunk_dot_ps(const uint4 *q, const float4 *xq, int nch,
-                                             uint64_t *acc) {
-    constexpr int PAIRS = BITS == 4 ? 4 : 8;           // pairs per word
-    constexpr uint32_t M = (1u << BITS) - 1u;
+__device__ __forceinline__ void chunk_dot_fix(const uint4 *q, const uint4 *xq, int nch, int c,
+                                              int *out) {
+    int hi[NR], lo[NR];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        uint32_t w[NR], wh[NR];
+    for (int r = 0; r < NR; r++) hi[r] = lo[r] = 0;
+    if (BITS == 4) {
 #pragma unroll
-        for (int r = 0; r < NR; r++) {
-            const uint32_t *qq = reinterpret_cast<const uint32_t *>(&q[r]);
-            w[r] = qq[i];
-            wh[r] = qq[i] >> 16;
-        }
-#pragma unroll
-        for (int jj = 0; jj < PAIRS / 2; jj++) {
-            const float4 xv = xq[(size_t)(i * (PAIRS / 2) + jj) * nch];
-            const uint64_t x0 = pack2(__float_as_uint(xv.x), __float_as_uint(xv.y));
-            const uint64_t x1 = pack2(__float_as_uint(xv.z), __float_as_uint(xv.w));
-            const int j0 = 2 * jj, j1 = 2 * jj + 1;
+        for (int i = 0; i < 4; i++) {
+            const uint4 xv = xq[i * nch + c];
 #pragma unroll
             for (int r = 0; r < NR; r++) {
-                const uint64_t c0 = pack2((w[r] & (M << (BITS * j0))) | kMagic,
-                                          (wh[r] & (M << (BITS * j0))) | kMagic);
-                const uint64_t c1 = pack2((w[r] & (M << (BITS * j1))) | kMagic,
-                                          (wh[r] & (M << (BITS * j1))) | kMagic);
-                acc[r] = f2_fma(f2_sub(c0, kMagic2), x0, acc[r]);
-                acc[r] = f2_fma(f2_sub(c1, kMagic2), x1, acc[r]);
+                const uint32_t w = (&q[r].x)[i];
+                const uint32_t ca = w & 0x0F0F0F0Fu, cb = (w >> 4) & 0x0F0F0F0Fu;
+                hi[r] = dp4a_us(ca, xv.x, hi[r]);
+                lo[r] = dp4a_uu(ca, xv.y, lo[r]);
+                hi[r] = dp4a_us(cb, xv.z, hi[r]);
+                lo[r] = dp4a_uu(cb, xv.w, lo[r]);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+#pragma unroll
+            for (int h2 = 0; h2 < 2; h2++) {
+                const uint4 xv = xq[(2 * i + h2) * nch + c];
+#pragma unroll
+                for (int r = 0; r < NR; r++) {
+                    const uint32_t w = (&q[r].x)[i];
+                    const uint32_t c0 = (w >> (4 * h2)) & 0x03030303u;
+                    const uint32_t c1 = (w >> (4 * h2 + 2)) & 0x03030303u;
+                    hi[r] = dp4a_us(c0, xv.x, hi[r]);
+                    lo[r] = dp4a_uu(c0, xv.y, lo[r]);
+                    hi[r] = dp4a_us(c1, xv.z, hi[r]);
+                    lo[r] = dp4a_uu(c1, xv.w, lo[r]);
+                }
             }
         }
     }
+#pragma unroll
+    for (int r = 0; r < NR; r++) out[r] = hi[r] * 256 + lo[r];
 }
 
 }  // namespace step

@@ -209,7 +209,7 @@ class DecodeStack:
             self._hd = (moe.HeadDesc * c.L)(*[ly["head_desc"] for ly in L]) if has_heads else None
             self.sd = moe.StackDesc(C.cast(self._ed, C.c_void_p), C.cast(self._rd, C.c_void_p),
                                     C.cast(self._hd, C.c_void_p) if has_heads else None,
-                                    c.L, c.depth, c.K, int(c.self_predict), 0, 0)
+                                    c.L, c.depth, c.K, int(c.self_predict), 0, 0, None)
             self.step_ws = torch.zeros(moe.moe_decode_step_workspace_bytes(self.sd),
                                        dtype=torch.uint8, device=dev)
 
