@@ -272,9 +272,11 @@ typedef struct {
     int debug_unset_wait;             /* test hook: 1 makes the kernel wait on
                                          a flag nothing sets (-> MOE_ETIMEOUT) */
     unsigned long long *debug_trace;  /* profiling hook: NULL, or a device
-                                         buffer of n_SM * depth * 12 u64 that
+                                         buffer of n_SM * depth * 16 u64 that
                                          receives %globaltimer stamps per CTA
                                          and layer at phase boundaries        */
+    unsigned inflight_bytes;          /* tuning: weight-copy bytes in flight
+                                         per SM (0 = 32 KiB; at least 16 KiB) */
 } moe_stack_desc;
 
 /* Workspace bytes of moe_decode_step; 0 if the descriptor is invalid. */

@@ -11,26 +11,42 @@
 //    2609.18063), so weight fetches never wait for the activations.  A
 //    producer warp streams each CTA's share of every layer's weights into a
 //    byte ring in shared memory with bulk copies (cp.async.bulk + mbarrier),
-//    as far ahead as the ring allows, across layer boundaries.
-//  * Dependencies between CTAs (h after gate/up, out after down, head values,
-//    LoRA products) travel as 64-bit (tag, value) words in global memory: a
-//    reader polls the words it needs until their tag is the current one.
-//    There is no grid-wide barrier; each value is its own ready flag.  All
-//    polls of a phase are issued together, so a layer costs two dependent
-//    round trips: x (the previous layer's out) and h.
+//    as far ahead as the ring allows, across layer boundaries.  All 32 lanes
+//    issue copies together (one thread issues about one copy per 200 ns), and
+//    the bytes in flight per SM are capped: a deep queue of weight copies
+//    delays every load that shares the return path, including the polls of
+//    the exchanges below (measured on GB300: an all-to-all exchange takes
+//    1.3 us with 32 KB in flight per SM, 8 us with 192 KB).
+//  * Dependencies between CTAs travel as 64-bit (tag, value) words in global
+//    memory, gated by one ready flag per CTA and exchange: one warp of a CTA
+//    polls the flags while the others sleep on an mbarrier, then every warp
+//    reads its words once (their tags are checked).  There is no grid-wide
+//    barrier.  A layer has exactly two exchanges on its critical path: x (the
+//    previous layer's out) and h.  The LoRA products ride on them: each CTA
+//    publishes, with its rows of out, its partial A x over those rows for the
+//    next layer's gate/up LoRA, and the owners of a down-LoRA slot's gate/up
+//    rows publish their partial A_d h with h.
+//  * The prerouter head's first layer (fc1, l) reads x like the gate/up rows
+//    do and is split with them; its second layer (fc2) and the top-K only feed
+//    the next token, so an auxiliary warp runs them off the critical path, and
+//    also prepares each layer's small operands (K-hot table sums, LoRA B rows,
+//    A columns and scales) in shared memory a layer ahead.
+//  * The launch context lives in shared memory (read with plain shared loads
+//    by every function) and per-thread state in registers: nothing of the hot
+//    path goes through local memory, whose misses would cost an L2 round trip
+//    each.
 //  * x enters the GEMVs unnormalised; 1/rms is applied to each finished row
-//    dot, so a CTA can start on x as soon as it has polled it.
+//    dot.  Activations are staged per 16-byte code chunk as 16-bit fixed
+//    point, and each chunk's code dot is an exact integer sum (dp4a).
 //  * Every wait is bounded (globaltimer); on expiry the kernel records
 //    MOE_ETIMEOUT in the workspace status word, waits (bounded) for its own
 //    copies in flight and returns.
 //
-// Work per layer.  Phase A (needs x): LoRA A-rows on x, gate/up row pairs of
-// every slot (slots with gate/up LoRA first), head fc1 rows and l rows --
-// split across CTAs by bytes.  The owners of a down-LoRA slot's gate/up rows
-// also publish their partial A_d h.  Phase B (needs h): down rows (CTA c owns
-// outputs [c*d/n, (c+1)*d/n) of every slot, adds their LoRA terms and
-// combines them), then head fc2 rows (split by count).  Phase R (layer 0,
-// when it routes with its own router): router rows.
+// Work per layer and CTA.  Phase A (needs x): gate/up row pairs of every slot,
+// head fc1 rows and l rows -- split across CTAs by bytes.  Phase B (needs h):
+// down rows of CTA c's outputs [c*d/n, (c+1)*d/n) for every slot; the warp
+// that owns an output row in one slot owns it in all, so it combines the row
+// itself.  Phase R (layer 0, when it routes with its own router): router rows.
 #include <algorithm>
 
 #include "step_common.cuh"
@@ -40,22 +56,45 @@ namespace step {
 
 constexpr int kMaxLayers = 48;
 constexpr int kNW = 12;                        // consumer warps
-constexpr int kProducerWarp = 0, kRouteWarp = 1, kCons0 = 2;
+constexpr int kProducerWarp = 0, kAuxWarp = 1, kCons0 = 2;
 constexpr int kThreads = (kCons0 + kNW) * 32;  // 448
 constexpr int kMaxPiece = 16384;               // bytes per bulk copy
-constexpr int kNB = 32;                        // pieces in flight (barrier pairs)
+constexpr int kNB = 64;                        // pieces in the ring at once (barrier pairs)
 constexpr int kMaxK = 16;
-constexpr int kMaxGroups = 40;
-constexpr int kMaxOwnE = 64;                   // fc2 rows one CTA may own
-constexpr int kMaxVdp = 4096;                  // floats of polled A_d h partials
+constexpr int kMaxGroups = 24;
+constexpr int kMaxR = 32;                      // LoRA rank bound of the fused kernel
+constexpr int kPollW = 20;                     // tagged words one lane polls at once
 constexpr int kTrace = 16;                     // stamps per (CTA, layer), debug trace
+constexpr uint32_t kDefaultInflight = 32768;   // weight bytes in flight per SM
+constexpr uint32_t kSleepHint = 20000;         // ns a thread may sleep in one mbarrier wait
 
-enum Kind : uint8_t { KLA = 0, KGU, KFC1, KLX, KROUTER, KDOWN, KFC2 };
-enum Tmpl : int { T_R = 0, T_A_HEAD, T_A_NOHEAD, T_B_HEAD, T_B_NOHEAD, T_COUNT };
+enum Kind : uint8_t { KGU = 0, KFC1, KLX, KROUTER, KDOWN };
+enum Tmpl : int { T_R = 0, T_A_HEAD, T_A_NOHEAD, T_B, T_COUNT };
 
 // control words at the start of the workspace
 enum Ctrl : int { C_STATUS = 0, C_EPOCH = 1, C_DONE = 2, C_ABORT = 3, C_NEVER = 4 };
 constexpr size_t kCtrlBytes = 256;
+
+// mbarriers after the kNB full / kNB empty pairs
+enum Bar : int {
+    B_ROUTE = 0, B_CONS, B_END, B_PREP_FULL0, B_PREP_FULL1, B_PREP_EMPTY0, B_PREP_EMPTY1, B_X, B_H,
+    B_COUNT
+};
+
+// last-warp counters and small values in the misc area (ints / floats)
+enum Misc : int {
+    M_SS = 0, M_INV = 12, M_CNT_A = 16, M_CNT_X, M_CNT_H, M_CNT_D, M_TMPL_OK, M_VDP_N0, M_VDP_N1,
+    M_COUNT
+};
+
+// debug trace stamps (per CTA and layer)
+enum Stamp : int {
+    ST_L0 = 0, ST_X = 1, ST_A = 2, ST_H = 3, ST_D = 4,
+    ST_PA = 8, ST_PB = 9, ST_PE = 10, ST_AUXP = 12, ST_AUXF = 13
+};
+
+// per-layer LoRA scales in the prep buffer
+enum Scale : int { SC_G = 0, SC_U, SC_DR, SC_DS, SC_COUNT };
 
 struct LoraP {
     int r;
@@ -76,24 +115,37 @@ struct LayerP {
     const uint16_t *l_tab, *bl;
 };
 
-struct Params {
-    int d, F, E, K, H, S, depth, n_res, self_predict, own0, t, n_cta, max_orows, rd;
-    uint32_t ring_bytes;
-    size_t stride;
+// Everything the device code reads besides the layer table; copied into
+// shared memory at the start of the kernel.
+struct Ctx {
+    int d, F, E, K, H, S, depth, n_res, self_predict, own0, t, n_cta;
+    int max_orows, max_erows, max_pairs, max_hrows;
+    int rg, ru, rd, rdr, rds, gu_slot, n_dl;   // LoRA ranks: gate, up (on gu_slot), down (max,
+                                               // routed, shared); down-LoRA slot count
+    uint32_t dl_mask;                          // slots with a down LoRA
+    uint32_t ring_bytes, inflight, epoch;
     uint32_t gu_off, down_off, rec_d, rec_F, rec_dh, rec_H;
+    size_t stride;
+    uint64_t timeout_ns;
+    int debug_unset_wait;
+    uint8_t *ws;
     const float *x0;
     float *out;
     int32_t *ridx;
     float *rw, *rmargin;
-    uint8_t *ws;
-    uint32_t off_h, off_v, off_vdp, off_ga, off_zl, off_zr, off_z, off_out;
-    uint64_t timeout_ns;
-    int debug_unset_wait;
-    unsigned long long *trace;   // debug: [n_cta][depth][kTrace] globaltimer stamps
+    unsigned long long *trace;                 // debug: [n_cta][depth][kTrace] globaltimer stamps
+    uint32_t off_h, off_vp, off_vdp, off_ga, off_zl, off_zr, off_z, off_out, off_xflag, off_hflag;
     // shared-memory layout (byte offsets from the dynamic base)
     uint32_t sm_ring, sm_bar, sm_pend, sm_tmpl, sm_xf, sm_xsc, sm_xhat, sm_xf4, sm_xsc4, sm_xhat4,
-        sm_stream, sm_hf, sm_hsc, sm_hhat, sm_gf, sm_gsc, sm_ghat, sm_zl, sm_y, sm_bd, sm_vdp,
-        sm_vd, sm_rcur, sm_rprev, sm_rw, sm_misc;
+        sm_stream, sm_hf, sm_hsc, sm_hhat, sm_vpw, sm_vx, sm_vdw, sm_vd, sm_vdacc, sm_vnw, sm_comb,
+        sm_prep, sm_gf, sm_gsc, sm_ghat, sm_frec, sm_rcur, sm_rprev, sm_rw, sm_misc, sm_hraw, sm_graw,
+        sm_vdpl;
+    // one prep buffer: bytes, and float offsets of its parts
+    uint32_t prep_bytes, pp_tsum, pp_bgu, pp_adn, pp_bd, pp_agu, pp_scale;
+};
+
+struct Params {
+    Ctx cx;
     LayerP layer[kMaxLayers];
 };
 
@@ -101,7 +153,7 @@ struct Params {
 struct Grp {
     uint32_t item_bytes;
     int n, lo, hi, cols;
-    uint8_t kind, slot, aux, pad;
+    uint8_t kind, slot, pad0, pad1;
 };
 
 // A phase's groups, identical for every layer of the same kind (only the
@@ -110,36 +162,61 @@ struct Tmplt {
     Grp g[kMaxGroups];
     int n;
     int o_lo, o_hi, e_lo, e_hi;
-    // phase A: owners [own0[s], own1[s]] of the gate/up rows of slot s
-    int own0[kMaxK + 1], own1[kMaxK + 1];
+    int own0[kMaxSlots], own1[kMaxSlots];   // CTAs owning the slot's gate/up rows
+    int plo[kMaxSlots], phi[kMaxSlots];     // this CTA's gate/up pairs of the slot
+    int pbase[kMaxSlots];                   // CTA-local index of the slot's first own pair
+    int f1lo, f1hi, llo, lhi;               // this CTA's fc1 and l rows
 };
 
-// ---------------------------------------------------------------- control
-__device__ __forceinline__ int *ctrl(const Params &p) { return reinterpret_cast<int *>(p.ws); }
+// ---------------------------------------------------------------- context
+extern __shared__ __align__(1024) uint8_t g_smem[];
 
-__device__ __forceinline__ void raise_error(const Params &p, int code) {
-    atomicCAS(ctrl(p) + C_STATUS, 0, code);
-    atomicExch(ctrl(p) + C_ABORT, 1);
+__device__ __forceinline__ const Ctx &CX() { return *reinterpret_cast<const Ctx *>(g_smem); }
+
+template <typename T>
+__device__ __forceinline__ T *SM(uint32_t off) {
+    return reinterpret_cast<T *>(g_smem + off);
 }
 
-__device__ __forceinline__ bool aborted(const Params &p) { return ld_flag(ctrl(p) + C_ABORT) != 0; }
+__device__ __forceinline__ uint64_t *bar_full(int i) { return SM<uint64_t>(CX().sm_bar) + i; }
+__device__ __forceinline__ uint64_t *bar_empty(int i) { return SM<uint64_t>(CX().sm_bar) + kNB + i; }
+__device__ __forceinline__ uint64_t *bar(int b) { return SM<uint64_t>(CX().sm_bar) + 2 * kNB + b; }
+__device__ __forceinline__ const Tmplt *tmpls() { return SM<Tmplt>(CX().sm_tmpl); }
+__device__ __forceinline__ int *misc_i() { return SM<int>(CX().sm_misc); }
+__device__ __forceinline__ float *misc_f() { return SM<float>(CX().sm_misc); }
 
-// Warp-collective bounded wait on an mbarrier phase: every lane observes the
+__device__ __forceinline__ float *prep_of(int N, uint32_t part) {
+    const Ctx &cx = CX();
+    return reinterpret_cast<float *>(g_smem + cx.sm_prep + (size_t)(N & 1) * cx.prep_bytes) + part;
+}
+
+// ---------------------------------------------------------------- control
+__device__ __forceinline__ int *ctrl() { return reinterpret_cast<int *>(CX().ws); }
+
+__device__ __forceinline__ void raise_error(int code) {
+    atomicCAS(ctrl() + C_STATUS, 0, code);
+    atomicExch(ctrl() + C_ABORT, 1);
+}
+
+__device__ __forceinline__ bool aborted() { return ld_flag(ctrl() + C_ABORT) != 0; }
+
+// Warp-collective bounded wait on an mbarrier phase (inlined copy for the
+// piece loop; wait_bar_warp is the out-of-line one): every lane observes the
 // phase and the warp leaves together; false (error recorded) on timeout or
 // when another CTA has aborted.
-__device__ bool wait_bar_warp(const Params &p, uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool wait_bar_warp_inl(uint64_t *b, uint32_t parity) {
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
     if (lane == 0) t0 = now_ns();
     for (int it = 1;; it++) {
-        const bool ok = mbar_try_wait(bar, parity);
+        const bool ok = mbar_try_wait_sleep(b, parity, kSleepHint);
         if (__all_sync(0xffffffffu, ok)) return true;
-        if ((it & 63) == 0) {
+        if ((it & 7) == 0) {
             int stop = 0;
             if (lane == 0) {
-                if (aborted(p)) stop = 1;
-                else if (now_ns() - t0 > p.timeout_ns) {
-                    raise_error(p, MOE_ETIMEOUT);
+                if (aborted()) stop = 1;
+                else if (now_ns() - t0 > CX().timeout_ns) {
+                    raise_error(MOE_ETIMEOUT);
                     stop = 1;
                 }
             }
@@ -148,63 +225,159 @@ __device__ bool wait_bar_warp(const Params &p, uint64_t *bar, uint32_t parity) {
     }
 }
 
-// Single-thread bounded wait (producer lane, end of kernel).
-__device__ bool wait_bar(const Params &p, uint64_t *bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool wait_bar_warp(uint64_t *b, uint32_t parity) {
+    return wait_bar_warp_inl(b, parity);
+}
+
+// Single-thread bounded wait (end of kernel).
+__device__ bool wait_bar(uint64_t *b, uint32_t parity) {
+    if (mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = now_ns();
     for (int it = 1;; it++) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
-            if (aborted(p)) return false;
-            if (now_ns() - t0 > p.timeout_ns) {
-                raise_error(p, MOE_ETIMEOUT);
+        if (mbar_try_wait_sleep(b, parity, kSleepHint)) return true;
+        if ((it & 7) == 0) {
+            if (aborted()) return false;
+            if (now_ns() - t0 > CX().timeout_ns) {
+                raise_error(MOE_ETIMEOUT);
                 return false;
             }
         }
     }
 }
 
-__device__ __forceinline__ uint64_t *tagged(const Params &p, uint32_t off) {
-    return reinterpret_cast<uint64_t *>(p.ws + off);
+__device__ __forceinline__ uint64_t *tagged(uint32_t off) {
+    return reinterpret_cast<uint64_t *>(CX().ws + off);
 }
 
-// Per-thread bounded poll of `cnt` (<= 8) tagged words at w + idx[k], all
-// loads in flight together; values to val[k].  False on timeout or abort.
-__device__ __forceinline__ bool poll_set(const Params &p, const uint64_t *w, const int *idx,
-                                         int cnt, uint32_t tag, float *val) {
-    uint32_t pend = (1u << cnt) - 1u;
+// the workspace as 64-bit words (tagged words are indexed from here)
+__device__ __forceinline__ const uint64_t *ws_words() {
+    return reinterpret_cast<const uint64_t *>(CX().ws);
+}
+
+__device__ __forceinline__ uint32_t *flag_of(uint32_t off, int c) {
+    return reinterpret_cast<uint32_t *>(CX().ws + off) + c;
+}
+
+// Per-lane bounded poll of the tagged words base[idx[k]] for the bits k set
+// in `pend`, all loads in flight together; word k must carry tagB if bit k of
+// selB is set, else tagA.  Values to val[k].  False on timeout or abort.
+template <int W>
+__device__ __forceinline__ bool poll_vals(const uint64_t *base, const uint32_t (&idx)[W],
+                                          uint32_t pend, uint32_t selB, uint32_t tagA,
+                                          uint32_t tagB, float (&val)[W]) {
     uint64_t t0 = 0;
     for (int it = 0; pend; it++) {
-        uint64_t v[8];
+        uint64_t v[W];
 #pragma unroll
-        for (int k = 0; k < 8; k++)
-            if (pend >> k & 1u) v[k] = get_word(w + idx[k]);
+        for (int k = 0; k < W; k++) v[k] = (pend >> k & 1u) ? get_word(base + idx[k]) : 0ull;
 #pragma unroll
-        for (int k = 0; k < 8; k++)
-            if ((pend >> k & 1u) && (uint32_t)(v[k] >> 32) == tag) {
+        for (int k = 0; k < W; k++) {
+            const uint32_t tg = (selB >> k & 1u) ? tagB : tagA;
+            if ((pend >> k & 1u) && (uint32_t)(v[k] >> 32) == tg) {
                 val[k] = __uint_as_float((uint32_t)v[k]);
                 pend &= ~(1u << k);
             }
-        if (pend) {
-            // back off so that waiting warps leave issue slots to working ones
-            __nanosleep(32u << (it < 3 ? it : 3));
-            if ((it & 7) == 7) {
-                if (it == 7) t0 = now_ns();
-                else if (aborted(p)) return false;
-                else if (now_ns() - t0 > p.timeout_ns) {
-                    raise_error(p, MOE_ETIMEOUT);
-                    return false;
-                }
+        }
+        if (pend && (it & 7) == 7) {
+            if (it == 7) t0 = now_ns();
+            else if (aborted()) return false;
+            else if (now_ns() - t0 > CX().timeout_ns) {
+                raise_error(MOE_ETIMEOUT);
+                return false;
             }
         }
     }
     return true;
 }
 
+// Slow path of the reads that follow a flag wait: word i of this lane
+// (index idx(i), i < n) is re-read until it carries `tag`, its value handed to
+// sink(i, value) in order.  Warp-uniform result (false on timeout or abort).
+template <typename Idx, typename Sink>
+__device__ __noinline__ bool reread_words(const uint64_t *base, int n, uint32_t tag, Idx idx, Sink sink) {
+    const uint64_t t0 = now_ns();
+    bool ok = true;
+#pragma unroll 1
+    for (int i = 0; i < n && ok; i++) {
+#pragma unroll 1
+        for (int it = 0;; it++) {
+            const uint64_t w = get_word(base + idx(i));
+            if ((uint32_t)(w >> 32) == tag) {
+                sink(i, __uint_as_float((uint32_t)w));
+                break;
+            }
+            if ((it & 7) == 7 && (aborted() || now_ns() - t0 > CX().timeout_ns)) {
+                if (!aborted()) raise_error(MOE_ETIMEOUT);
+                ok = false;
+                break;
+            }
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Reads the tagged words base[idx(i)], i < n, of this lane (loads four at a
+// time, in flight together) and hands their values to sink(i, value) in
+// order; if any word still carried an old tag, all are read again through the
+// bounded slow path (reset() first).  Warp-uniform result.
+template <typename Idx, typename Sink, typename Reset>
+__device__ __forceinline__ bool read_words(const uint64_t *base, int n, uint32_t tag, Idx idx,
+                                           Sink sink, Reset reset) {
+    bool stale = false;
+#pragma unroll 1
+    for (int i0 = 0; i0 < n; i0 += 4) {
+        uint64_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; k++) w[k] = i0 + k < n ? get_word(base + idx(i0 + k)) : 0ull;
+#pragma unroll
+        for (int k = 0; k < 4; k++)
+            if (i0 + k < n) {
+                stale |= (uint32_t)(w[k] >> 32) != tag;
+                sink(i0 + k, __uint_as_float((uint32_t)w[k]));
+            }
+    }
+    if (!__any_sync(0xffffffffu, stale)) return true;
+    reset();
+    return reread_words(base, n, tag, idx, sink);
+}
+
+// Warp-collective bounded wait until every CTA's flag at workspace offset
+// `off` has reached `tag` (flags only grow within a step); lane j polls flags
+// j, j+32, ...
+__device__ __noinline__ bool poll_flags(uint32_t off, uint32_t tag, int lane, uint32_t sleep_ns) {
+    const uint32_t *f = flag_of(off, 0);
+    const int n_cta = CX().n_cta;
+    uint32_t pend = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        if (lane + 32 * i < n_cta) pend |= 1u << i;
+    uint64_t t0 = 0;
+    for (int it = 0;; it++) {
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+            if ((pend >> i & 1u) && (int)(ld_acquire(f + lane + 32 * i) - tag) >= 0)
+                pend &= ~(1u << i);
+        if (__all_sync(0xffffffffu, pend == 0)) return true;
+        if (sleep_ns) __nanosleep(sleep_ns);
+        if ((it & 7) == 7) {
+            int stop = 0;
+            if (lane == 0) {
+                if (it == 7) t0 = now_ns();
+                else if (aborted()) stop = 1;
+                else if (now_ns() - t0 > CX().timeout_ns) {
+                    raise_error(MOE_ETIMEOUT);
+                    stop = 1;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+        }
+    }
+}
+
 // Warp poll of E logits, lane-strided (vals[i] = logit lane + 32 i), all in
 // flight together.  Warp-uniform result.
-__device__ __noinline__ bool poll_logits(const Params &p, const uint64_t *z, int E, uint32_t tag, int lane,
-                            float (&vals)[32]) {
+__device__ __forceinline__ bool poll_logits(const uint64_t *z, int E, uint32_t tag, int lane,
+                                            float (&vals)[32], uint32_t sleep_ns) {
     uint32_t pend = 0;
 #pragma unroll
     for (int i = 0; i < 32; i++) {
@@ -223,73 +396,62 @@ __device__ __noinline__ bool poll_logits(const Params &p, const uint64_t *z, int
                     pend &= ~(1u << i);
                 }
             }
-        if (pend) {
-            __nanosleep(64u << (it < 2 ? it : 2));
-            if ((it & 7) == 7) {
-                if (it == 7) t0 = now_ns();
-                else if (aborted(p)) lok = false;
-                else if (now_ns() - t0 > p.timeout_ns) {
-                    raise_error(p, MOE_ETIMEOUT);
-                    lok = false;
-                }
+        if (pend && sleep_ns) __nanosleep(sleep_ns);
+        if (pend && (it & 7) == 7) {
+            if (it == 7) t0 = now_ns();
+            else if (aborted()) lok = false;
+            else if (now_ns() - t0 > CX().timeout_ns) {
+                raise_error(MOE_ETIMEOUT);
+                lok = false;
             }
         }
     }
     return __all_sync(0xffffffffu, lok);
 }
 
+__device__ __forceinline__ void stamp_at(int c, int N, int k) {
+    const Ctx &cx = CX();
+    if (cx.trace) cx.trace[((size_t)c * cx.depth + N) * kTrace + k] = now_ns();
+}
+
 // ---------------------------------------------------------------- layers
+__device__ __forceinline__ bool head_runs(int N) {
+    const Ctx &cx = CX();
+    return N + 1 < cx.depth || cx.self_predict;
+}
+
 __device__ __forceinline__ const LayerP &layer_of(const Params &p, int N) {
-    return p.layer[N % p.n_res];
+    return p.layer[N % p.cx.n_res];
 }
 
-__device__ __forceinline__ bool head_runs(const Params &p, int N) {
-    return N + 1 < p.depth || p.self_predict;
+__device__ __forceinline__ const LoraP &slot_lora(const LayerP &L, int K, int s, int w) {
+    return s < K ? L.lora[w] : L.slora[w];
 }
 
-__device__ __forceinline__ const LoraP &slot_lora(const Params &p, const LayerP &L, int s, int w) {
-    return s < p.K ? L.lora[w] : L.slora[w];
+__device__ __forceinline__ const uint16_t *lora_a(const LayerP &L, int K, const int *route, int s,
+                                                  int w) {
+    const LoraP &l = slot_lora(L, K, s, w);
+    return l.A + (s < K ? (size_t)route[s] * l.as : 0);
 }
 
-__device__ __forceinline__ const uint8_t *slot_blob(const Params &p, const LayerP &L,
-                                                    const int *route, int s) {
-    return s < p.K ? L.pool + (size_t)route[s] * p.stride : L.shared;
+__device__ __forceinline__ const uint16_t *lora_bm(const LayerP &L, int K, const int *route, int s,
+                                                   int w) {
+    const LoraP &l = slot_lora(L, K, s, w);
+    return l.B + (s < K ? (size_t)route[s] * l.bs : 0);
 }
 
-__device__ __forceinline__ const uint16_t *lora_a(const Params &p, const LayerP &L, const int *route,
-                                                  int s, int w) {
-    const LoraP &l = slot_lora(p, L, s, w);
-    return l.A + (s < p.K ? (size_t)route[s] * l.as : 0);
+// rank of slot s's down LoRA
+__device__ __forceinline__ int dl_rank(int s) {
+    const Ctx &cx = CX();
+    return s < cx.K ? cx.rdr : cx.rds;
 }
 
-__device__ __forceinline__ const uint16_t *lora_bm(const Params &p, const LayerP &L,
-                                                   const int *route, int s, int w) {
-    const LoraP &l = slot_lora(p, L, s, w);
-    return l.B + (s < p.K ? (size_t)route[s] * l.bs : 0);
-}
-
-// Address of item 0 of group g in layer N.
-__device__ __forceinline__ const uint8_t *group_src(const Params &p, int N, const Grp &g,
-                                                    const int *route) {
-    const LayerP &L = layer_of(p, N);
-    switch (g.kind) {
-        case KLA: return reinterpret_cast<const uint8_t *>(lora_a(p, L, route, g.slot, g.aux));
-        case KGU: return slot_blob(p, L, route, g.slot) + p.gu_off;
-        case KFC1: return L.fc1x;
-        case KLX: return L.lx;
-        case KROUTER: return L.router;
-        case KDOWN: return slot_blob(p, L, route, g.slot) + p.down_off;
-        default: return L.fc2;
-    }
-}
-
-__device__ __forceinline__ bool gu_lora(const Params &p, const LayerP &L, int s) {
-    return slot_lora(p, L, s, 0).r || slot_lora(p, L, s, 1).r;
-}
+// index of slot s among the down-LoRA slots
+__device__ __forceinline__ int dl_index(int s) { return __popc(CX().dl_mask & ((1u << s) - 1u)); }
 
 // ---------------------------------------------------------------- templates
-__device__ void add_group(Tmplt &t, uint32_t ib, int n, int kind, int slot, int aux, int cols,
-                          int lo = 0, int hi = 0) {
+__device__ void add_group(Tmplt &t, uint32_t ib, int n, int kind, int slot, int cols, int lo = 0,
+                          int hi = 0) {
     Grp &g = t.g[t.n++];
     g.item_bytes = ib;
     g.n = n;
@@ -298,8 +460,7 @@ __device__ void add_group(Tmplt &t, uint32_t ib, int n, int kind, int slot, int 
     g.cols = cols;
     g.kind = (uint8_t)kind;
     g.slot = (uint8_t)slot;
-    g.aux = (uint8_t)aux;
-    g.pad = 0;
+    g.pad0 = g.pad1 = 0;
 }
 
 __device__ __forceinline__ long long split_at(long long total, int c, int n) {
@@ -315,13 +476,17 @@ __device__ int owner_of(long long pos, long long total, int n) {
     return c;
 }
 
-// Item ranges of all groups of t under an even split of their bytes; also the
-// owner CTAs of each gate/up group.
+// Item ranges of all groups of t under an even split of their bytes (an item
+// belongs to the CTA whose share holds its first byte); also the owner CTAs
+// of each gate/up group and this CTA's own ranges.
 __device__ void split_bytes(Tmplt &t, int c, int n_cta) {
     long long total = 0;
+#pragma unroll 1
     for (int i = 0; i < t.n; i++) total += (long long)t.g[i].n * t.g[i].item_bytes;
     const long long a = split_at(total, c, n_cta), b = split_at(total, c + 1, n_cta);
     long long base = 0;
+    int pairs = 0;
+#pragma unroll 1
     for (int i = 0; i < t.n; i++) {
         Grp &g = t.g[i];
         const long long ib = g.item_bytes;
@@ -332,58 +497,19 @@ __device__ void split_bytes(Tmplt &t, int c, int n_cta) {
         if (g.kind == KGU) {
             t.own0[g.slot] = owner_of(base, total, n_cta);
             t.own1[g.slot] = owner_of(base + (long long)(g.n - 1) * ib, total, n_cta);
+            t.plo[g.slot] = g.lo;
+            t.phi[g.slot] = g.hi;
+            t.pbase[g.slot] = pairs;
+            pairs += g.hi - g.lo;
+        } else if (g.kind == KFC1) {
+            t.f1lo = g.lo;
+            t.f1hi = g.hi;
+        } else if (g.kind == KLX) {
+            t.llo = g.lo;
+            t.lhi = g.hi;
         }
         base += (long long)g.n * ib;
     }
-}
-
-// The CTA's phase templates (built once per launch by one thread).
-__device__ __noinline__ void build_templates(const Params &p, int c, Tmplt *T) {
-    const LayerP &L = p.layer[0];
-    {
-        Tmplt &t = T[T_R];
-        t.n = 0;
-        add_group(t, p.rec_dh, p.E, KROUTER, 0, 0, p.d);
-        split_bytes(t, c, p.n_cta);
-    }
-    for (int head = 1; head >= 0; head--) {
-        Tmplt &t = T[head ? T_A_HEAD : T_A_NOHEAD];
-        t.n = 0;
-        for (int s = 0; s < p.S; s++)
-            for (int w = 0; w < 2; w++)
-                if (slot_lora(p, L, s, w).r)
-                    add_group(t, 2u * p.d, slot_lora(p, L, s, w).r, KLA, s, w, p.d);
-        for (int pass = 0; pass < 2; pass++)              // LoRA slots first
-            for (int s = 0; s < p.S; s++)
-                if (gu_lora(p, L, s) == (pass == 0)) add_group(t, 2u * p.rec_d, p.F, KGU, s, 0, p.d);
-        if (head) {
-            if (p.H) add_group(t, p.rec_dh, p.H, KFC1, 0, 0, p.d);
-            add_group(t, p.rec_dh, p.E, KLX, 0, 0, p.d);
-        }
-        split_bytes(t, c, p.n_cta);
-    }
-    const int o_lo = (int)((long long)p.d * c / p.n_cta);
-    const int o_hi = (int)((long long)p.d * (c + 1) / p.n_cta);
-    const int e_lo = (int)((long long)p.E * c / p.n_cta);
-    const int e_hi = (int)((long long)p.E * (c + 1) / p.n_cta);
-    for (int head = 1; head >= 0; head--) {
-        Tmplt &t = T[head ? T_B_HEAD : T_B_NOHEAD];
-        t.n = 0;
-        t.o_lo = o_lo;
-        t.o_hi = o_hi;
-        t.e_lo = e_lo;
-        t.e_hi = e_hi;
-        for (int s = 0; s < p.S; s++) add_group(t, p.rec_F, p.d, KDOWN, s, 0, p.F, o_lo, o_hi);
-        if (head && p.H > 0) add_group(t, p.rec_H, p.E, KFC2, 0, 0, p.H, e_lo, e_hi);
-    }
-}
-
-__device__ __forceinline__ const Tmplt &tmpl_A(const Params &p, const Tmplt *T, int N) {
-    return T[head_runs(p, N) ? T_A_HEAD : T_A_NOHEAD];
-}
-
-__device__ __forceinline__ const Tmplt &tmpl_B(const Params &p, const Tmplt *T, int N) {
-    return T[head_runs(p, N) ? T_B_HEAD : T_B_NOHEAD];
 }
 
 __host__ __device__ __forceinline__ int pow2_floor32(int n) {
@@ -398,10 +524,65 @@ __device__ __forceinline__ int item_chunks(const Grp &g) {
     switch (g.kind) {
         case KGU:
         case KDOWN: return g.cols * BITS / 128;
-        case KLA: return g.cols / 8;
         default: return g.cols / 32;              // int4 head rows
     }
 }
+
+// Items per bulk copy of a group: as many as fit kMaxPiece, a multiple of
+// the rows one warp task takes (so a down row keeps its warp in every slot).
+template <int BITS>
+__device__ __forceinline__ int piece_items(const Grp &g) {
+    const int rpw = 32 / pow2_floor32(item_chunks<BITS>(g));
+    int per = kMaxPiece / (int)g.item_bytes;
+    if (per < 1) per = 1;
+    if (per >= rpw) per -= per % rpw;
+    return per;
+}
+
+// The CTA's phase templates (built once per launch by one thread); false if a
+// per-CTA bound of the shared-memory layout is exceeded.
+__device__ __noinline__ bool build_templates(int c, Tmplt *T) {
+    const Ctx &cx = CX();
+    {
+        Tmplt &t = T[T_R];
+        t.n = 0;
+        add_group(t, cx.rec_dh, cx.E, KROUTER, 0, cx.d);
+        split_bytes(t, c, cx.n_cta);
+    }
+    bool ok = true;
+    for (int head = 1; head >= 0; head--) {
+        Tmplt &t = T[head ? T_A_HEAD : T_A_NOHEAD];
+        t.n = 0;
+        t.f1lo = t.f1hi = t.llo = t.lhi = 0;
+        for (int s = 0; s < cx.S; s++) add_group(t, 2u * cx.rec_d, cx.F, KGU, s, cx.d);
+        if (head) {
+            if (cx.H) add_group(t, cx.rec_dh, cx.H, KFC1, 0, cx.d);
+            add_group(t, cx.rec_dh, cx.E, KLX, 0, cx.d);
+        }
+        split_bytes(t, c, cx.n_cta);
+        // the (slot, owner) words of the down-LoRA partials, slot by slot
+        uint32_t *list = SM<uint32_t>(cx.sm_vdpl) + (head ? 0 : cx.n_dl * cx.n_cta);
+        int nl = 0;
+        for (int s = 0; s < cx.S; s++)
+            if (cx.dl_mask >> s & 1u)
+                for (int o = t.own0[s]; o <= t.own1[s] && nl < cx.n_dl * cx.n_cta; o++)
+                    list[nl++] = (uint32_t)s << 16 | (uint32_t)o;
+        misc_i()[head ? M_VDP_N0 : M_VDP_N1] = nl;
+        int pairs = 0;
+        for (int s = 0; s < cx.S; s++) pairs += t.phi[s] - t.plo[s];
+        ok = ok && pairs <= cx.max_pairs && (t.f1hi - t.f1lo) + (t.lhi - t.llo) <= cx.max_hrows;
+    }
+    Tmplt &t = T[T_B];
+    t.n = 0;
+    t.o_lo = (int)((long long)cx.d * c / cx.n_cta);
+    t.o_hi = (int)((long long)cx.d * (c + 1) / cx.n_cta);
+    t.e_lo = (int)((long long)cx.E * c / cx.n_cta);
+    t.e_hi = (int)((long long)cx.E * (c + 1) / cx.n_cta);
+    for (int s = 0; s < cx.S; s++) add_group(t, cx.rec_F, cx.d, KDOWN, s, cx.F, t.o_lo, t.o_hi);
+    return ok && t.o_hi - t.o_lo <= cx.max_orows && t.e_hi - t.e_lo <= cx.max_erows;
+}
+
+__device__ __forceinline__ int tmpl_A_index(int N) { return head_runs(N) ? T_A_HEAD : T_A_NOHEAD; }
 
 // ---------------------------------------------------------------- ring
 // Byte ring of pieces: a piece never straddles the end of the ring; producer
@@ -416,55 +597,6 @@ struct RingPos {
         return start;
     }
 };
-
-// ---------------------------------------------------------------- smem views
-struct Smem {
-    uint8_t *ring;
-    uint64_t *full, *empty, *route_bar, *cons_bar, *end_bar, *pend;
-    Tmplt *T;
-    uint8_t *xf, *xf4, *hf, *gf;          // staged fixed-point vectors
-    float *xsc, *xhat, *xsc4, *xhat4, *hsc, *hhat, *gsc, *ghat;
-    float *stream, *zl, *y, *bd, *vdp, *vd;
-    int *rcur, *rprev;
-    float *rw, *misc;
-};
-
-__device__ __forceinline__ Smem smem_views(const Params &p, uint8_t *base) {
-    Smem s;
-    s.ring = base + p.sm_ring;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base + p.sm_bar);
-    s.full = bars;
-    s.empty = bars + kNB;
-    s.route_bar = bars + 2 * kNB;
-    s.cons_bar = s.route_bar + 1;
-    s.end_bar = s.route_bar + 2;
-    s.pend = reinterpret_cast<uint64_t *>(base + p.sm_pend);
-    s.T = reinterpret_cast<Tmplt *>(base + p.sm_tmpl);
-    auto f = [&](uint32_t o) { return reinterpret_cast<float *>(base + o); };
-    s.xf = base + p.sm_xf;
-    s.xf4 = base + p.sm_xf4;
-    s.hf = base + p.sm_hf;
-    s.gf = base + p.sm_gf;
-    s.xsc = f(p.sm_xsc);
-    s.xhat = f(p.sm_xhat);
-    s.xsc4 = f(p.sm_xsc4);
-    s.xhat4 = f(p.sm_xhat4);
-    s.hsc = f(p.sm_hsc);
-    s.hhat = f(p.sm_hhat);
-    s.gsc = f(p.sm_gsc);
-    s.ghat = f(p.sm_ghat);
-    s.stream = f(p.sm_stream);
-    s.zl = f(p.sm_zl);
-    s.y = f(p.sm_y);
-    s.bd = f(p.sm_bd);
-    s.vdp = f(p.sm_vdp);
-    s.vd = f(p.sm_vd);
-    s.rcur = reinterpret_cast<int *>(base + p.sm_rcur);
-    s.rprev = reinterpret_cast<int *>(base + p.sm_rprev);
-    s.rw = f(p.sm_rw);
-    s.misc = f(p.sm_misc);
-    return s;
-}
 
 // ---------------------------------------------------------------- math helpers
 // Dot products of R rows (records at rec + r*stride) with a staged vector
@@ -505,21 +637,11 @@ __device__ __forceinline__ void rows_dot(const uint8_t *rec, uint32_t stride, in
     for (int r = 0; r < R; r++) out[r] = warp_sum(acc[r], lpr);
 }
 
-// Dot product of one fp16 row (in smem) with a plain float vector (smem),
-// reduced over the lpr lanes of the row group.
-__device__ __forceinline__ float f16_row_dot_s(const uint8_t *row, int cols, const float *v,
-                                               int sub, int lpr) {
-    float acc = 0.0f;
-    for (int c = sub; c < cols / 8; c += lpr)
-        acc += chunk_dot_f16(*reinterpret_cast<const uint4 *>(row + (size_t)kChunk * c), v + 8 * c);
-    return warp_sum(acc, lpr);
-}
-
 // Warp top-K over E logits (value desc, index asc) -> idx, softmax weights,
 // margin (lane 0's copies are the ones used).  vals[i]: logit of expert
 // lane + 32 i (-inf beyond E).
-__device__ __noinline__ void warp_topk(const float (&vals)[32], int E, int K, int lane, int *idx, float *w,
-                          float *margin) {
+__device__ __forceinline__ void warp_topk(const float (&vals)[32], int E, int K, int lane,
+                                          int (&idx)[kMaxK], float (&w)[kMaxK], float *margin) {
     uint32_t taken = 0;
     float topv[kMaxK + 1];
     int topi[kMaxK + 1];
@@ -557,630 +679,961 @@ __device__ __noinline__ void warp_topk(const float (&vals)[32], int E, int K, in
     *margin = K < E ? topv[K - 1] - topv[K] : INFINITY;
 }
 
+// Polls the E logits at z (tag), top-K, and writes the route of layer `tgt`
+// into route set `set` of the caller's buffers (lane 0, with to_global) and
+// into the CTA's current routes (with to_smem).  Warp-uniform result.
+__device__ __noinline__ bool route_from_logits(const uint64_t *z, uint32_t tag, int set, int tgt,
+                                               bool to_global, bool to_smem, uint32_t sleep_ns) {
+    const Ctx &cx = CX();
+    const int lane = threadIdx.x & 31;
+    float vals[32];
+    if (!poll_logits(z, cx.E, tag, lane, vals, sleep_ns)) return false;
+    int idx[kMaxK];
+    float w[kMaxK], margin;
+    warp_topk(vals, cx.E, cx.K, lane, idx, w, &margin);
+    if (lane == 0) {
+        for (int k = 0; k < cx.K; k++) {
+            if (to_global) {
+                cx.ridx[((size_t)set * cx.depth + tgt) * cx.K + k] = idx[k];
+                cx.rw[((size_t)set * cx.depth + tgt) * cx.K + k] = w[k];
+            }
+            if (to_smem) {
+                SM<int>(cx.sm_rcur)[tgt * cx.K + k] = idx[k];
+                SM<float>(cx.sm_rw)[tgt * cx.K + k] = w[k];
+            }
+        }
+        if (to_global) cx.rmargin[(size_t)set * cx.depth + tgt] = margin;
+    }
+    return true;
+}
+
 // ---------------------------------------------------------------- producer
+// All 32 lanes walk the same piece sequence; pieces are issued in batches of
+// up to 32 (lane i issues piece i of the batch) under three limits: ring
+// space, barrier pairs, and the bytes in flight (issued, not yet landed).
 template <int BITS>
-__device__ __noinline__ void producer(const Params &p, const Smem &s) {
+struct Producer {
+    const Params &p;
+    int lane;
     RingPos rp;
-    uint32_t rel = 0;       // pieces [rel, rp.q) are not yet released
-    uint64_t tail = 0;      // ring bytes before `tail` are free
-    bool ok = true;
-    auto issue = [&](int N, const Tmplt &t) -> bool {
-        const int *route = s.rcur + N * p.K;
+    uint32_t rel = 0, landed = 0;   // pieces [rel, q) not yet released; [landed, q) maybe in flight
+    uint64_t tail = 0;              // ring bytes before `tail` are free
+    uint64_t landed_end = 0;        // ring position up to which copies have landed
+    uint64_t issued_end = 0;        // ring position up to which copies were issued
+    uint32_t qb = 0;                // first piece of the open batch
+    int nb = 0;                     // pieces in the open batch
+    uint32_t bbytes = 0;
+    uint64_t bend = 0;
+    const uint8_t *my_src = nullptr;
+    uint32_t my_bytes = 0;
+    uint64_t my_start = 0;
+
+    __device__ __forceinline__ bool flush() {
+        if (nb == 0) return true;
+        const Ctx &cx = CX();
+        uint64_t *pend = SM<uint64_t>(cx.sm_pend);
+        const uint32_t qe = qb + nb;
+        // ring space and barrier pairs for the whole batch
+        while (rel < qe && (bend - tail > cx.ring_bytes || qe - 1 - rel >= (uint32_t)kNB)) {
+            if (!wait_bar_warp(bar_empty(rel % kNB), (rel / kNB) & 1)) return false;
+            tail = pend[rel % kNB];
+            rel++;
+            if (landed < rel) {
+                landed = rel;
+                landed_end = tail;
+            }
+        }
+        // bytes in flight
+        while (landed < qb && issued_end - landed_end + bbytes > cx.inflight) {
+            if (!wait_bar_warp(bar_full(landed % kNB), (landed / kNB) & 1)) return false;
+            landed_end = pend[landed % kNB];
+            landed++;
+        }
+        if (lane < nb) {
+            const uint32_t q = qb + lane;
+            pend[q % kNB] = my_start + my_bytes;
+            mbar_arrive_expect_tx(bar_full(q % kNB), my_bytes);
+            bulk_g2s(SM<uint8_t>(cx.sm_ring) + my_start % cx.ring_bytes, my_src, my_bytes,
+                     bar_full(q % kNB));
+        }
+        __syncwarp();
+        issued_end = bend;
+        qb = qe;
+        nb = 0;
+        bbytes = 0;
+        return true;
+    }
+
+    __device__ __forceinline__ bool add(const uint8_t *src, uint32_t bytes) {
+        const Ctx &cx = CX();
+        const uint32_t cap = cx.inflight / 2 > bytes ? cx.inflight / 2 : bytes;
+        if (nb == 32 || (nb > 0 && bbytes + bytes > cap))
+            if (!flush()) return false;
+        const uint64_t start = rp.place(bytes, cx.ring_bytes);
+        rp.q++;
+        if (lane == nb) {
+            my_src = src;
+            my_bytes = bytes;
+            my_start = start;
+        }
+        nb++;
+        bbytes += bytes;
+        bend = start + bytes;
+        return true;
+    }
+
+    // address of item 0 of group g in layer N
+    __device__ __forceinline__ const uint8_t *group_src(int N, const Grp &g, const int *route) {
+        const Ctx &cx = CX();
+        const LayerP &L = layer_of(p, N);
+        const uint8_t *blob = g.slot < cx.K ? L.pool + (size_t)route[g.slot] * cx.stride : L.shared;
+        switch (g.kind) {
+            case KGU: return blob + cx.gu_off;
+            case KFC1: return L.fc1x;
+            case KLX: return L.lx;
+            case KROUTER: return L.router;
+            default: return blob + cx.down_off;
+        }
+    }
+
+    __device__ __forceinline__ bool issue(int N, int ti) {
+        const Ctx &cx = CX();
+        const Tmplt &t = tmpls()[ti];
+        const int *route = SM<int>(cx.sm_rcur) + N * cx.K;
         for (int gi = 0; gi < t.n; gi++) {
             const Grp &g = t.g[gi];
-            const uint8_t *src = group_src(p, N, g, route);
-            const int per = max(1, kMaxPiece / (int)g.item_bytes);
+            const uint8_t *src = group_src(N, g, route);
+            const int per = piece_items<BITS>(g);
             for (int i0 = g.lo; i0 < g.hi; i0 += per) {
                 const uint32_t bytes = (uint32_t)min(per, g.hi - i0) * g.item_bytes;
-                const uint64_t start = rp.place(bytes, p.ring_bytes);
-                const uint32_t q = rp.q++;
-                while (rel < q && (start + bytes - tail > p.ring_bytes || q - rel >= (uint32_t)kNB)) {
-                    if (!wait_bar(p, s.empty + rel % kNB, (rel / kNB) & 1)) return false;
-                    tail = s.pend[rel % kNB];
-                    rel++;
-                }
-                s.pend[q % kNB] = start + bytes;
-                mbar_arrive_expect_tx(s.full + q % kNB, bytes);
-                bulk_g2s(s.ring + start % p.ring_bytes, src + (size_t)i0 * g.item_bytes, bytes,
-                         s.full + q % kNB);
+                if (!add(src + (size_t)i0 * g.item_bytes, bytes)) return false;
             }
         }
         return true;
-    };
-    for (int N = 0; N < p.depth && ok; N++) {
-        if (N == 0 && p.own0) {
-            if (!(ok = issue(0, s.T[T_R]))) break;
-            if (!(ok = wait_bar(p, s.route_bar, 0))) break;
-        }
-        // validate the route before it turns into addresses
-        for (int k = 0; k < p.K; k++)
-            if ((unsigned)s.rcur[N * p.K + k] >= (unsigned)p.E) {
-                raise_error(p, MOE_EINVAL);
-                ok = false;
-            }
-        if (!ok) break;
-        if (p.trace) p.trace[((size_t)blockIdx.x * p.depth + N) * kTrace + 9] = now_ns();
-        if (!(ok = issue(N, tmpl_A(p, s.T, N)))) break;
-        if (p.trace) p.trace[((size_t)blockIdx.x * p.depth + N) * kTrace + 10] = now_ns();
-        if (!(ok = issue(N, tmpl_B(p, s.T, N)))) break;
-        if (p.trace) p.trace[((size_t)blockIdx.x * p.depth + N) * kTrace + 11] = now_ns();
     }
-    // never leave the CTA with copies in flight: wait (bounded) for every
-    // piece not yet released
-    for (uint32_t q = rel; q < rp.q; q++) {
-        if (!mbar_try_wait(s.full + q % kNB, (q / kNB) & 1)) {
-            const uint64_t t0 = now_ns();
-            while (!mbar_try_wait(s.full + q % kNB, (q / kNB) & 1) && now_ns() - t0 < p.timeout_ns) {
+
+    __device__ __forceinline__ bool routes_valid(int N) {
+        const Ctx &cx = CX();
+        bool ok = true;
+        for (int k = 0; k < cx.K; k++)
+            if ((unsigned)SM<int>(cx.sm_rcur)[N * cx.K + k] >= (unsigned)cx.E) ok = false;
+        if (!ok && lane == 0) raise_error(MOE_EINVAL);
+        return ok;
+    }
+
+    __device__ __forceinline__ void run() {
+        const Ctx &cx = CX();
+        const int c = blockIdx.x;
+        bool ok = true;
+#pragma unroll 1
+        for (int N = 0; N < cx.depth && ok; N++) {
+            // phase 0: router rows (layer 0 routing with its own router; the
+            // producer then waits for the route), 1: phase A, 2: phase B
+#pragma unroll 1
+            for (int ph = N == 0 && cx.own0 ? 0 : 1; ph < 3 && ok; ph++) {
+                // validate the route before it turns into addresses
+                if (ph == 1 && !(ok = routes_valid(N))) break;
+                if (lane == 0) stamp_at(c, N, ST_PA + ph - 1 + (ph == 0));
+                ok = issue(N, ph == 0 ? T_R : ph == 1 ? tmpl_A_index(N) : T_B);
+                if (ok && ph == 0) ok = flush() && wait_bar_warp(bar(B_ROUTE), 0);
+            }
+            if (ok && lane == 0) stamp_at(c, N, ST_PE);
+        }
+        if (ok) flush();
+        // never leave the CTA with copies in flight: wait (bounded) for every
+        // piece that may not have landed (a barrier pair is reused only after
+        // its piece was released, hence landed)
+        if (lane == 0) {
+            const uint32_t q_end = qb;
+            const uint32_t from = q_end > (uint32_t)kNB && landed < q_end - kNB ? q_end - kNB : landed;
+            for (uint32_t q = from; q < q_end; q++) {
+                if (!mbar_try_wait(bar_full(q % kNB), (q / kNB) & 1)) {
+                    const uint64_t t0 = now_ns();
+                    while (!mbar_try_wait(bar_full(q % kNB), (q / kNB) & 1) &&
+                           now_ns() - t0 < cx.timeout_ns) {
+                    }
+                }
             }
         }
+        __syncwarp();
+    }
+};
+
+// ---------------------------------------------------------------- aux warp
+// Prepares each layer's small operands in shared memory (double-buffered by
+// layer parity), runs head fc2 of every layer once gelu(fc1 f) is complete,
+// and finally the top-K of the heads this CTA owns.
+__device__ __forceinline__ uint32_t tag_of(int N) { return CX().epoch * 64u + (uint32_t)N + 1u; }
+__device__ __forceinline__ uint32_t tag_router() { return CX().epoch * 64u + 63u; }
+
+// A columns of layer M's gate/up LoRA for this CTA's rows of x
+__device__ __noinline__ void aux_load_agu(const LayerP *L, float *agu, int lane) {
+    const Ctx &cx = CX();
+    const Tmplt &tb = tmpls()[T_B];
+    const int r2 = cx.rg + cx.ru, no = tb.o_hi - tb.o_lo;
+    const uint16_t *Ag = L->slora[0].A, *Au = L->slora[1].A;
+    #pragma unroll 1
+    for (int i = lane; i < no * r2; i += 32) {
+        const int o = tb.o_lo + i / r2, k = i % r2;
+        agu[i] = k < cx.rg ? half_f(Ag[(size_t)k * cx.d + o]) : half_f(Au[(size_t)(k - cx.rg) * cx.d + o]);
     }
 }
 
-// ---------------------------------------------------------------- route warp
-// Top-K of the heads' logits of the layers this CTA is responsible for;
-// writes the predicted routes for the next step.
-__device__ __noinline__ void route_warp(const Params &p, int c, int lane) {
-    const int nxt = (p.t + 1) % 3;
-    const uint32_t epoch = (uint32_t)ld_flag(ctrl(p) + C_EPOCH);
-    for (int N = c; N < p.depth; N += p.n_cta) {
-        if (!head_runs(p, N)) continue;
-        float vals[32];
-        if (!poll_logits(p, tagged(p, p.off_z) + (size_t)N * p.E, p.E, epoch * 64u + N + 1, lane,
-                         vals))
-            return;
-        int idx[kMaxK];
-        float w[kMaxK], margin;
-        warp_topk(vals, p.E, p.K, lane, idx, w, &margin);
-        const int tgt = N + 1 < p.depth ? N + 1 : 0;
-        if (lane == 0) {
-            for (int k = 0; k < p.K; k++) {
-                p.ridx[((size_t)nxt * p.depth + tgt) * p.K + k] = idx[k];
-                p.rw[((size_t)nxt * p.depth + tgt) * p.K + k] = w[k];
+// layer 0's x partials for the gate/up LoRA over this CTA's rows of x0
+__device__ __noinline__ void aux_vp0(const LayerP *L0, int c, int lane) {
+    const Ctx &cx = CX();
+    float *agu = prep_of(1, cx.pp_agu);           // buffer 1 is free until layer 1 is prepared
+    aux_load_agu(L0, agu, lane);
+    __syncwarp();
+    const Tmplt &tb = tmpls()[T_B];
+    const int r2 = cx.rg + cx.ru;
+    for (int k = lane; k < r2; k += 32) {
+        float a = 0.0f;
+        #pragma unroll 1
+        for (int o = tb.o_lo; o < tb.o_hi; o++) a = fmaf(agu[(o - tb.o_lo) * r2 + k], cx.x0[o], a);
+        put_tagged(tagged(cx.off_vp) + (size_t)c * 2 * kMaxR + k, tag_of(0), a);
+    }
+    __syncwarp();
+}
+
+// the routes of layer N (this step's and the previous one's) index the tables
+// and the routed LoRA matrices: check them before any use
+__device__ __forceinline__ bool aux_routes_ok(int N) {
+    const Ctx &cx = CX();
+    bool ok = true;
+    for (int k = 0; k < cx.K; k++)
+        ok = ok && (unsigned)SM<int>(cx.sm_rcur)[N * cx.K + k] < (unsigned)cx.E &&
+             (unsigned)SM<int>(cx.sm_rprev)[N * cx.K + k] < (unsigned)cx.E;
+    return ok;
+}
+
+__device__ __noinline__ void aux_prep(const LayerP *Lp, const LayerP *Lnext, int N, int lane) {
+    const Ctx &cx = CX();
+    const LayerP &L = *Lp;
+    const Tmplt &ta = tmpls()[tmpl_A_index(N)], &tb = tmpls()[T_B];
+    const int *cur = SM<int>(cx.sm_rcur) + N * cx.K, *prev = SM<int>(cx.sm_rprev) + N * cx.K;
+    // LoRA scales of this layer
+    if (lane == 0) {
+        float *sc = prep_of(N, cx.pp_scale);
+        sc[SC_G] = L.slora[0].scale;
+        sc[SC_U] = L.slora[1].scale;
+        sc[SC_DR] = L.lora[2].scale;
+        sc[SC_DS] = L.slora[2].scale;
+    }
+    // K-hot table sums (+ bias) of this CTA's fc1 and l rows
+    if (head_runs(N)) {
+        float *ts = prep_of(N, cx.pp_tsum);
+        const int n1 = ta.f1hi - ta.f1lo, nl = ta.lhi - ta.llo;
+        #pragma unroll 1
+        for (int i = lane; i < n1 + nl; i += 32) {
+            const bool fc1 = i < n1;
+            const int row = fc1 ? ta.f1lo + i : ta.llo + (i - n1);
+            const int width = fc1 ? cx.H : cx.E;
+            const uint16_t *tab = fc1 ? L.fc1_tab : L.l_tab;
+            const uint16_t *bias = fc1 ? L.b1 : L.bl;
+            float a = 0.0f;
+            if (tab) {
+                for (int k = 0; k < cx.K; k++) a += half_f(tab[(size_t)cur[k] * width + row]);
+                for (int k = 0; k < cx.K; k++) a += half_f(tab[(size_t)(cx.E + prev[k]) * width + row]);
             }
-            p.rmargin[(size_t)nxt * p.depth + tgt] = margin;
+            if (bias) a += half_f(bias[row]);
+            ts[i] = a;
         }
+    }
+    // B rows of this CTA's gate/up LoRA rows
+    if (cx.gu_slot >= 0) {
+        float *bgu = prep_of(N, cx.pp_bgu);
+        const int gs = cx.gu_slot, r2 = cx.rg + cx.ru;
+        const int np = ta.phi[gs] - ta.plo[gs];
+        const uint16_t *Bg = L.slora[0].B, *Bu = L.slora[1].B;
+        #pragma unroll 1
+        for (int i = lane; i < np * r2; i += 32) {
+            const int f = ta.plo[gs] + i / r2, k = i % r2;
+            bgu[i] = k < cx.rg ? half_f(Bg[(size_t)f * cx.rg + k]) : half_f(Bu[(size_t)f * cx.ru + (k - cx.rg)]);
+        }
+    }
+    // down LoRA: A_d columns of this CTA's gate/up rows, B_d rows of its outputs
+    if (cx.dl_mask) {
+        float *adn = prep_of(N, cx.pp_adn), *bd = prep_of(N, cx.pp_bd);
+        const int no = tb.o_hi - tb.o_lo;
+        for (int sl = 0; sl < cx.S; sl++) {
+            if (!(cx.dl_mask >> sl & 1u)) continue;
+            const int r = dl_rank(sl), j = dl_index(sl);
+            const uint16_t *A = lora_a(L, cx.K, cur, sl, 2), *B = lora_bm(L, cx.K, cur, sl, 2);
+            const int np = ta.phi[sl] - ta.plo[sl];
+            #pragma unroll 1
+            for (int i = lane; i < np * r; i += 32) {
+                const int f = ta.plo[sl] + i / r, k = i % r;
+                adn[(ta.pbase[sl] + i / r) * cx.rd + k] = half_f(A[(size_t)k * cx.F + f]);
+            }
+            #pragma unroll 1
+            for (int i = lane; i < no * r; i += 32) {
+                const int o = tb.o_lo + i / r, k = i % r;
+                bd[(j * cx.max_orows + i / r) * cx.rd + k] = half_f(B[(size_t)o * r + k]);
+            }
+        }
+    }
+    // A columns of the next layer's gate/up LoRA (for its x partials)
+    if (cx.gu_slot >= 0 && Lnext) aux_load_agu(Lnext, prep_of(N, cx.pp_agu), lane);
+}
+
+// fc2 rows of head N: z = fc2 gelu(fc1 f) + b2 + l f, published per row
+__device__ __noinline__ bool aux_fc2(const LayerP *Lp, int N, int lane) {
+    const Ctx &cx = CX();
+    const Tmplt &tb = tmpls()[T_B];
+    const int ne = tb.e_hi - tb.e_lo;
+    const uint32_t tg = tag_of(N);
+    if (cx.H == 0 || ne <= 0) return true;
+    uint8_t *frec = SM<uint8_t>(cx.sm_frec);
+    // records of this CTA's rows (plain 16-byte loads)
+    const int q16 = cx.rec_H / 16;
+    #pragma unroll 1
+    for (int i = lane; i < ne * q16; i += 32)
+        reinterpret_cast<uint4 *>(frec)[i] =
+            *reinterpret_cast<const uint4 *>(Lp->fc2 + (size_t)tb.e_lo * cx.rec_H + (size_t)i * 16);
+    // every CTA has finished phase A of layer N (fc1 and l rows published)
+    if (!poll_flags(cx.off_hflag, tg, lane, 128)) return false;
+    // gelu(fc1 f) (lane j: value j of every 32-value chunk, into graw) and l f
+    // of this CTA's rows (lane i: row i), then staged chunk by chunk
+    const int nch = cx.H / 32;
+    uint8_t *gf = SM<uint8_t>(cx.sm_gf);
+    float *gsc = SM<float>(cx.sm_gsc), *ghat = SM<float>(cx.sm_ghat), *graw = SM<float>(cx.sm_graw);
+    float zl = 0.0f;
+    if (!read_words(ws_words(), nch + (lane < ne ? 1 : 0), tg,
+                    [&](int i) {
+                        return i < nch ? cx.off_ga / 8 + (uint32_t)(N * cx.H + i * 32 + lane)
+                                       : cx.off_zl / 8 + (uint32_t)(N * cx.E + tb.e_lo + lane);
+                    },
+                    [&](int i, float v) {
+                        if (i < nch) graw[i * 32 + lane] = v;
+                        else zl = v;
+                    },
+                    [] {}))
+        return false;
+    __syncwarp();
+#pragma unroll 1
+    for (int ch = 0; ch < nch; ch++) {
+        const float v = graw[ch * 32 + lane];
+        stage_chunk<4>(&v, lane, gf, ch, nch, gsc, ghat);
+    }
+    __syncwarp();
+    const int lpr = pow2_floor32(nch), rpw = 32 / lpr;
+    const int sub = lane % lpr, rsub = lane / lpr;
+    for (int i0 = 0; i0 < ne; i0 += rpw) {
+        const int i = i0 + rsub;
+        float a;
+        rows_dot<4, 1>(frec + (size_t)(i < ne ? i : 0) * cx.rec_H, 0, cx.H, gf, gsc, ghat, sub, lpr, &a);
+        const float zli = __shfl_sync(0xffffffffu, zl, i & 31);
+        if (i < ne && sub == 0) {
+            const int e = tb.e_lo + i;
+            const float b = Lp->b2 ? half_f(Lp->b2[e]) : 0.0f;
+            put_tagged(tagged(cx.off_z) + (size_t)N * cx.E + e, tg, a + b + zli);
+        }
+    }
+    __syncwarp();
+    return true;
+}
+
+template <int BITS>
+__device__ __noinline__ void aux_main(const Params &p, int c, int lane) {
+    const Ctx &cx = CX();
+    if (cx.gu_slot >= 0) aux_vp0(&p.layer[0], c, lane);
+    for (int N = 0; N < cx.depth; N++) {
+        if (N >= 2 && !wait_bar_warp(bar(B_PREP_EMPTY0 + (N & 1)), ((N >> 1) - 1) & 1)) return;
+        if (N == 0 && cx.own0 && !wait_bar_warp(bar(B_ROUTE), 0)) return;
+        if (!aux_routes_ok(N)) {
+            if (lane == 0) raise_error(MOE_EINVAL);
+            return;
+        }
+        aux_prep(&layer_of(p, N), N + 1 < cx.depth ? &layer_of(p, N + 1) : nullptr, N, lane);
+        __syncwarp();
+        if (lane == 0) {
+            stamp_at(c, N, ST_AUXP);
+            mbar_arrive(bar(B_PREP_FULL0 + (N & 1)));
+        }
+        if (N >= 1 && head_runs(N - 1)) {
+            if (!aux_fc2(&layer_of(p, N - 1), N - 1, lane)) return;
+            if (lane == 0) stamp_at(c, N - 1, ST_AUXF);
+        }
+    }
+    if (head_runs(cx.depth - 1) && !aux_fc2(&layer_of(p, cx.depth - 1), cx.depth - 1, lane)) return;
+    // top-K of the heads this CTA owns: routes for the next step
+    const int nxt = (cx.t + 1) % 3;
+    for (int N = c; N < cx.depth; N += cx.n_cta) {
+        if (!head_runs(N)) continue;
+        const int tgt = N + 1 < cx.depth ? N + 1 : 0;
+        if (!route_from_logits(tagged(cx.off_z) + (size_t)N * cx.E, tag_of(N), nxt, tgt, true,
+                               false, 256))
+            return;
     }
 }
 
 // ---------------------------------------------------------------- consumers
+// true in the warp that arrives last at counter `cnt` (reset for reuse);
+// every warp's shared-memory writes before the call are visible to it
+__device__ __forceinline__ bool last_warp(int *cnt) {
+    const int lane = threadIdx.x & 31;
+    __syncwarp();
+    int old = 0;
+    if (lane == 0) {
+        __threadfence_block();
+        old = atomicAdd(cnt, 1);
+    }
+    old = __shfl_sync(0xffffffffu, old, 0);
+    if (old != kNW - 1) return false;
+    __threadfence_block();
+    if (lane == 0) *cnt = 0;
+    return true;
+}
+
+// x of layer N (the previous layer's out, or x0), staged for the GEMVs (and,
+// with 2-bit experts, in the int4 layout for the heads); the raw values go to
+// the residual stream.  Warp w reads and stages chunks w, w+kNW, ... (lane j:
+// values j, j+32 of a chunk).  With want_vp also the partial A x of every CTA
+// for the gate/up LoRA (lane k: component k, warp w: CTAs w, w+kNW, ...),
+// summed per lane in CTA order; the last warp sums the warps' sums into vx and
+// the sums of squares into 1/rms.  Called after the flags of layer N-1.
+template <int BITS>
+__device__ __noinline__ bool phase_x(int N, bool want_x, bool want_vp, int warp, int lane) {
+    constexpr int VALS = 128 / BITS, PER = VALS / 32;
+    const Ctx &cx = CX();
+    const int d = cx.d, nch = d / VALS;
+    float *stream = SM<float>(cx.sm_stream) + (size_t)(N & 1) * d;
+    const int ncw = want_x && warp < nch ? (nch - warp + kNW - 1) / kNW : 0;   // chunks of this warp
+    const int nx = ncw * PER;
+    auto xpos = [&](int i) { return (warp + kNW * (i / PER)) * VALS + lane + 32 * (i % PER); };
+    if (N == 0) {
+#pragma unroll 1
+        for (int i = 0; i < nx; i++) stream[xpos(i)] = cx.x0[xpos(i)];
+    } else if (!read_words(ws_words(), nx, tag_of(N - 1),
+                           [&](int i) { return cx.off_out / 8 + (uint32_t)xpos(i); },
+                           [&](int i, float v) { stream[xpos(i)] = v; }, [] {})) {
+        return false;
+    }
+    float va = 0.0f;
+    if (want_vp) {
+        const int nvo = (cx.n_cta - warp + kNW - 1) / kNW;               // CTAs of this warp
+        const int n = lane < cx.rg + cx.ru ? nvo : 0;
+        if (!read_words(ws_words(), n, tag_of(N),
+                        [&](int j) { return cx.off_vp / 8 + (uint32_t)((warp + kNW * j) * 2 * kMaxR + lane); },
+                        [&](int, float v) { va += v; }, [&] { va = 0.0f; }))
+            return false;
+    }
+    __syncwarp();
+    uint8_t *xf = SM<uint8_t>(cx.sm_xf), *xf4 = SM<uint8_t>(cx.sm_xf4);
+    float *xsc = SM<float>(cx.sm_xsc), *xhat = SM<float>(cx.sm_xhat);
+    float *xsc4 = SM<float>(cx.sm_xsc4), *xhat4 = SM<float>(cx.sm_xhat4);
+    float ss = 0.0f;
+#pragma unroll 1
+    for (int i = 0; i < ncw; i++) {
+        const int ch = warp + kNW * i;
+        float v[PER];
+#pragma unroll
+        for (int m = 0; m < PER; m++) {
+            v[m] = stream[ch * VALS + lane + 32 * m];
+            ss = fmaf(v[m], v[m], ss);
+        }
+        stage_chunk<BITS>(v, lane, xf, ch, nch, xsc, xhat);
+        if (BITS != 4) {
+#pragma unroll
+            for (int m = 0; m < PER; m++)
+                stage_chunk<4>(&v[m], lane, xf4, ch * PER + m, d / 32, xsc4, xhat4);
+        }
+    }
+    float *mf = misc_f();
+    float *vpw = SM<float>(cx.sm_vpw);
+    if (want_x) {
+        ss = warp_sum(ss, 32);
+        if (lane == 0) mf[M_SS + warp] = ss;
+    }
+    if (want_vp) vpw[warp * 2 * kMaxR + lane] = va;
+    if (last_warp(misc_i() + M_CNT_X)) {
+        if (want_x && lane == 0) {
+            float tot = 0.0f;
+            for (int w = 0; w < kNW; w++) tot += mf[M_SS + w];
+            mf[M_INV] = N > 0 ? 1.0f / sqrtf(tot / d + 1e-6f) : 1.0f;
+        }
+        if (want_vp) {
+            float a = 0.0f;
+            for (int w = 0; w < kNW; w++) a += vpw[w * 2 * kMaxR + lane];
+            SM<float>(cx.sm_vx)[lane] = a;
+        }
+    }
+    return true;
+}
+
+// h of every slot (read into hraw, then staged per slot: warp w takes chunks
+// w, w+kNW, ...); with down LoRA also the partial A_d h of every owner CTA
+// (lane k: component k; list entry e = slot << 16 | owner, warp w takes
+// entries w, w+kNW, ...), summed per warp in list order into vdw and over the
+// warps into vd by the last warp.  Called after the flags of phase A.
+template <int BITS>
+__device__ __noinline__ bool phase_h(int N, int warp, int lane) {
+    constexpr int VALS = 128 / BITS, PER = VALS / 32;
+    const Ctx &cx = CX();
+    const int ai = tmpl_A_index(N);
+    const int cps = cx.F / VALS;                    // chunks per slot
+    const int nch = cx.S * cps;
+    const int ncw = warp < nch ? (nch - warp + kNW - 1) / kNW : 0;
+    const uint32_t tg = tag_of(N);
+    float *hraw = SM<float>(cx.sm_hraw);
+    // chunk ch of the concatenated slots covers h[ch * VALS, (ch+1) * VALS)
+    auto hpos = [&](int i) { return (warp + kNW * (i / PER)) * VALS + lane + 32 * (i % PER); };
+    if (!read_words(ws_words(), ncw * PER, tg, [&](int i) { return cx.off_h / 8 + (uint32_t)hpos(i); },
+                    [&](int i, float v) { hraw[hpos(i)] = v; }, [] {}))
+        return false;
+    if (cx.dl_mask) {
+        const int nlist = misc_i()[M_VDP_N0 + (ai == T_A_HEAD ? 0 : 1)];
+        const uint32_t *list = SM<uint32_t>(cx.sm_vdpl) + (ai == T_A_HEAD ? 0 : cx.n_dl * cx.n_cta);
+        const int nv = warp < nlist ? (nlist - warp + kNW - 1) / kNW : 0;
+        float *vdw = SM<float>(cx.sm_vdw) + warp * cx.n_dl * kMaxR;
+        auto zero = [&] {
+            for (int j = 0; j < cx.n_dl; j++) vdw[j * kMaxR + lane] = 0.0f;
+        };
+        zero();
+        // a lane at or above an entry's rank reads h[0] instead (published in
+        // this phase, so current) and ignores it
+        auto ent = [&](int j) { return list[warp + kNW * j]; };
+        if (!read_words(ws_words(), nv, tg,
+                        [&](int j) {
+                            const uint32_t e = ent(j);
+                            const uint32_t sl = e >> 16;
+                            return lane < dl_rank((int)sl)
+                                       ? cx.off_vdp / 8 + (sl * cx.n_cta + (e & 0xffffu)) * kMaxR + lane
+                                       : cx.off_h / 8;
+                        },
+                        [&](int j, float v) {
+                            const int sl = (int)(ent(j) >> 16);
+                            if (lane < dl_rank(sl)) vdw[dl_index(sl) * kMaxR + lane] += v;
+                        },
+                        zero))
+            return false;
+    }
+    __syncwarp();
+    uint8_t *hf = SM<uint8_t>(cx.sm_hf);
+    float *hsc = SM<float>(cx.sm_hsc), *hhat = SM<float>(cx.sm_hhat);
+#pragma unroll 1
+    for (int i = 0; i < ncw; i++) {
+        const int ch = warp + kNW * i, sc = ch / cps, cl = ch % cps;
+        float v[PER];
+#pragma unroll
+        for (int m = 0; m < PER; m++) v[m] = hraw[ch * VALS + lane + 32 * m];
+        stage_chunk<BITS>(v, lane, hf + (size_t)sc * cx.F * 2, cl, cps, hsc + sc * cps, hhat + sc * cps);
+    }
+    if (cx.dl_mask && last_warp(misc_i() + M_CNT_H)) {
+        float *vd = SM<float>(cx.sm_vd), *vdw0 = SM<float>(cx.sm_vdw);
+        for (int j = 0; j < cx.n_dl; j++) {
+            float a = 0.0f;
+            for (int w = 0; w < kNW; w++) a += vdw0[(w * cx.n_dl + j) * kMaxR + lane];
+            vd[j * kMaxR + lane] = a;
+        }
+    }
+    return true;
+}
+
+// ---- tasks -----------------------------------------------------------
+// Gate/up row pairs: h = silu(g) * u (+ gate/up LoRA), published; the
+// partial A_d h of a down-LoRA slot accumulates in vdacc[warp].
+template <int BITS>
+__device__ __forceinline__ void task_gu(int N, int gi, const uint8_t *base, int i, int cnt, int lpr,
+                                     float inv, int warp, int lane) {
+    const Ctx &cx = CX();
+    const Tmplt &t = tmpls()[tmpl_A_index(N)];
+    const Grp &g = t.g[gi];
+    const int sub = lane % lpr, rsub = lane / lpr;
+    const int f = i + rsub;
+    const bool ok = rsub < cnt;
+    const int sl = g.slot;
+    float r2v[2];
+    rows_dot<BITS, 2>(base + (size_t)(ok ? rsub : 0) * g.item_bytes, cx.rec_d, cx.d,
+                      SM<uint8_t>(cx.sm_xf), SM<float>(cx.sm_xsc), SM<float>(cx.sm_xhat), sub, lpr,
+                      r2v);
+    float gg = r2v[0] * inv, uu = r2v[1] * inv;
+    if (sl == cx.gu_slot) {
+        const float *sc = prep_of(N, cx.pp_scale);
+        const float *bgu = prep_of(N, cx.pp_bgu) + (ok ? f - t.plo[sl] : 0) * (cx.rg + cx.ru);
+        const float *vx = SM<float>(cx.sm_vx);
+        float a = 0.0f, b = 0.0f;
+        if (ok) {
+            for (int k = sub; k < cx.rg; k += lpr) a = fmaf(bgu[k], vx[k], a);
+            for (int k = sub; k < cx.ru; k += lpr) b = fmaf(bgu[cx.rg + k], vx[cx.rg + k], b);
+        }
+        gg += sc[SC_G] * inv * warp_sum(a, lpr);
+        uu += sc[SC_U] * inv * warp_sum(b, lpr);
+    }
+    const float h = silu_f(gg) * uu;
+    if (ok && sub == 0) put_tagged(tagged(cx.off_h) + (size_t)sl * cx.F + f, tag_of(N), h);
+    if (cx.dl_mask >> sl & 1u) {
+        const int r = dl_rank(sl), j = dl_index(sl);
+        const float *adn = prep_of(N, cx.pp_adn) + (t.pbase[sl] + (ok ? f - t.plo[sl] : 0)) * cx.rd;
+        float *vdacc = SM<float>(cx.sm_vdacc) + (warp * cx.n_dl + j) * kMaxR;
+        for (int k0 = 0; k0 < r; k0 += lpr) {
+            const int k = k0 + sub;
+            float a = (ok && k < r) ? adn[k] * h : 0.0f;
+            for (int o = lpr; o < 32; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+            if (rsub == 0 && k < r) vdacc[k] += a;
+        }
+    }
+}
+
+// fc1 / l / router rows on x, with the K-hot table sums and the bias.
+template <int BITS>
+__device__ __forceinline__ void task_head(int N, int ti, int gi, const uint8_t *base, int i, int cnt,
+                                       int lpr, float inv, int lane) {
+    const Ctx &cx = CX();
+    const Tmplt &t = tmpls()[ti];
+    const Grp &g = t.g[gi];
+    const int sub = lane % lpr, rsub = lane / lpr;
+    const int row = i + rsub;
+    const bool ok = rsub < cnt;
+    float a;
+    rows_dot<4, 1>(base + (size_t)(ok ? rsub : 0) * g.item_bytes, 0, cx.d, SM<uint8_t>(cx.sm_xf4),
+                   SM<float>(cx.sm_xsc4), SM<float>(cx.sm_xhat4), sub, lpr, &a);
+    if (ok && sub == 0) {
+        a *= inv;
+        const uint32_t tg = tag_of(N);
+        if (g.kind == KFC1) {
+            a += prep_of(N, cx.pp_tsum)[row - t.f1lo];
+            put_tagged(tagged(cx.off_ga) + (size_t)N * cx.H + row, tg, gelu_erf_f(a));
+        } else if (g.kind == KLX) {
+            a += prep_of(N, cx.pp_tsum)[(t.f1hi - t.f1lo) + row - t.llo];
+            if (cx.H > 0) put_tagged(tagged(cx.off_zl) + (size_t)N * cx.E + row, tg, a);
+            else put_tagged(tagged(cx.off_z) + (size_t)N * cx.E + row, tg, a);
+        } else {
+            put_tagged(tagged(cx.off_zr) + row, tag_router(), a);
+        }
+    }
+}
+
+// Down rows of one slot for this CTA's outputs; the warp owning output o
+// accumulates w_s y_s(o) over the slots and, at the last slot, combines:
+// out = residual + sum, published (with its share of the next layer's
+// gate/up LoRA partial, accumulated in vnw[warp]).
+template <int BITS>
+__device__ __forceinline__ void task_down(int N, int gi, const uint8_t *base, int i, int cnt, int lpr,
+                                       int warp, int lane) {
+    constexpr int VALS = 128 / BITS;
+    const Ctx &cx = CX();
+    const Tmplt &t = tmpls()[T_B];
+    const Grp &g = t.g[gi];
+    const int sub = lane % lpr, rsub = lane / lpr;
+    const int o = i + rsub;
+    const bool ok = rsub < cnt;
+    const int sl = g.slot;
+    float y;
+    rows_dot<BITS, 1>(base + (size_t)(ok ? rsub : 0) * g.item_bytes, 0, cx.F,
+                      SM<uint8_t>(cx.sm_hf) + (size_t)sl * cx.F * 2,
+                      SM<float>(cx.sm_hsc) + sl * (cx.F / VALS),
+                      SM<float>(cx.sm_hhat) + sl * (cx.F / VALS), sub, lpr, &y);
+    if (cx.dl_mask >> sl & 1u) {
+        const int r = dl_rank(sl), j = dl_index(sl);
+        const float *bd = prep_of(N, cx.pp_bd) + (j * cx.max_orows + (ok ? o - t.o_lo : 0)) * cx.rd;
+        const float *vd = SM<float>(cx.sm_vd) + j * kMaxR;
+        float a = 0.0f;
+        for (int k = sub; k < r; k += lpr) a = fmaf(bd[k], vd[k], a);
+        y += prep_of(N, cx.pp_scale)[sl < cx.K ? SC_DR : SC_DS] * warp_sum(a, lpr);
+    }
+    const float wgt = sl < cx.K ? SM<float>(cx.sm_rw)[N * cx.K + sl] : 1.0f;
+    float outv = 0.0f;
+    if (ok && sub == 0) {
+        float *cb = SM<float>(cx.sm_comb) + (o - t.o_lo);
+        const float acc = fmaf(wgt, y, sl == 0 ? 0.0f : *cb);
+        *cb = acc;
+        if (sl == cx.S - 1) {
+            outv = SM<float>(cx.sm_stream)[(size_t)(N & 1) * cx.d + o] + acc;
+            if (N + 1 < cx.depth) put_tagged(tagged(cx.off_out) + o, tag_of(N), outv);
+            else cx.out[o] = outv;
+        }
+    }
+    if (sl == cx.S - 1 && cx.gu_slot >= 0 && N + 1 < cx.depth) {
+        const int r2 = cx.rg + cx.ru, rpw = 32 / lpr;
+        const float *agu = prep_of(N, cx.pp_agu);
+        float *vn = SM<float>(cx.sm_vnw) + warp * 2 * kMaxR;
+        float a0 = 0.0f;
+        for (int rg = 0; rg < rpw; rg++) {
+            const float ov = __shfl_sync(0xffffffffu, outv, rg * lpr);
+            if (rg < cnt && lane < r2) a0 = fmaf(agu[(i + rg - t.o_lo) * r2 + lane], ov, a0);
+        }
+        vn[lane] += a0;
+    }
+}
+
+// End of phase A: this CTA's h rows (and fc1 / l rows) are out.  Every warp
+// fences its writes; the last one publishes, for the owners of a down-LoRA
+// slot's gate/up rows, the partial A_d h (sum of the warps' partials), then
+// the CTA's flag.
+__device__ __noinline__ void publish_a(int N, int c, int lane) {
+    __threadfence();
+    if (!last_warp(misc_i() + M_CNT_A)) return;
+    const Ctx &cx = CX();
+    const Tmplt &ta = tmpls()[tmpl_A_index(N)];
+    const uint32_t tg = tag_of(N);
+    for (int sl = 0; sl < cx.S; sl++) {
+        if (!(cx.dl_mask >> sl & 1u) || c < ta.own0[sl] || c > ta.own1[sl]) continue;
+        const int r = dl_rank(sl), j = dl_index(sl);
+        if (lane < r) {
+            float a = 0.0f;
+            for (int w = 0; w < kNW; w++) {
+                float *v = SM<float>(cx.sm_vdacc) + (w * cx.n_dl + j) * kMaxR + lane;
+                a += *v;
+                *v = 0.0f;
+            }
+            put_tagged(tagged(cx.off_vdp) + ((size_t)sl * cx.n_cta + c) * kMaxR + lane, tg, a);
+        }
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) put_flag(flag_of(cx.off_hflag, c), tg);
+}
+
+// End of phase B: this CTA's rows of out are published.  The last warp
+// publishes the next layer's gate/up LoRA partial over those rows (sum of the
+// warps' partials), then the CTA's flag.
+__device__ __noinline__ void publish_d(int N, int c, int lane) {
+    const Ctx &cx = CX();
+    __threadfence();
+    if (!last_warp(misc_i() + M_CNT_D)) return;
+    const uint32_t tg = tag_of(N);
+    if (cx.gu_slot >= 0) {
+        const int r2 = cx.rg + cx.ru;
+        float *vnw = SM<float>(cx.sm_vnw);
+        float a = 0.0f;
+        for (int w = 0; w < kNW; w++) {
+            a += vnw[w * 2 * kMaxR + lane];
+            vnw[w * 2 * kMaxR + lane] = 0.0f;
+        }
+        if (lane < r2) put_tagged(tagged(cx.off_vp) + (size_t)c * 2 * kMaxR + lane, tag_of(N + 1), a);
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) put_flag(flag_of(cx.off_xflag, c), tg);
+}
+
+// Ring position and task rotation of a consumer warp, carried from one
+// template's pieces to the next.
+struct RunState {
+    uint64_t head;
+    uint32_t q, tasks, ok;
+};
+
+// Consumes this CTA's pieces of template ti, in the producer's order; warp
+// tasks of rpw items go round-robin to the consumer warps (down rows: by
+// output row, the same warp in every slot).  A leaf function: the tasks are
+// inlined, so no loop state is saved around calls.
+template <int BITS>
+__device__ __noinline__ RunState run_tmpl(int N, int ti, float inv, int warp, int lane, RunState st) {
+    const Ctx &cx = CX();
+    const Tmplt &t = tmpls()[ti];
+    const uint8_t *ring = SM<uint8_t>(cx.sm_ring);
+    RingPos rp;
+    rp.head = st.head;
+    rp.q = st.q;
+    uint32_t tasks = st.tasks;
+    for (int gi = 0; gi < t.n; gi++) {
+        const Grp &g = t.g[gi];
+        const int kind = g.kind, lo = g.lo, hi = g.hi;
+        const uint32_t ib = g.item_bytes;
+        const int per = piece_items<BITS>(g);
+        const int lpr = pow2_floor32(item_chunks<BITS>(g));
+        const int rpw = 32 / lpr;
+        for (int i0 = lo; i0 < hi; i0 += per) {
+            const int cnt = min(per, hi - i0);
+            const uint64_t start = rp.place((uint32_t)cnt * ib, cx.ring_bytes);
+            const uint32_t q = rp.q++;
+            if (!wait_bar_warp_inl(bar_full(q % kNB), (q / kNB) & 1)) return RunState{rp.head, rp.q, tasks, 0u};
+            const uint8_t *base = ring + start % cx.ring_bytes;
+            const int ntask = (cnt + rpw - 1) / rpw;
+            const int k0 = kind == KDOWN ? (kNW + warp - ((i0 - lo) / rpw) % kNW) % kNW
+                                         : (int)((kNW + warp - tasks % kNW) % kNW);
+            for (int k = k0; k < ntask; k += kNW) {
+                const int li = k * rpw;
+                const uint8_t *b = base + (size_t)li * ib;
+                const int n = min(rpw, cnt - li);
+                if (kind == KGU) task_gu<BITS>(N, gi, b, i0 + li, n, lpr, inv, warp, lane);
+                else if (kind == KDOWN) task_down<BITS>(N, gi, b, i0 + li, n, lpr, warp, lane);
+                else task_head<BITS>(N, ti, gi, b, i0 + li, n, lpr, inv, lane);
+            }
+            if (kind != KDOWN) tasks += ntask;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty(q % kNB));
+        }
+    }
+    return RunState{rp.head, rp.q, tasks, 1u};
+}
+
 template <int BITS>
 struct Consumer {
-    const Params &p;
-    const Smem &s;
     int c, warp, lane;   // warp: 0 .. kNW-1
-    uint32_t epoch;
     RingPos rp;
-    uint32_t nsync = 0;
-    float inv = 1.0f;    // 1/rms of this layer's input
-    float vdp0 = 0.0f, vdp1 = 0.0f;   // partial A_d h, by slot parity
-    int trace_gu = 0;
-
-    static constexpr int kT = kNW * 32;
-    static constexpr int VALS = 128 / BITS;
-    __device__ uint32_t tag(int N) const { return epoch * 64u + (uint32_t)N + 1u; }
-    __device__ uint32_t tag_router() const { return epoch * 64u + 63u; }
-    __device__ int tid() const { return warp * 32 + lane; }
-    __device__ void stamp(int N, int k) const {
-        if (p.trace && warp == 0 && lane == 0)
-            p.trace[((size_t)c * p.depth + N) * kTrace + k] = now_ns();
-    }
+    uint32_t nsync = 0, xuses = 0, huses = 0, tasks = 0;
 
     // barrier among the consumer warps (bounded)
-    __device__ bool sync() {
+    __device__ __forceinline__ bool sync() {
         __syncwarp();
-        if (lane == 0) mbar_arrive(s.cons_bar);
-        const bool ok = wait_bar_warp(p, s.cons_bar, nsync & 1);
+        if (lane == 0) mbar_arrive(bar(B_CONS));
+        const bool ok = wait_bar_warp(bar(B_CONS), nsync & 1);
         nsync++;
         __syncwarp();
         return ok;
     }
 
-    // Polls the tagged words of `nvec` vectors of `vec` values at w and stages
-    // them chunk by chunk (VB-bit chunks of vb values): warp w takes chunks
-    // w, w+kNW, ...; lane j polls values j, j+32, ... of a chunk.  Vector vi is
-    // staged at xf + vi*vec*2 bytes with scales/xhat at sc/hat + vi*(vec/vb).
-    // Plain values go to plain[] if not null; ss accumulates their squares.
-    template <int VB>
-    __device__ __noinline__ bool poll_chunks(const uint64_t *w, int nvec, int vec, uint32_t tg,
-                                             uint8_t *xf, float *sc, float *hat, float *plain,
-                                             float *ss) {
-        constexpr int vb = 128 / VB;              // values per chunk
-        constexpr int per = vb / 32;              // values per lane per chunk
-        const int cpv = vec / vb;                 // chunks per vector
-        const int nchunks = nvec * cpv;
-        constexpr int CB = 8 / per;               // chunks per poll batch
-        bool lok = true;
-        for (int ch0 = warp; ch0 < nchunks; ch0 += kNW * CB) {
-            int idx[8];
-            float val[8];
-            int cnt = 0;
-#pragma unroll
-            for (int b = 0; b < CB; b++) {
-                const int ch = ch0 + b * kNW;
-#pragma unroll
-                for (int m = 0; m < per; m++) {
-                    idx[b * per + m] = ch * vb + lane + 32 * m;
-                    val[b * per + m] = 0.0f;
-                }
-                if (ch < nchunks) cnt = (b + 1) * per;
-            }
-            if (lok) lok = poll_set(p, w, idx, cnt, tg, val);
-#pragma unroll
-            for (int b = 0; b < CB; b++) {
-                const int ch = ch0 + b * kNW;
-                if (ch >= nchunks) break;             // warp-uniform
-                const int vi = ch / cpv, cl = ch % cpv;
-                stage_chunk<VB>(val + b * per, lane, xf + (size_t)vi * vec * 2, cl, cpv,
-                                sc + vi * cpv, hat + vi * cpv);
-#pragma unroll
-                for (int m = 0; m < per; m++) {
-                    const float v = val[b * per + m];
-                    if (plain) plain[vi * vec + cl * vb + lane + 32 * m] = v;
-                    *ss = fmaf(v, v, *ss);
-                }
-            }
-        }
-        return __all_sync(0xffffffffu, lok);
-    }
-
-    // Stages a plain vector in smem (n values) in the VB-bit layout.
-    template <int VB>
-    __device__ void stage_plain(const float *v, int n, uint8_t *xf, float *sc, float *hat) {
-        constexpr int vb = 128 / VB, per = vb / 32;
-        for (int ch = warp; ch < n / vb; ch += kNW) {
-            float val[per];
-#pragma unroll
-            for (int m = 0; m < per; m++) val[m] = v[ch * vb + lane + 32 * m];
-            stage_chunk<VB>(val, lane, xf, ch, n / vb, sc, hat);
-        }
-    }
-
-    // x of layer N (unnormalised: the previous layer's out, or x0), staged for
-    // the expert GEMVs (and, with 2-bit experts, for the int4 heads too);
-    // inv = 1/rms (1 for layer 0).
-    __device__ __noinline__ bool prologue_A(int N) {
-        const int d = p.d;
-        float ss = 0.0f;
-        if (N == 0) {
-            for (int i = tid(); i < d; i += kT) s.stream[i] = p.x0[i];
-            if (!sync()) return false;
-            stage_plain<BITS>(s.stream, d, s.xf, s.xsc, s.xhat);
-            if (BITS != 4) stage_plain<4>(s.stream, d, s.xf4, s.xsc4, s.xhat4);
-            inv = 1.0f;
-            return sync();
-        }
-        const uint64_t *out = tagged(p, p.off_out);
-        if (!poll_chunks<BITS>(out, 1, d, tag(N - 1), s.xf, s.xsc, s.xhat, s.stream, &ss))
-            return false;
-        ss = warp_sum(ss, 32);
-        if (lane == 0) s.misc[warp] = ss;
-        if (!sync()) return false;
-        if (BITS != 4) stage_plain<4>(s.stream, d, s.xf4, s.xsc4, s.xhat4);
-        float tot = 0.0f;
-        for (int w = 0; w < kNW; w++) tot += s.misc[w];
-        inv = 1.0f / sqrtf(tot / d + 1e-6f);
-        if (BITS != 4) return sync();
-        return true;
-    }
-
-    // Everything phase B needs from other CTAs, polled together: h of every
-    // slot, gelu(fc1 f), l f of this CTA's fc2 rows, and the partial A_d h of
-    // down-LoRA slots; plus this CTA's rows of the down-LoRA B matrices.
-    __device__ __noinline__ bool prologue_B(int N, const Tmplt &ta, const Tmplt &tb) {
-        const uint32_t tg = tag(N);
-        const LayerP &L = layer_of(p, N);
-        const int *route = s.rcur + N * p.K;
-        float ss = 0.0f;
-        // B_d rows of this CTA's outputs (plain loads, issued first)
-        if (p.rd) {
-            const int no = tb.o_hi - tb.o_lo;
-            for (int sl = 0; sl < p.S; sl++) {
-                const LoraP &l = slot_lora(p, L, sl, 2);
-                if (!l.r) continue;
-                const uint16_t *B = lora_bm(p, L, route, sl, 2);
-                for (int i = tid(); i < no * l.r; i += kT)
-                    s.bd[(sl * p.max_orows + i / l.r) * p.rd + i % l.r] =
-                        half_f(B[(size_t)(tb.o_lo + i / l.r) * l.r + i % l.r]);
-            }
-        }
-        bool lok = poll_chunks<BITS>(tagged(p, p.off_h), p.S, p.F, tg, s.hf, s.hsc, s.hhat, nullptr, &ss);
-        const bool fc2 = head_runs(p, N) && p.H > 0;
-        if (fc2 && lok)
-            lok = poll_chunks<4>(tagged(p, p.off_ga), 1, p.H, tg, s.gf, s.gsc, s.ghat, nullptr, &ss);
-        if (fc2 && lok && tb.e_hi > tb.e_lo) {
-            const int n = tb.e_hi - tb.e_lo;
-            for (int i0 = tid(); i0 < n && lok; i0 += 8 * kT) {
-                int idx[8];
-                float val[8];
-                int cnt = 0;
-                for (int k = 0; k < 8; k++) {
-                    const int i = i0 + k * kT;
-                    idx[k] = tb.e_lo + (i < n ? i : 0);
-                    if (i < n) cnt = k + 1;
-                }
-                lok = poll_set(p, tagged(p, p.off_zl), idx, cnt, tg, val);
-                for (int k = 0; k < cnt; k++) s.zl[i0 + k * kT] = val[k];
-            }
-        }
-        if (p.rd && lok) {
-            // partial A_d h of down-LoRA slots from their gate/up owners
-            int base = 0;
-            for (int sl = 0; sl < p.S && lok; sl++) {
-                const int r = slot_lora(p, L, sl, 2).r;
-                if (!r) continue;
-                const int n = (ta.own1[sl] - ta.own0[sl] + 1) * r;
-                const uint64_t *w = tagged(p, p.off_vdp) + (size_t)sl * p.n_cta * kMaxLoraRank;
-                for (int i0 = tid(); i0 < n && lok; i0 += 8 * kT) {
-                    int idx[8];
-                    float val[8];
-                    int cnt = 0;
-                    for (int k = 0; k < 8; k++) {
-                        const int i = i0 + k * kT;
-                        const int ii = i < n ? i : 0;
-                        idx[k] = (ta.own0[sl] + ii / r) * kMaxLoraRank + ii % r;
-                        if (i < n) cnt = k + 1;
-                    }
-                    lok = poll_set(p, w, idx, cnt, tg, val);
-                    for (int k = 0; k < cnt; k++) s.vdp[base + i0 + k * kT] = val[k];
-                }
-                base += n;
-            }
-        }
-        if (!__all_sync(0xffffffffu, lok)) return false;
-        if (!sync()) return false;
-        if (p.rd && warp == 0) {
-            // vd[s][k] = sum over owners (ascending) of the partials
-            int base = 0;
-            for (int sl = 0; sl < p.S; sl++) {
-                const int r = slot_lora(p, L, sl, 2).r;
-                if (!r) continue;
-                const int no = ta.own1[sl] - ta.own0[sl] + 1;
-                for (int k = lane; k < r; k += 32) {
-                    float a = 0.0f;
-                    for (int o = 0; o < no; o++) a += s.vdp[base + o * r + k];
-                    s.vd[sl * kMaxLoraRank + k] = a;
-                }
-                base += no * r;
-            }
-        }
-        return true;
-    }
-
-    // ---- tasks -------------------------------------------------------
-    // Gate/up row pairs: h = silu(g) * u (+ gate/up LoRA), published; the
-    // partial A_d h of down-LoRA slots accumulates in vdp_acc (lane k of
-    // every row group holds component k).
-    __device__ __noinline__ void task_gu(int N, const Grp &g, const uint8_t *base, int i, int cnt, int lpr) {
-        const int sub = lane % lpr, rsub = lane / lpr;
-        const int f = i + rsub;
-        const bool ok = rsub < cnt;
-        const LayerP &L = layer_of(p, N);
-        const int *route = s.rcur + N * p.K;
-        const int sl = g.slot;
-        const uint32_t tg = tag(N);
-        const LoraP &lg = slot_lora(p, L, sl, 0), &lu = slot_lora(p, L, sl, 1),
-                    &ld = slot_lora(p, L, sl, 2);
-        // LoRA operands for this row, loaded before the dot product
-        float bg = 0.0f, bu = 0.0f, ad = 0.0f;
-        if (ok && sub < lg.r) bg = half_f(lora_bm(p, L, route, sl, 0)[(size_t)f * lg.r + sub]);
-        if (ok && sub < lu.r) bu = half_f(lora_bm(p, L, route, sl, 1)[(size_t)f * lu.r + sub]);
-        if (ok && sub < ld.r) ad = half_f(lora_a(p, L, route, sl, 2)[(size_t)sub * p.F + f]);
-        float r2[2];
-        rows_dot<BITS, 2>(base + (size_t)(rsub < cnt ? rsub : 0) * g.item_bytes, p.rec_d, p.d, s.xf,
-                          s.xsc, s.xhat, sub, lpr, r2);
-        float gg = r2[0] * inv, uu = r2[1] * inv;
-        if (lg.r || lu.r) {
-            // this lane's components of A_g x and A_u x
-            int idx[2];
-            float val[2] = {0.0f, 0.0f};
-            int n = 0, at_g = -1, at_u = -1;
-            if (ok && sub < lg.r) {
-                at_g = n;
-                idx[n++] = (sl * 2 + 0) * kMaxLoraRank + sub;
-            }
-            if (ok && sub < lu.r) {
-                at_u = n;
-                idx[n++] = (sl * 2 + 1) * kMaxLoraRank + sub;
-            }
-            if (n) poll_set(p, tagged(p, p.off_v), idx, n, tg, val);
-            const float vg = at_g >= 0 ? val[at_g] : 0.0f;
-            const float vu = at_u >= 0 ? val[at_u] : 0.0f;
-            gg += lg.scale * warp_sum(bg * vg, lpr);
-            uu += lu.scale * warp_sum(bu * vu, lpr);
-        }
-        const float h = silu_f(gg) * uu;
-        if (ok && sub == 0) put_tagged(tagged(p, p.off_h) + (size_t)sl * p.F + f, tg, h);
-        if (ld.r) {
-            const float hf = __shfl_sync(0xffffffffu, h, rsub * lpr);
-            if (ok) {
-                if (sl & 1) vdp1 = fmaf(ad, hf, vdp1);
-                else vdp0 = fmaf(ad, hf, vdp0);
-            }
-        }
-    }
-
-    // fc1 / l / router rows on x, with the K-hot table rows and the bias.
-    __device__ __noinline__ void task_head(int N, const Grp &g, const uint8_t *base, int i, int cnt, int lpr) {
-        const int sub = lane % lpr, rsub = lane / lpr;
-        const int row = i + rsub;
-        const bool ok = rsub < cnt;
-        const LayerP &L = layer_of(p, N);
-        const int *cur = s.rcur + N * p.K;
-        const int *prev = p.t > 0 ? s.rprev + N * p.K : nullptr;
-        const uint16_t *tab = g.kind == KFC1 ? L.fc1_tab : (g.kind == KLX ? L.l_tab : nullptr);
-        const int width = g.kind == KFC1 ? p.H : p.E;
-        const uint16_t *bias = g.kind == KFC1 ? L.b1 : (g.kind == KLX ? L.bl : nullptr);
-        // table rows of the 2K active one-hot columns: lanes of the row group
-        float gv = 0.0f;
-        if (ok && tab)
-            for (int k = sub; k < 2 * p.K; k += lpr) {
-                const int e = k < p.K ? cur[k] : (prev ? prev[k - p.K] : -1);
-                if ((unsigned)e < (unsigned)p.E)
-                    gv += half_f(tab[(size_t)(k < p.K ? e : p.E + e) * width + row]);
-            }
-        const float b = (ok && sub == 0 && bias) ? half_f(bias[row]) : 0.0f;
-        const uint8_t *xf = BITS == 4 ? s.xf : s.xf4;
-        const float *xsc = BITS == 4 ? s.xsc : s.xsc4;
-        const float *xhat = BITS == 4 ? s.xhat : s.xhat4;
-        float a;
-        rows_dot<4, 1>(base + (size_t)(rsub < cnt ? rsub : 0) * g.item_bytes, 0, p.d, xf, xsc, xhat,
-                       sub, lpr, &a);
-        const float gsum = tab ? warp_sum(gv, lpr) : 0.0f;
-        if (ok && sub == 0) {
-            a = a * inv + gsum + b;
-            const uint32_t tg = tag(N);
-            if (g.kind == KFC1) put_tagged(tagged(p, p.off_ga) + row, tg, gelu_erf_f(a));
-            else if (g.kind == KLX) {
-                if (p.H > 0) put_tagged(tagged(p, p.off_zl) + row, tg, a);
-                else put_tagged(tagged(p, p.off_z) + (size_t)N * p.E + row, tg, a);
-            } else
-                put_tagged(tagged(p, p.off_zr) + row, tag_router(), a);
-        }
-    }
-
-    // LoRA A rows on x: v = A x, published.
-    __device__ __noinline__ void task_la(int N, const Grp &g, const uint8_t *base, int i, int cnt, int lpr) {
-        const int sub = lane % lpr, rsub = lane / lpr;
-        const float a = f16_row_dot_s(base + (size_t)(rsub < cnt ? rsub : 0) * g.item_bytes, p.d, s.stream, sub, lpr);
-        if (rsub < cnt && sub == 0)
-            put_tagged(tagged(p, p.off_v) + ((size_t)g.slot * 2 + g.aux) * kMaxLoraRank + i + rsub,
-                       tag(N), a * inv);
-    }
-
-    __device__ __noinline__ void task_down(int N, const Grp &g, const Tmplt &t, const uint8_t *base, int i,
-                              int cnt, int lpr) {
-        const int sub = lane % lpr, rsub = lane / lpr;
-        float a;
-        rows_dot<BITS, 1>(base + (size_t)(rsub < cnt ? rsub : 0) * g.item_bytes, 0, p.F,
-                          s.hf + (size_t)g.slot * p.F * 2, s.hsc + g.slot * (p.F / VALS),
-                          s.hhat + g.slot * (p.F / VALS), sub, lpr, &a);
-        if (rsub < cnt && sub == 0) s.y[g.slot * p.max_orows + (i + rsub - t.o_lo)] = a;
-    }
-
-    __device__ __noinline__ void task_fc2(int N, const Grp &g, const Tmplt &t, const uint8_t *base, int i,
-                             int cnt, int lpr) {
-        const int sub = lane % lpr, rsub = lane / lpr;
-        const int e = i + rsub;
-        const LayerP &L = layer_of(p, N);
-        const float b = (rsub < cnt && sub == 0 && L.b2) ? half_f(L.b2[e]) : 0.0f;
-        float a;
-        rows_dot<4, 1>(base + (size_t)(rsub < cnt ? rsub : 0) * g.item_bytes, 0, p.H, s.gf, s.gsc,
-                       s.ghat, sub, lpr, &a);
-        if (rsub < cnt && sub == 0)
-            put_tagged(tagged(p, p.off_z) + (size_t)N * p.E + e, tag(N), a + b + s.zl[e - t.e_lo]);
-    }
-
-    // Consumes this CTA's pieces of groups [g0, g1) of t, in the producer's
-    // order; warp tasks of rpw items go round-robin to the consumer warps.
-    __device__ __noinline__ bool run(int N, const Tmplt &t, int g0, int g1) {
-        uint32_t tasks = 0;
-        for (int gi = g0; gi < g1; gi++) {
-            const Grp &g = t.g[gi];
-            const int per = max(1, kMaxPiece / (int)g.item_bytes);
-            const int lpr = pow2_floor32(item_chunks<BITS>(g));
-            const int rpw = 32 / lpr;
-            for (int i0 = g.lo; i0 < g.hi; i0 += per) {
-                const int cnt = min(per, g.hi - i0);
-                const uint64_t start = rp.place((uint32_t)cnt * g.item_bytes, p.ring_bytes);
-                const uint32_t q = rp.q++;
-                if (!wait_bar_warp(p, s.full + q % kNB, (q / kNB) & 1)) return false;
-                const uint8_t *base = s.ring + start % p.ring_bytes;
-                const int ntask = (cnt + rpw - 1) / rpw;
-                for (int k = (int)((kNW + warp - tasks % kNW) % kNW); k < ntask; k += kNW) {
-                    const int li = k * rpw;
-                    const uint8_t *b = base + (size_t)li * g.item_bytes;
-                    const int n = min(rpw, cnt - li);
-                    const bool tr = g.kind == KGU && trace_gu == 0 && p.trace;
-                    if (tr) stamp(N, 15);
-                    switch (g.kind) {
-                        case KGU: task_gu(N, g, b, i0 + li, n, lpr); break;
-                        case KFC1:
-                        case KLX:
-                        case KROUTER: task_head(N, g, b, i0 + li, n, lpr); break;
-                        case KLA: task_la(N, g, b, i0 + li, n, lpr); break;
-                        case KDOWN: task_down(N, g, t, b, i0 + li, n, lpr); break;
-                        default: task_fc2(N, g, t, b, i0 + li, n, lpr); break;
-                    }
-                    if (tr) {
-                        trace_gu = 1;
-                        if (warp == 0 && lane == 0) {
-                            const size_t at = ((size_t)c * p.depth + N) * kTrace + 15;
-                            p.trace[at] = now_ns() - p.trace[at];
-                        }
-                    }
-                }
-                tasks += ntask;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s.empty + q % kNB);
-            }
-        }
-        return true;
-    }
-
-    // Layer 0's own route: poll the router logits, top-K (every CTA alike).
-    __device__ __noinline__ bool route0() {
+    // Waits until every CTA's flag at `off` has reached `tg`: warp 0 polls the
+    // flags, the other warps sleep on the mbarrier `b`.
+    __device__ __forceinline__ bool flag_wait(uint32_t off, uint32_t tg, uint64_t *b, uint32_t &uses) {
         if (warp == 0) {
-            float vals[32];
-            if (!poll_logits(p, tagged(p, p.off_zr), p.E, tag_router(), lane, vals)) return false;
-            int idx[kMaxK];
-            float w[kMaxK], margin;
-            warp_topk(vals, p.E, p.K, lane, idx, w, &margin);
-            if (lane == 0) {
-                const int use = p.t % 3;
-                for (int k = 0; k < p.K; k++) {
-                    s.rcur[k] = idx[k];
-                    s.rw[k] = w[k];
-                    if (c == 0) {
-                        p.ridx[(size_t)use * p.depth * p.K + k] = idx[k];
-                        p.rw[(size_t)use * p.depth * p.K + k] = w[k];
-                    }
-                }
-                if (c == 0) p.rmargin[(size_t)use * p.depth] = margin;
-                mbar_arrive(s.route_bar);
-            }
+            if (!poll_flags(off, tg, lane, 0)) return false;
+            if (lane == 0) mbar_arrive(b);
         }
-        return sync();
+        const bool ok = wait_bar_warp(b, uses & 1);
+        uses++;
+        return ok;
     }
 
-    // Publishes this CTA's partial A_d h for every down-LoRA slot whose
-    // gate/up rows it helps own (zeros if it owns none of them).
-    __device__ __noinline__ bool publish_vdp(int N, const Tmplt &ta) {
-        const LayerP &L = layer_of(p, N);
-        // per-warp partials: lane k of row group 0 after folding the row
-        // groups (every row group of a gate/up task has the lpr of d); a CTA
-        // spans at most two down-LoRA slots, kept apart by slot parity
-        const int lpr = pow2_floor32(p.d * BITS / 128);
-        for (int par = 0; par < 2; par++) {
-            float v = par ? vdp1 : vdp0;
-            for (int o = lpr; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane < lpr) s.misc[16 + (par * kNW + warp) * 32 + lane] = v;
-        }
-        vdp0 = vdp1 = 0.0f;
+    __device__ __forceinline__ bool gu_lora_here(int N) const {
+        const Ctx &cx = CX();
+        if (cx.gu_slot < 0) return false;
+        const Tmplt &ta = tmpls()[tmpl_A_index(N)];
+        return ta.phi[cx.gu_slot] > ta.plo[cx.gu_slot];
+    }
+
+    __device__ __forceinline__ bool run(int N, int ti, float inv) {
+        const RunState st = run_tmpl<BITS>(N, ti, inv, warp, lane, RunState{rp.head, rp.q, tasks, 1u});
+        rp.head = st.head;
+        rp.q = st.q;
+        tasks = st.tasks;
+        return st.ok != 0;
+    }
+
+    __device__ __forceinline__ bool layer(int N) {
+        const Ctx &cx = CX();
+        if (warp == 0 && lane == 0) stamp_at(c, N, ST_L0);
+        const bool r0 = N == 0 && cx.own0;
+        const bool vp = gu_lora_here(N);
+        if (N > 0 && !flag_wait(cx.off_xflag, tag_of(N - 1), bar(B_X), xuses)) return false;
+        if (!phase_x<BITS>(N, true, vp && !r0, warp, lane)) return false;
         if (!sync()) return false;
-        const uint32_t tg = tag(N);
-        for (int sl = 0; sl < p.S; sl++) {
-            const int r = slot_lora(p, L, sl, 2).r;
-            if (!r || c < ta.own0[sl] || c > ta.own1[sl]) continue;
-            for (int k = tid(); k < r; k += kT) {
-                float a = 0.0f;
-                for (int w = 0; w < kNW; w++) a += s.misc[16 + ((sl & 1) * kNW + w) * 32 + k];
-                put_tagged(tagged(p, p.off_vdp) + ((size_t)sl * p.n_cta + c) * kMaxLoraRank + k, tg,
-                           a);
+        const float inv = misc_f()[M_INV];
+        if (warp == 0 && lane == 0) stamp_at(c, N, ST_X);
+        if (r0) {
+            if (!run(0, T_R, inv)) return false;
+            // layer 0's own route (every CTA alike)
+            if (warp == 0) {
+                if (!route_from_logits(tagged(cx.off_zr), tag_router(), cx.t % 3, 0, c == 0, true, 0))
+                    return false;
+                if (lane == 0) mbar_arrive(bar(B_ROUTE));
             }
+            if (vp && !phase_x<BITS>(0, false, true, warp, lane)) return false;
+            if (!sync()) return false;
         }
+        if (!wait_bar_warp(bar(B_PREP_FULL0 + (N & 1)), (N >> 1) & 1)) return false;
+        if (!run(N, tmpl_A_index(N), inv)) return false;
+        publish_a(N, c, lane);
+        if (warp == 0 && lane == 0) stamp_at(c, N, ST_A);
+        if (!flag_wait(cx.off_hflag, tag_of(N), bar(B_H), huses)) return false;
+        if (!phase_h<BITS>(N, warp, lane)) return false;
+        if (!sync()) return false;               // h and vd visible to all warps
+        if (warp == 0 && lane == 0) stamp_at(c, N, ST_H);
+        if (!run(N, T_B, inv)) return false;     // down rows + combine
+        if (N + 1 < cx.depth) publish_d(N, c, lane);
+        if (warp == 0 && lane == 0) stamp_at(c, N, ST_D);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PREP_EMPTY0 + (N & 1)));
         return true;
     }
 
-    // Combine + residual over this CTA's output rows; publishes out.
-    __device__ __noinline__ void combine(int N, const Tmplt &t) {
-        const uint32_t tg = tag(N);
-        const float *w = s.rw + N * p.K;
-        const LayerP &L = layer_of(p, N);
-        for (int o = t.o_lo + tid(); o < t.o_hi; o += kT) {
-            const int li = o - t.o_lo;
-            float v = s.stream[o];
-            for (int sl = 0; sl < p.S; sl++) {
-                float ys = s.y[sl * p.max_orows + li];
-                const LoraP &l = slot_lora(p, L, sl, 2);
-                if (l.r) {
-                    float a = 0.0f;
-                    for (int k = 0; k < l.r; k++)
-                        a = fmaf(s.bd[(sl * p.max_orows + li) * p.rd + k], s.vd[sl * kMaxLoraRank + k], a);
-                    ys += l.scale * a;
-                }
-                v = sl < p.K ? fmaf(w[sl], ys, v) : v + ys;
-            }
-            put_tagged(tagged(p, p.off_out) + o, tg, v);
-            if (N == p.depth - 1) p.out[o] = v;
-        }
-    }
-
-    __device__ bool layer(int N) {
-        trace_gu = 0;
-        stamp(N, 0);
-        if (!prologue_A(N)) return false;
-        stamp(N, 1);
-        if (N == 0 && p.own0) {
-            if (!run(0, s.T[T_R], 0, s.T[T_R].n)) return false;
-            if (!route0()) return false;
-        }
-        const Tmplt &ta = tmpl_A(p, s.T, N), &tb = tmpl_B(p, s.T, N);
-        if (!run(N, ta, 0, ta.n)) return false;
-        stamp(N, 2);
-        if (p.rd && !publish_vdp(N, ta)) return false;
-        if (!prologue_B(N, ta, tb)) return false;
-        stamp(N, 3);
-        if (!sync()) return false;              // h, ga and vd visible to all warps
-        stamp(N, 4);
-        const int nd = head_runs(p, N) && p.H > 0 ? tb.n - 1 : tb.n;
-        if (!run(N, tb, 0, nd)) return false;   // down rows
-        stamp(N, 6);
-        if (!sync()) return false;
-        combine(N, tb);
-        stamp(N, 7);
-        if (!run(N, tb, nd, tb.n)) return false;  // head fc2 rows
-        stamp(N, 8);
-        return true;
-    }
-
-    __device__ bool run_all() {
-        if (p.debug_unset_wait && c == 0 && warp == 0) {
+    __device__ __forceinline__ void run_all() {
+        const Ctx &cx = CX();
+        if (cx.debug_unset_wait && c == 0 && warp == 0) {
             // test hook: a flag nothing ever sets, so this wait runs out
-            float v;
-            int idx = 0;
-            const bool lok = poll_set(p, tagged(p, C_NEVER * 4), &idx, 1, 0xFFFFFFFFu, &v);
-            if (!__all_sync(0xffffffffu, lok)) return false;
+            const uint32_t idx[1] = {C_NEVER / 2};
+            float v[1];
+            if (!__all_sync(0xffffffffu, poll_vals<1>(reinterpret_cast<const uint64_t *>(cx.ws), idx,
+                                                      1u, 0u, 0xFFFFFFFFu, 0xFFFFFFFFu, v)))
+                return;
         }
-        for (int N = 0; N < p.depth; N++)
-            if (!layer(N)) return false;
-        return true;
+        for (int N = 0; N < cx.depth; N++)
+            if (!layer(N)) return;
     }
 };
 
+// The three roles, each in a function of its own (its own registers: no
+// spills of one role's loop state into local memory because of another's).
+template <int BITS>
+__device__ __noinline__ void producer_main(const Params &p, int lane) {
+    Producer<BITS> pr{p, lane};
+    pr.run();
+}
+
+template <int BITS>
+__device__ __noinline__ void consumer_main(int c, int warp, int lane) {
+    Consumer<BITS> cons{c, warp, lane};
+    cons.run_all();
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_constant__ Params p) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const Smem s = smem_views(p, smem);
     const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the context: copied into shared memory (its first bytes), read from there
+    {
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(&p.cx);
+        uint32_t *dst = reinterpret_cast<uint32_t *>(g_smem);
+        for (int i = threadIdx.x; i < (int)(sizeof(Ctx) / 4); i += blockDim.x) dst[i] = src[i];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        reinterpret_cast<Ctx *>(g_smem)->epoch =
+            (uint32_t)ld_flag(reinterpret_cast<const int *>(p.cx.ws) + C_EPOCH);
+    const Ctx &cx = CX();
 
     // routes of this step (layer 0's own route is filled in later)
-    const int use = p.t % 3, prv = (p.t + 2) % 3;
-    for (int i = threadIdx.x; i < p.depth * p.K; i += blockDim.x) {
-        s.rcur[i] = p.ridx[(size_t)use * p.depth * p.K + i];
-        s.rw[i] = p.rw[(size_t)use * p.depth * p.K + i];
-        s.rprev[i] = p.ridx[(size_t)prv * p.depth * p.K + i];
+    const int use = p.cx.t % 3, prv = (p.cx.t + 2) % 3;
+    for (int i = threadIdx.x; i < p.cx.depth * p.cx.K; i += blockDim.x) {
+        SM<int>(p.cx.sm_rcur)[i] = p.cx.ridx[(size_t)use * p.cx.depth * p.cx.K + i];
+        SM<float>(p.cx.sm_rw)[i] = p.cx.rw[(size_t)use * p.cx.depth * p.cx.K + i];
+        SM<int>(p.cx.sm_rprev)[i] = p.cx.ridx[(size_t)prv * p.cx.depth * p.cx.K + i];
     }
+    for (int i = threadIdx.x; i < kNW * p.cx.n_dl * kMaxR; i += blockDim.x)
+        SM<float>(p.cx.sm_vdacc)[i] = 0.0f;
+    for (int i = threadIdx.x; i < kNW * 2 * kMaxR; i += blockDim.x) SM<float>(p.cx.sm_vnw)[i] = 0.0f;
     if (threadIdx.x == 0) {
+        uint64_t *bars = SM<uint64_t>(p.cx.sm_bar);
         for (int i = 0; i < kNB; i++) {
-            mbar_init(s.full + i, 1);
-            mbar_init(s.empty + i, kNW);
+            mbar_init(bars + i, 1);
+            mbar_init(bars + kNB + i, kNW);
         }
-        mbar_init(s.route_bar, 1);
-        mbar_init(s.cons_bar, kNW);
-        mbar_init(s.end_bar, kCons0 + kNW);
+        uint64_t *b = bars + 2 * kNB;
+        mbar_init(b + B_ROUTE, 1);
+        mbar_init(b + B_CONS, kNW);
+        mbar_init(b + B_END, kCons0 + kNW);
+        mbar_init(b + B_X, 1);
+        mbar_init(b + B_H, 1);
+        for (int k = 0; k < 2; k++) {
+            mbar_init(b + B_PREP_FULL0 + k, 1);
+            mbar_init(b + B_PREP_EMPTY0 + k, kNW);
+        }
+        int *mi = SM<int>(p.cx.sm_misc);
+        for (int i = M_CNT_A; i <= M_CNT_D; i++) mi[i] = 0;
         mbar_fence_init();
-        build_templates(p, c, s.T);
+        mi[M_TMPL_OK] = build_templates(c, SM<Tmplt>(p.cx.sm_tmpl)) ? 1 : 0;
+        if (!mi[M_TMPL_OK]) raise_error(MOE_EINVAL);
     }
     __syncthreads();
 
-    if (warp == kProducerWarp) {
-        if (lane == 0) producer<BITS>(p, s);
-    } else if (warp == kRouteWarp) {
-        route_warp(p, c, lane);
-    } else {
-        Consumer<BITS> cons{p, s, c, warp - kCons0, lane, (uint32_t)ld_flag(ctrl(p) + C_EPOCH)};
-        cons.run_all();
+    if (misc_i()[M_TMPL_OK] && !aborted()) {
+        if (warp == kProducerWarp) producer_main<BITS>(p, lane);
+        else if (warp == kAuxWarp) aux_main<BITS>(p, c, lane);
+        else consumer_main<BITS>(c, warp - kCons0, lane);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(s.end_bar);
+    if (lane == 0) mbar_arrive(bar(B_END));
     if (threadIdx.x == 0) {
         // the step is complete in this CTA once every warp has arrived
-        if (wait_bar(p, s.end_bar, 0) && !aborted(p)) {
+        if (wait_bar(bar(B_END), 0) && !aborted()) {
             __threadfence();
-            const int prev = atomicAdd(ctrl(p) + C_DONE, 1);
-            if (prev == p.n_cta - 1) {
-                atomicExch(ctrl(p) + C_DONE, 0);
-                atomicAdd(ctrl(p) + C_EPOCH, 1);
+            const int prev = atomicAdd(ctrl() + C_DONE, 1);
+            if (prev == cx.n_cta - 1) {
+                atomicExch(ctrl() + C_DONE, 0);
+                atomicAdd(ctrl() + C_EPOCH, 1);
             }
         }
     }
@@ -1202,13 +1655,15 @@ static void step_ws_layout(int d, int F, int E, int H, int S, int depth, int n_c
         return (uint32_t)o;
     };
     offs[0] = take((size_t)S * F);                          // h
-    offs[1] = take((size_t)S * 2 * kMaxLoraRank);           // LoRA A x (gate, up)
-    offs[2] = take((size_t)S * n_cta * kMaxLoraRank);       // partial A_d h per owner CTA
-    offs[3] = take((size_t)(H > 0 ? H : 1));                // gelu(fc1 f)
-    offs[4] = take((size_t)E);                              // l f
+    offs[1] = take((size_t)n_cta * 2 * kMaxR);              // partial A x per CTA (gate/up LoRA)
+    offs[2] = take((size_t)S * n_cta * kMaxR);              // partial A_d h per owner CTA
+    offs[3] = take((size_t)depth * (H > 0 ? H : 1));        // gelu(fc1 f) per layer
+    offs[4] = take((size_t)depth * E);                      // l f per layer
     offs[5] = take((size_t)E);                              // router logits
     offs[6] = take((size_t)depth * E);                      // head logits per layer
     offs[7] = take((size_t)d);                              // out
+    offs[8] = take((size_t)(n_cta + 1) / 2);                // per-CTA flag: out (+ partials) published
+    offs[9] = take((size_t)(n_cta + 1) / 2);                // per-CTA flag: phase A published
     *total = off;
 }
 
@@ -1244,7 +1699,6 @@ static int check_stack(const moe_stack_desc *sd) {
         return fail(MOE_EINVAL, "decode_step: expert shape d=%d F=%d E=%d bits=%d", e0.d, e0.F,
                     e0.E, e0.bits);
     const int H = heads ? sd->heads[0].H : 0;
-    int down_lora_slots = 0;
     for (int i = 0; i < sd->n_layers; i++) {
         const moe_experts_desc &e = sd->experts[i];
         if (e.d != e0.d || e.F != e0.F || e.E != e0.E || e.bits != e0.bits ||
@@ -1256,13 +1710,16 @@ static int check_stack(const moe_stack_desc *sd) {
         for (int j = 0; j < 3; j++) {
             const int r0 = e.lora[j].r, r1 = e.shared ? e.shared_lora[j].r : 0;
             const int q0 = e0.lora[j].r, q1 = e0.shared ? e0.shared_lora[j].r : 0;
-            if (r0 != q0 || r1 != q1 || r0 < 0 || r0 > 32 || r1 < 0 || r1 > 32)
+            if (r0 != q0 || r1 != q1 || r0 < 0 || r0 > kMaxR || r1 < 0 || r1 > kMaxR)
                 return fail(MOE_EUNSUPPORTED,
-                            "decode_step: LoRA ranks must match across layers and be <= 32");
+                            "decode_step: LoRA ranks must match across layers and be <= %d", kMaxR);
             if ((r0 && (!e.lora[j].A || !e.lora[j].B)) ||
                 (r1 && (!e.shared_lora[j].A || !e.shared_lora[j].B)))
                 return fail(MOE_EINVAL, "decode_step: LoRA with NULL A or B");
         }
+        if (e.lora[0].r || e.lora[1].r)
+            return fail(MOE_EUNSUPPORTED,
+                        "decode_step: gate/up LoRA on routed experts runs through the per-call path");
         const moe_head_desc &r = sd->routers[i];
         if (r.d != e0.d || r.E != e0.E || r.lx == nullptr)
             return fail(MOE_EINVAL, "decode_step: router %d shape", i);
@@ -1277,13 +1734,6 @@ static int check_stack(const moe_stack_desc *sd) {
                 return fail(MOE_EUNSUPPORTED, "decode_step: fp16 heads run through the per-call path");
         }
     }
-    down_lora_slots = (e0.lora[2].r ? sd->K : 0) + (e0.shared && e0.shared_lora[2].r ? 1 : 0);
-    if (down_lora_slots > 1 && (e0.lora[2].r || e0.shared_lora[2].r)) {
-        // one CTA owning gate/up rows of two down-LoRA slots would mix their
-        // partials; the split keeps slots apart only when each slot's rows
-        // span whole CTAs, which the host cannot promise in general
-        if (e0.d < 64) return fail(MOE_EUNSUPPORTED, "decode_step: down-LoRA layout");
-    }
     return MOE_OK;
 }
 
@@ -1291,7 +1741,7 @@ extern "C" size_t moe_decode_step_workspace_bytes(const moe_stack_desc *sd) {
     if (check_stack(sd) != MOE_OK) return 0;
     const moe_experts_desc &e0 = sd->experts[0];
     const int H = (sd->depth > 1 || sd->self_predict) ? sd->heads[0].H : 0;
-    uint32_t offs[8];
+    uint32_t offs[10];
     size_t total = 0;
     const int sms = device_sms();
     step_ws_layout(e0.d, e0.F, e0.E, H, sd->K + (e0.shared ? 1 : 0), sd->depth,
@@ -1343,7 +1793,7 @@ static int launch_bits(const Params &p, size_t smem, cudaStream_t st) {
         configured_smem = smem;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_cta);
+    cfg.gridDim = dim3(p.cx.n_cta);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -1364,53 +1814,74 @@ static int launch_decode_step(const moe_stack_desc *sd, const float *x0, float *
     const moe_experts_desc &e0 = sd->experts[0];
     const bool heads = sd->depth > 1 || sd->self_predict;
     p = Params{};
-    p.d = e0.d;
-    p.F = e0.F;
-    p.E = e0.E;
-    p.K = sd->K;
-    p.H = heads ? sd->heads[0].H : 0;
-    p.S = sd->K + (e0.shared ? 1 : 0);
-    p.depth = sd->depth;
-    p.n_res = sd->n_layers;
-    p.self_predict = sd->self_predict;
-    p.own0 = !sd->self_predict;
-    p.t = t;
+    Ctx &cx = p.cx;
+    cx.d = e0.d;
+    cx.F = e0.F;
+    cx.E = e0.E;
+    cx.K = sd->K;
+    cx.H = heads ? sd->heads[0].H : 0;
+    cx.S = sd->K + (e0.shared ? 1 : 0);
+    cx.depth = sd->depth;
+    cx.n_res = sd->n_layers;
+    cx.self_predict = sd->self_predict;
+    cx.own0 = !sd->self_predict;
+    cx.t = t;
     const int bits = e0.bits;
-    const BlobLayout L = blob_layout(p.d, p.F, bits);
-    p.stride = e0.expert_stride;
-    p.gu_off = (uint32_t)L.gu_off;
-    p.down_off = (uint32_t)L.down_off;
-    p.rec_d = (uint32_t)L.gu_rec;
-    p.rec_F = (uint32_t)L.down_rec;
-    p.rec_dh = (uint32_t)record_bytes(p.d, 4);
-    p.rec_H = p.H ? (uint32_t)record_bytes(p.H, 4) : 0;
-    p.rd = std::max(e0.lora[2].r, e0.shared ? e0.shared_lora[2].r : 0);
-    p.x0 = x0;
-    p.out = out;
-    p.ridx = ridx;
-    p.rw = rw;
-    p.rmargin = rmargin;
-    p.ws = static_cast<uint8_t *>(ws);
+    const BlobLayout L = blob_layout(cx.d, cx.F, bits);
+    cx.stride = e0.expert_stride;
+    cx.gu_off = (uint32_t)L.gu_off;
+    cx.down_off = (uint32_t)L.down_off;
+    cx.rec_d = (uint32_t)L.gu_rec;
+    cx.rec_F = (uint32_t)L.down_rec;
+    cx.rec_dh = (uint32_t)record_bytes(cx.d, 4);
+    cx.rec_H = cx.H ? (uint32_t)record_bytes(cx.H, 4) : 0;
+    // LoRA: gate/up only on the shared slot; down on routed and/or shared
+    const moe_lora_desc *sl = e0.shared ? e0.shared_lora : nullptr;
+    cx.rg = sl ? sl[0].r : 0;
+    cx.ru = sl ? sl[1].r : 0;
+    cx.gu_slot = (cx.rg || cx.ru) ? cx.S - 1 : -1;
+    if (cx.rg + cx.ru > 32)
+        return fail(MOE_EUNSUPPORTED, "decode_step: gate + up LoRA ranks %d + %d exceed 32", cx.rg,
+                    cx.ru);
+    cx.rdr = e0.lora[2].r;
+    cx.rds = sl ? sl[2].r : 0;
+    cx.dl_mask = 0;
+    if (cx.rdr)
+        for (int s = 0; s < cx.K; s++) cx.dl_mask |= 1u << s;
+    if (cx.rds) cx.dl_mask |= 1u << (cx.S - 1);
+    cx.n_dl = __builtin_popcount(cx.dl_mask);
+    cx.rd = std::max(cx.rdr, cx.rds);
+    cx.x0 = x0;
+    cx.out = out;
+    cx.ridx = ridx;
+    cx.rw = rw;
+    cx.rmargin = rmargin;
+    cx.ws = static_cast<uint8_t *>(ws);
     const int sms = device_sms();
     int dev = 0, smem_max = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (sms <= 0 || smem_max <= 0) return fail(MOE_ECUDA, "decode_step: no device attributes");
-    p.n_cta = sms;
-    uint32_t offs[8];
+    if (sms > 256) return fail(MOE_EUNSUPPORTED, "decode_step: %d SMs (at most 256)", sms);
+    cx.n_cta = sms;
+    uint32_t offs[10];
     size_t total = 0;
-    step_ws_layout(p.d, p.F, p.E, p.H, p.S, p.depth, sms, offs, &total);
-    p.off_h = offs[0];
-    p.off_v = offs[1];
-    p.off_vdp = offs[2];
-    p.off_ga = offs[3];
-    p.off_zl = offs[4];
-    p.off_zr = offs[5];
-    p.off_z = offs[6];
-    p.off_out = offs[7];
-    p.timeout_ns = sd->timeout_ns ? sd->timeout_ns : 1000000000ull;
-    p.debug_unset_wait = sd->debug_unset_wait;
-    p.trace = sd->debug_trace;
+    step_ws_layout(cx.d, cx.F, cx.E, cx.H, cx.S, cx.depth, sms, offs, &total);
+    cx.off_h = offs[0];
+    cx.off_vp = offs[1];
+    cx.off_vdp = offs[2];
+    cx.off_ga = offs[3];
+    cx.off_zl = offs[4];
+    cx.off_zr = offs[5];
+    cx.off_z = offs[6];
+    cx.off_out = offs[7];
+    cx.off_xflag = offs[8];
+    cx.off_hflag = offs[9];
+    cx.timeout_ns = sd->timeout_ns ? sd->timeout_ns : 1000000000ull;
+    cx.debug_unset_wait = sd->debug_unset_wait;
+    cx.trace = sd->debug_trace;
+    cx.inflight = sd->inflight_bytes ? sd->inflight_bytes : kDefaultInflight;
+    if (cx.inflight < (uint32_t)kMaxPiece) cx.inflight = kMaxPiece;
     for (int i = 0; i < sd->n_layers; i++) {
         const moe_experts_desc &e = sd->experts[i];
         LayerP &lp = p.layer[i];
@@ -1437,82 +1908,96 @@ static int launch_decode_step(const moe_stack_desc *sd, const float *x0, float *
         }
     }
 
-    p.max_orows = (p.d + sms - 1) / sms;
-    if ((p.E + sms - 1) / sms > kMaxOwnE)
-        return fail(MOE_EUNSUPPORTED, "decode_step: E=%d too large for %d SMs", p.E, sms);
+    // per-CTA bounds of the byte split (checked again on the device)
+    {
+        const long long gu = (long long)cx.S * cx.F * 2 * cx.rec_d;
+        const long long total_a = gu + (heads ? (long long)(cx.H + cx.E) * cx.rec_dh : 0);
+        const long long share = (total_a + sms - 1) / sms;
+        cx.max_pairs = (int)(share / (2 * cx.rec_d)) + cx.S + 1;
+        cx.max_hrows = (int)(share / cx.rec_dh) + 3;
+    }
+    cx.max_orows = (cx.d + sms - 1) / sms;
+    cx.max_erows = (cx.E + sms - 1) / sms;
+    if (cx.max_erows > 32 || cx.max_erows * (int)cx.rec_H > 16384)
+        return fail(MOE_EUNSUPPORTED, "decode_step: E=%d too large for %d SMs", cx.E, sms);
 
-    // shared-memory layout
+    // shared-memory layout: the context first
     const int VALS = 128 / bits;
-    size_t off = 0;
+    size_t off = sizeof(Ctx);
     auto take = [&](size_t bytes) {
         off = al(off, 16);
         const size_t o = off;
         off += bytes;
         return (uint32_t)o;
     };
-    p.sm_bar = take((size_t)(2 * kNB + 3) * 8);
-    p.sm_pend = take((size_t)kNB * 8);
-    p.sm_tmpl = take(T_COUNT * sizeof(Tmplt));
-    p.sm_xf = take((size_t)p.d * 2);
-    p.sm_xsc = take((size_t)(p.d / VALS) * 4);
-    p.sm_xhat = take((size_t)(p.d / VALS) * 4);
-    p.sm_xf4 = bits == 4 ? p.sm_xf : take((size_t)p.d * 2);
-    p.sm_xsc4 = bits == 4 ? p.sm_xsc : take((size_t)(p.d / 32) * 4);
-    p.sm_xhat4 = bits == 4 ? p.sm_xhat : take((size_t)(p.d / 32) * 4);
-    p.sm_stream = take((size_t)p.d * 4);
-    p.sm_hf = take((size_t)p.S * p.F * 2);
-    p.sm_hsc = take((size_t)p.S * (p.F / VALS) * 4);
-    p.sm_hhat = take((size_t)p.S * (p.F / VALS) * 4);
-    p.sm_gf = take((size_t)(p.H ? p.H : 64) * 2);
-    p.sm_gsc = take((size_t)(p.H ? p.H / 32 : 2) * 4);
-    p.sm_ghat = take((size_t)(p.H ? p.H / 32 : 2) * 4);
-    p.sm_zl = take((size_t)kMaxOwnE * 4);
-    p.sm_y = take((size_t)p.S * p.max_orows * 4);
-    p.sm_bd = take((size_t)p.S * p.max_orows * (p.rd ? p.rd : 1) * 4);
-    p.sm_vdp = take((size_t)(p.rd ? kMaxVdp : 1) * 4);
-    p.sm_vd = take((size_t)p.S * kMaxLoraRank * 4);
-    p.sm_rcur = take((size_t)p.depth * p.K * 4);
-    p.sm_rprev = take((size_t)p.depth * p.K * 4);
-    p.sm_rw = take((size_t)p.depth * p.K * 4);
-    p.sm_misc = take((size_t)(16 + 2 * kNW * 32) * 4);
-    p.sm_ring = (uint32_t)al(off, 1024);
-    long long room = (long long)smem_max - (long long)p.sm_ring;
+    const int r2 = cx.rg + cx.ru;
+    const int ndl = std::max(cx.n_dl, 1);
+    cx.sm_bar = take((size_t)(2 * kNB + B_COUNT) * 8);
+    cx.sm_pend = take((size_t)kNB * 8);
+    cx.sm_tmpl = take(T_COUNT * sizeof(Tmplt));
+    cx.sm_xf = take((size_t)cx.d * 2);
+    cx.sm_xsc = take((size_t)(cx.d / VALS) * 4);
+    cx.sm_xhat = take((size_t)(cx.d / VALS) * 4);
+    cx.sm_xf4 = bits == 4 ? cx.sm_xf : take((size_t)cx.d * 2);
+    cx.sm_xsc4 = bits == 4 ? cx.sm_xsc : take((size_t)(cx.d / 32) * 4);
+    cx.sm_xhat4 = bits == 4 ? cx.sm_xhat : take((size_t)(cx.d / 32) * 4);
+    cx.sm_stream = take((size_t)2 * cx.d * 4);
+    cx.sm_hf = take((size_t)cx.S * cx.F * 2);
+    cx.sm_hsc = take((size_t)cx.S * (cx.F / VALS) * 4);
+    cx.sm_hhat = take((size_t)cx.S * (cx.F / VALS) * 4);
+    cx.sm_vpw = take((size_t)kNW * 2 * kMaxR * 4);
+    cx.sm_vx = take((size_t)2 * kMaxR * 4);
+    cx.sm_vdw = take((size_t)kNW * ndl * kMaxR * 4);
+    cx.sm_vd = take((size_t)ndl * kMaxR * 4);
+    cx.sm_vdacc = take((size_t)kNW * ndl * kMaxR * 4);
+    cx.sm_vnw = take((size_t)kNW * 2 * kMaxR * 4);
+    cx.sm_comb = take((size_t)cx.max_orows * 4);
+    // prep buffer (floats): scales | tsum | bgu | adn | bd | agu
+    {
+        uint32_t f = 0;
+        cx.pp_scale = f;
+        f += SC_COUNT;
+        cx.pp_tsum = f;
+        f += (uint32_t)cx.max_hrows;
+        cx.pp_bgu = f;
+        f += (uint32_t)(cx.gu_slot >= 0 ? cx.max_pairs * r2 : 0);
+        cx.pp_adn = f;
+        f += (uint32_t)(cx.dl_mask ? cx.max_pairs * cx.rd : 0);
+        cx.pp_bd = f;
+        f += (uint32_t)(cx.n_dl * cx.max_orows * cx.rd);
+        cx.pp_agu = f;
+        f += (uint32_t)(cx.gu_slot >= 0 ? cx.max_orows * r2 : 0);
+        cx.prep_bytes = (uint32_t)al((size_t)f * 4, 16);
+    }
+    cx.sm_prep = take((size_t)2 * cx.prep_bytes);
+    cx.sm_gf = take((size_t)(cx.H ? cx.H : 64) * 2);
+    cx.sm_gsc = take((size_t)(cx.H ? cx.H / 32 : 2) * 4);
+    cx.sm_ghat = take((size_t)(cx.H ? cx.H / 32 : 2) * 4);
+    cx.sm_frec = take((size_t)std::max(cx.max_erows * (int)cx.rec_H, 16));
+    cx.sm_rcur = take((size_t)cx.depth * cx.K * 4);
+    cx.sm_rprev = take((size_t)cx.depth * cx.K * 4);
+    cx.sm_rw = take((size_t)cx.depth * cx.K * 4);
+    cx.sm_misc = take((size_t)M_COUNT * 4);
+    cx.sm_hraw = take((size_t)cx.S * cx.F * 4);
+    cx.sm_graw = take((size_t)(cx.H ? cx.H : 32) * 4);
+    cx.sm_vdpl = take((size_t)2 * std::max(cx.n_dl, 1) * sms * 4);
+    cx.sm_ring = (uint32_t)al(off, 1024);
+    long long room = (long long)smem_max - (long long)cx.sm_ring;
     room = room / 1024 * 1024;
     if (room < 3 * kMaxPiece)
         return fail(MOE_EUNSUPPORTED, "decode_step: shapes leave a %lld-byte ring (< 48 KiB)", room);
-    p.ring_bytes = (uint32_t)room;
-    const size_t smem = (size_t)p.sm_ring + p.ring_bytes;
+    cx.ring_bytes = (uint32_t)room;
+    const size_t smem = (size_t)cx.sm_ring + cx.ring_bytes;
+    // a batch of copies (at most half the in-flight bytes, or one piece) must
+    // always fit the ring with room to spare
+    cx.inflight = std::min(cx.inflight, cx.ring_bytes / 2);
 
-    // every item must fit a piece; the down-LoRA partials must fit their
-    // buffer (each slot's owners x rank)
-    if (2 * p.rec_d > (uint32_t)kMaxPiece || 2u * p.d > (uint32_t)kMaxPiece)
-        return fail(MOE_EUNSUPPORTED, "decode_step: d=%d rows exceed a %d-byte piece", p.d,
+    // every item must fit a piece
+    if (2 * cx.rec_d > (uint32_t)kMaxPiece || cx.rec_dh > (uint32_t)kMaxPiece)
+        return fail(MOE_EUNSUPPORTED, "decode_step: d=%d rows exceed a %d-byte piece", cx.d,
                     kMaxPiece);
-    if (3 * p.S + 2 > kMaxGroups)
-        return fail(MOE_EUNSUPPORTED, "decode_step: K=%d needs too many work groups", p.K);
-    if (p.rd) {
-        // CTAs owning gate/up rows of a slot: about the slot's share of the
-        // phase bytes plus one on each side
-        const long long gu_bytes = 2LL * p.rec_d * p.F;
-        long long total = (long long)p.S * gu_bytes +
-                          (p.H ? (long long)p.H * p.rec_dh : 0) + (long long)p.E * p.rec_dh;
-        for (int sl = 0; sl < p.S; sl++)
-            for (int w = 0; w < 2; w++) {
-                const int r = sl < p.K ? e0.lora[w].r : (e0.shared ? e0.shared_lora[w].r : 0);
-                total += 2LL * p.d * r;
-            }
-        const long long owners = gu_bytes * sms / total + 3;
-        const int slots = (e0.lora[2].r ? p.K : 0) + (e0.shared && e0.shared_lora[2].r ? 1 : 0);
-        if (owners * slots * p.rd > kMaxVdp)
-            return fail(MOE_EUNSUPPORTED, "decode_step: down-LoRA partials exceed %d floats", kMaxVdp);
-        // a CTA may span the gate/up rows of at most two down-LoRA slots (two
-        // accumulators): each slot's rows must be at least one CTA's share
-        if (slots > 1 && gu_bytes * sms < total)
-            return fail(MOE_EUNSUPPORTED, "decode_step: down-LoRA slots too small to split");
-        // lane k of a gate/up row group holds component k of A_d h
-        if (p.rd > pow2_floor32(p.d * bits / 128))
-            return fail(MOE_EUNSUPPORTED, "decode_step: down-LoRA rank %d above lanes per row", p.rd);
-    }
+    if (cx.S + 2 > kMaxGroups)
+        return fail(MOE_EUNSUPPORTED, "decode_step: K=%d needs too many work groups", cx.K);
 
     return bits == 4 ? launch_bits<4>(p, smem, st) : launch_bits<2>(p, smem, st);
 }

@@ -1,6 +1,6 @@
 // step_common.cuh -- device primitives of the persistent decode-step kernel:
 // mbarriers, bulk copies into shared memory, tagged (value, tag) words for
-// dataflow between CTAs, bounded waits, and the paired-fp32 dequant dot.
+// dataflow between CTAs, bounded waits, and the fixed-point dequant dot.
 #pragma once
 
 #include "internal.h"
@@ -41,6 +41,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended up to `hint_ns` (it is
+// woken as soon as the phase completes), so a waiting warp does not spin.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; "
+        "selp.u32 %0, 1, 0, p; }"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
@@ -70,6 +83,18 @@ __device__ __forceinline__ uint64_t get_word(const uint64_t *p) {
     uint64_t w;
     asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
     return w;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Publishes a ready flag after this thread's (and, through the fences the
+// other warps executed before handing over, the CTA's) earlier global writes.
+__device__ __forceinline__ void put_flag(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ int ld_flag(const int *p) {
@@ -126,16 +151,16 @@ template <int BITS>
 __device__ __forceinline__ void stage_chunk(const float *v, int lane, uint8_t *xf, int c, int nch,
                                             float *scale, float *xhat) {
     constexpr int PER = Fix<BITS>::VALS / 32;
-    float m = 0.0f;
+    // max |v| over the warp: the bit patterns of non-negative floats order
+    // like the values
+    uint32_t mb = 0;
 #pragma unroll
-    for (int k = 0; k < PER; k++) m = fmaxf(m, fabsf(v[k]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    // e: 2^(e-1) <= m < 2^e; f = 2^(15-e) exactly
-    int e = 0;
-    if ((__float_as_uint(m) >> 23) == 0) m = 0.0f;          // zero or subnormal: treat as zero
-    if (m > 0.0f) e = (int)((__float_as_uint(m) >> 23) & 0xff) - 126;
-    const float f = m > 0.0f ? __uint_as_float((uint32_t)(127 + 15 - e) << 23) : 0.0f;
+    for (int k = 0; k < PER; k++) mb = max(mb, __float_as_uint(fabsf(v[k])));
+    mb = __reduce_max_sync(0xffffffffu, mb);
+    // e: 2^(e-1) <= m < 2^e; f = 2^(15-e) exactly; zero or subnormal m: all zero
+    const bool nz = (mb >> 23) != 0;
+    const int e = nz ? (int)((mb >> 23) & 0xff) - 126 : 0;
+    const float f = nz ? __uint_as_float((uint32_t)(127 + 15 - e) << 23) : 0.0f;
     int sum = 0;
 #pragma unroll
     for (int k = 0; k < PER; k++) {
@@ -149,10 +174,9 @@ __device__ __forceinline__ void stage_chunk(const float *v, int lane, uint8_t *x
         w[byte] = (uint8_t)((q >> 8) & 0xff);
         w[byte + 4] = (uint8_t)(q & 0xff);
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    sum = __reduce_add_sync(0xffffffffu, sum);
     if (lane == 0) {
-        const float sc = m > 0.0f ? __uint_as_float((uint32_t)(127 + e - 15) << 23) : 0.0f;
+        const float sc = nz ? __uint_as_float((uint32_t)(127 + e - 15) << 23) : 0.0f;
         scale[c] = sc;
         xhat[c] = (float)sum * sc;
     }

@@ -53,7 +53,8 @@ class StackDesc(C.Structure):
     _fields_ = [("experts", C.c_void_p), ("routers", C.c_void_p), ("heads", C.c_void_p),
                 ("n_layers", C.c_int), ("depth", C.c_int), ("K", C.c_int),
                 ("self_predict", C.c_int), ("timeout_ns", C.c_ulonglong),
-                ("debug_unset_wait", C.c_int), ("debug_trace", C.c_void_p)]
+                ("debug_unset_wait", C.c_int), ("debug_trace", C.c_void_p),
+                ("inflight_bytes", C.c_uint)]
 
 
 # ------------------------------------------------------------------ loading
