@@ -139,7 +139,7 @@ struct Ctx {
     uint32_t sm_ring, sm_bar, sm_pend, sm_tmpl, sm_xf, sm_xsc, sm_xhat, sm_xf4, sm_xsc4, sm_xhat4,
         sm_stream, sm_hf, sm_hsc, sm_hhat, sm_vpw, sm_vx, sm_vdw, sm_vd, sm_vdacc, sm_vnw, sm_comb,
         sm_prep, sm_gf, sm_gsc, sm_ghat, sm_frec, sm_rcur, sm_rprev, sm_rw, sm_misc, sm_hraw, sm_graw,
-        sm_vdpl;
+        sm_vdpl, sm_poff;
     // one prep buffer: bytes, and float offsets of its parts
     uint32_t prep_bytes, pp_tsum, pp_bgu, pp_adn, pp_bd, pp_agu, pp_scale;
 };
@@ -205,6 +205,7 @@ __device__ __forceinline__ bool aborted() { return ld_flag(ctrl() + C_ABORT) != 
 // phase and the warp leaves together; false (error recorded) on timeout or
 // when another CTA has aborted.
 __device__ __forceinline__ bool wait_bar_warp_inl(uint64_t *b, uint32_t parity) {
+    if (__all_sync(0xffffffffu, mbar_test_wait(b, parity))) return true;
     const int lane = threadIdx.x & 31;
     uint64_t t0 = 0;
     if (lane == 0) t0 = now_ns();
@@ -290,55 +291,39 @@ __device__ __forceinline__ bool poll_vals(const uint64_t *base, const uint32_t (
     return true;
 }
 
-// Slow path of the reads that follow a flag wait: word i of this lane
-// (index idx(i), i < n) is re-read until it carries `tag`, its value handed to
-// sink(i, value) in order.  Warp-uniform result (false on timeout or abort).
-template <typename Idx, typename Sink>
-__device__ __noinline__ bool reread_words(const uint64_t *base, int n, uint32_t tag, Idx idx, Sink sink) {
-    const uint64_t t0 = now_ns();
-    bool ok = true;
-#pragma unroll 1
-    for (int i = 0; i < n && ok; i++) {
-#pragma unroll 1
-        for (int it = 0;; it++) {
-            const uint64_t w = get_word(base + idx(i));
-            if ((uint32_t)(w >> 32) == tag) {
-                sink(i, __uint_as_float((uint32_t)w));
-                break;
-            }
-            if ((it & 7) == 7 && (aborted() || now_ns() - t0 > CX().timeout_ns)) {
-                if (!aborted()) raise_error(MOE_ETIMEOUT);
-                ok = false;
-                break;
-            }
-        }
-    }
-    return __all_sync(0xffffffffu, ok);
-}
-
 // Reads the tagged words base[idx(i)], i < n, of this lane (loads four at a
 // time, in flight together) and hands their values to sink(i, value) in
-// order; if any word still carried an old tag, all are read again through the
-// bounded slow path (reset() first).  Warp-uniform result.
+// order.  Called after the flags of the words' writers, so their tags are
+// normally current; if any word still carried an old tag, the whole read is
+// repeated (reset() first) after a short sleep, bounded.  Warp-uniform result.
 template <typename Idx, typename Sink, typename Reset>
 __device__ __forceinline__ bool read_words(const uint64_t *base, int n, uint32_t tag, Idx idx,
                                            Sink sink, Reset reset) {
-    bool stale = false;
+    uint64_t t0 = 0;
 #pragma unroll 1
-    for (int i0 = 0; i0 < n; i0 += 4) {
-        uint64_t w[4];
+    for (int attempt = 0;; attempt++) {
+        bool stale = false;
+#pragma unroll 1
+        for (int i0 = 0; i0 < n; i0 += 4) {
+            uint64_t w[4];
 #pragma unroll
-        for (int k = 0; k < 4; k++) w[k] = i0 + k < n ? get_word(base + idx(i0 + k)) : 0ull;
+            for (int k = 0; k < 4; k++) w[k] = i0 + k < n ? get_word(base + idx(i0 + k)) : 0ull;
 #pragma unroll
-        for (int k = 0; k < 4; k++)
-            if (i0 + k < n) {
-                stale |= (uint32_t)(w[k] >> 32) != tag;
-                sink(i0 + k, __uint_as_float((uint32_t)w[k]));
-            }
+            for (int k = 0; k < 4; k++)
+                if (i0 + k < n) {
+                    stale |= (uint32_t)(w[k] >> 32) != tag;
+                    sink(i0 + k, __uint_as_float((uint32_t)w[k]));
+                }
+        }
+        if (!__any_sync(0xffffffffu, stale)) return true;
+        if (attempt == 0) t0 = now_ns();
+        else if (aborted() || now_ns() - t0 > CX().timeout_ns) {
+            if (!aborted()) raise_error(MOE_ETIMEOUT);
+            return false;
+        }
+        __nanosleep(256);
+        reset();
     }
-    if (!__any_sync(0xffffffffu, stale)) return true;
-    reset();
-    return reread_words(base, n, tag, idx, sink);
 }
 
 // Warp-collective bounded wait until every CTA's flag at workspace offset
@@ -528,10 +513,12 @@ __device__ __forceinline__ int item_chunks(const Grp &g) {
     }
 }
 
-// Items per bulk copy of a group: as many as fit kMaxPiece, a multiple of
-// the rows one warp task takes (so a down row keeps its warp in every slot).
+// Items per bulk copy of a group: as many as fit kMaxPiece, a multiple of the
+// rows one warp task takes; a slot's down rows of this CTA are one piece (the
+// host checks that they fit).
 template <int BITS>
 __device__ __forceinline__ int piece_items(const Grp &g) {
+    if (g.kind == KDOWN) return g.hi > g.lo ? g.hi - g.lo : 1;   // one piece per slot
     const int rpw = 32 / pow2_floor32(item_chunks<BITS>(g));
     int per = kMaxPiece / (int)g.item_bytes;
     if (per < 1) per = 1;
@@ -1177,38 +1164,45 @@ __device__ __noinline__ bool phase_h(int N, int warp, int lane) {
     const int ncw = warp < nch ? (nch - warp + kNW - 1) / kNW : 0;
     const uint32_t tg = tag_of(N);
     float *hraw = SM<float>(cx.sm_hraw);
-    // chunk ch of the concatenated slots covers h[ch * VALS, (ch+1) * VALS)
+    // chunk ch of the concatenated slots covers h[ch * VALS, (ch+1) * VALS);
+    // after this warp's h words come its down-LoRA partial words (a lane at
+    // or above an entry's rank reads h[0] instead -- published in this phase,
+    // so current -- and ignores it)
     auto hpos = [&](int i) { return (warp + kNW * (i / PER)) * VALS + lane + 32 * (i % PER); };
-    if (!read_words(ws_words(), ncw * PER, tg, [&](int i) { return cx.off_h / 8 + (uint32_t)hpos(i); },
-                    [&](int i, float v) { hraw[hpos(i)] = v; }, [] {}))
-        return false;
+    const int nx = ncw * PER;
+    int nv = 0;
+    const uint32_t *list = nullptr;
+    float *vdw = SM<float>(cx.sm_vdw) + warp * cx.n_dl * kMaxR;
+    auto zero = [&] {
+        for (int j = 0; j < cx.n_dl; j++) vdw[j * kMaxR + lane] = 0.0f;
+    };
     if (cx.dl_mask) {
         const int nlist = misc_i()[M_VDP_N0 + (ai == T_A_HEAD ? 0 : 1)];
-        const uint32_t *list = SM<uint32_t>(cx.sm_vdpl) + (ai == T_A_HEAD ? 0 : cx.n_dl * cx.n_cta);
-        const int nv = warp < nlist ? (nlist - warp + kNW - 1) / kNW : 0;
-        float *vdw = SM<float>(cx.sm_vdw) + warp * cx.n_dl * kMaxR;
-        auto zero = [&] {
-            for (int j = 0; j < cx.n_dl; j++) vdw[j * kMaxR + lane] = 0.0f;
-        };
+        list = SM<uint32_t>(cx.sm_vdpl) + (ai == T_A_HEAD ? 0 : cx.n_dl * cx.n_cta);
+        nv = warp < nlist ? (nlist - warp + kNW - 1) / kNW : 0;
         zero();
-        // a lane at or above an entry's rank reads h[0] instead (published in
-        // this phase, so current) and ignores it
-        auto ent = [&](int j) { return list[warp + kNW * j]; };
-        if (!read_words(ws_words(), nv, tg,
-                        [&](int j) {
-                            const uint32_t e = ent(j);
-                            const uint32_t sl = e >> 16;
-                            return lane < dl_rank((int)sl)
-                                       ? cx.off_vdp / 8 + (sl * cx.n_cta + (e & 0xffffu)) * kMaxR + lane
-                                       : cx.off_h / 8;
-                        },
-                        [&](int j, float v) {
-                            const int sl = (int)(ent(j) >> 16);
-                            if (lane < dl_rank(sl)) vdw[dl_index(sl) * kMaxR + lane] += v;
-                        },
-                        zero))
-            return false;
     }
+    if (!read_words(ws_words(), nx + nv, tg,
+                    [&](int i) {
+                        if (i < nx) return cx.off_h / 8 + (uint32_t)hpos(i);
+                        const uint32_t e = list[warp + kNW * (i - nx)];
+                        const uint32_t sl = e >> 16;
+                        return lane < dl_rank((int)sl)
+                                   ? cx.off_vdp / 8 + (sl * cx.n_cta + (e & 0xffffu)) * kMaxR + lane
+                                   : cx.off_h / 8;
+                    },
+                    [&](int i, float v) {
+                        if (i < nx) {
+                            hraw[hpos(i)] = v;
+                        } else {
+                            const int sl = (int)(list[warp + kNW * (i - nx)] >> 16);
+                            if (lane < dl_rank(sl)) vdw[dl_index(sl) * kMaxR + lane] += v;
+                        }
+                    },
+                    [&] {
+                        if (cx.dl_mask) zero();
+                    }))
+        return false;
     __syncwarp();
     uint8_t *hf = SM<uint8_t>(cx.sm_hf);
     float *hsc = SM<float>(cx.sm_hsc), *hhat = SM<float>(cx.sm_hhat);
@@ -1305,65 +1299,13 @@ __device__ __forceinline__ void task_head(int N, int ti, int gi, const uint8_t *
     }
 }
 
-// Down rows of one slot for this CTA's outputs; the warp owning output o
-// accumulates w_s y_s(o) over the slots and, at the last slot, combines:
-// out = residual + sum, published (with its share of the next layer's
-// gate/up LoRA partial, accumulated in vnw[warp]).
-template <int BITS>
-__device__ __forceinline__ void task_down(int N, int gi, const uint8_t *base, int i, int cnt, int lpr,
-                                       int warp, int lane) {
-    constexpr int VALS = 128 / BITS;
-    const Ctx &cx = CX();
-    const Tmplt &t = tmpls()[T_B];
-    const Grp &g = t.g[gi];
-    const int sub = lane % lpr, rsub = lane / lpr;
-    const int o = i + rsub;
-    const bool ok = rsub < cnt;
-    const int sl = g.slot;
-    float y;
-    rows_dot<BITS, 1>(base + (size_t)(ok ? rsub : 0) * g.item_bytes, 0, cx.F,
-                      SM<uint8_t>(cx.sm_hf) + (size_t)sl * cx.F * 2,
-                      SM<float>(cx.sm_hsc) + sl * (cx.F / VALS),
-                      SM<float>(cx.sm_hhat) + sl * (cx.F / VALS), sub, lpr, &y);
-    if (cx.dl_mask >> sl & 1u) {
-        const int r = dl_rank(sl), j = dl_index(sl);
-        const float *bd = prep_of(N, cx.pp_bd) + (j * cx.max_orows + (ok ? o - t.o_lo : 0)) * cx.rd;
-        const float *vd = SM<float>(cx.sm_vd) + j * kMaxR;
-        float a = 0.0f;
-        for (int k = sub; k < r; k += lpr) a = fmaf(bd[k], vd[k], a);
-        y += prep_of(N, cx.pp_scale)[sl < cx.K ? SC_DR : SC_DS] * warp_sum(a, lpr);
-    }
-    const float wgt = sl < cx.K ? SM<float>(cx.sm_rw)[N * cx.K + sl] : 1.0f;
-    float outv = 0.0f;
-    if (ok && sub == 0) {
-        float *cb = SM<float>(cx.sm_comb) + (o - t.o_lo);
-        const float acc = fmaf(wgt, y, sl == 0 ? 0.0f : *cb);
-        *cb = acc;
-        if (sl == cx.S - 1) {
-            outv = SM<float>(cx.sm_stream)[(size_t)(N & 1) * cx.d + o] + acc;
-            if (N + 1 < cx.depth) put_tagged(tagged(cx.off_out) + o, tag_of(N), outv);
-            else cx.out[o] = outv;
-        }
-    }
-    if (sl == cx.S - 1 && cx.gu_slot >= 0 && N + 1 < cx.depth) {
-        const int r2 = cx.rg + cx.ru, rpw = 32 / lpr;
-        const float *agu = prep_of(N, cx.pp_agu);
-        float *vn = SM<float>(cx.sm_vnw) + warp * 2 * kMaxR;
-        float a0 = 0.0f;
-        for (int rg = 0; rg < rpw; rg++) {
-            const float ov = __shfl_sync(0xffffffffu, outv, rg * lpr);
-            if (rg < cnt && lane < r2) a0 = fmaf(agu[(i + rg - t.o_lo) * r2 + lane], ov, a0);
-        }
-        vn[lane] += a0;
-    }
-}
-
-// End of phase A: this CTA's h rows (and fc1 / l rows) are out.  Every warp
-// fences its writes; the last one publishes, for the owners of a down-LoRA
-// slot's gate/up rows, the partial A_d h (sum of the warps' partials), then
-// the CTA's flag.
+// End of phase A: this CTA's h rows (and fc1 / l rows) are out.  The last warp
+// to get here publishes, for the owners of a down-LoRA slot's gate/up rows,
+// the partial A_d h (sum of the warps' partials), then the CTA's flag with a
+// release store: the other warps' writes reach it through the CTA-scope
+// hand-over of last_warp, and the release orders them all before the flag (a
+// reader that still finds an old tag reads again).
 __device__ __noinline__ void publish_a(int N, int c, int lane) {
-    __threadfence();
     if (!last_warp(misc_i() + M_CNT_A)) return;
     const Ctx &cx = CX();
     const Tmplt &ta = tmpls()[tmpl_A_index(N)];
@@ -1381,17 +1323,15 @@ __device__ __noinline__ void publish_a(int N, int c, int lane) {
             put_tagged(tagged(cx.off_vdp) + ((size_t)sl * cx.n_cta + c) * kMaxR + lane, tg, a);
         }
     }
-    __threadfence();
     __syncwarp();
     if (lane == 0) put_flag(flag_of(cx.off_hflag, c), tg);
 }
 
 // End of phase B: this CTA's rows of out are published.  The last warp
 // publishes the next layer's gate/up LoRA partial over those rows (sum of the
-// warps' partials), then the CTA's flag.
+// warps' partials), then the CTA's flag (release store, as in publish_a).
 __device__ __noinline__ void publish_d(int N, int c, int lane) {
     const Ctx &cx = CX();
-    __threadfence();
     if (!last_warp(misc_i() + M_CNT_D)) return;
     const uint32_t tg = tag_of(N);
     if (cx.gu_slot >= 0) {
@@ -1404,7 +1344,6 @@ __device__ __noinline__ void publish_d(int N, int c, int lane) {
         }
         if (lane < r2) put_tagged(tagged(cx.off_vp) + (size_t)c * 2 * kMaxR + lane, tag_of(N + 1), a);
     }
-    __threadfence();
     __syncwarp();
     if (lane == 0) put_flag(flag_of(cx.off_xflag, c), tg);
 }
@@ -1416,10 +1355,10 @@ struct RunState {
     uint32_t q, tasks, ok;
 };
 
-// Consumes this CTA's pieces of template ti, in the producer's order; warp
-// tasks of rpw items go round-robin to the consumer warps (down rows: by
-// output row, the same warp in every slot).  A leaf function: the tasks are
-// inlined, so no loop state is saved around calls.
+// Consumes this CTA's pieces of template ti (phase R or A), in the producer's
+// order; warp tasks of rpw items go round-robin to the consumer warps.  A
+// leaf function: the tasks are inlined, so no loop state is saved around
+// calls.
 template <int BITS>
 __device__ __noinline__ RunState run_tmpl(int N, int ti, float inv, int warp, int lane, RunState st) {
     const Ctx &cx = CX();
@@ -1443,22 +1382,105 @@ __device__ __noinline__ RunState run_tmpl(int N, int ti, float inv, int warp, in
             if (!wait_bar_warp_inl(bar_full(q % kNB), (q / kNB) & 1)) return RunState{rp.head, rp.q, tasks, 0u};
             const uint8_t *base = ring + start % cx.ring_bytes;
             const int ntask = (cnt + rpw - 1) / rpw;
-            const int k0 = kind == KDOWN ? (kNW + warp - ((i0 - lo) / rpw) % kNW) % kNW
-                                         : (int)((kNW + warp - tasks % kNW) % kNW);
+            const int k0 = (int)((kNW + warp - tasks % kNW) % kNW);
             for (int k = k0; k < ntask; k += kNW) {
                 const int li = k * rpw;
                 const uint8_t *b = base + (size_t)li * ib;
                 const int n = min(rpw, cnt - li);
                 if (kind == KGU) task_gu<BITS>(N, gi, b, i0 + li, n, lpr, inv, warp, lane);
-                else if (kind == KDOWN) task_down<BITS>(N, gi, b, i0 + li, n, lpr, warp, lane);
                 else task_head<BITS>(N, ti, gi, b, i0 + li, n, lpr, inv, lane);
             }
-            if (kind != KDOWN) tasks += ntask;
+            tasks += ntask;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty(q % kNB));
         }
     }
     return RunState{rp.head, rp.q, tasks, 1u};
+}
+
+// Phase B in one pass per output row: the S pieces (one per slot) are waited
+// for, then the warp owning output o (o - o_lo = warp mod kNW) spreads the
+// S * cps (slot, chunk) pairs of the row over its lanes, weights each slot's
+// part by its combine weight, adds the down-LoRA terms, reduces once and
+// writes out = residual + sum (published, with its share of the next layer's
+// gate/up LoRA partial in vnw[warp]).  Then the pieces are released.
+template <int BITS>
+__device__ __noinline__ RunState run_down(int N, int warp, int lane, RunState st) {
+    constexpr int VALS = 128 / BITS;
+    const Ctx &cx = CX();
+    const Tmplt &t = tmpls()[T_B];
+    const uint8_t *ring = SM<uint8_t>(cx.sm_ring);
+    uint32_t *poff = SM<uint32_t>(cx.sm_poff) + warp * kMaxSlots;
+    RingPos rp;
+    rp.head = st.head;
+    rp.q = st.q;
+    const int no = t.o_hi - t.o_lo;
+    const uint32_t q0 = rp.q;
+#pragma unroll 1
+    for (int sl = 0; sl < cx.S; sl++) {
+        const uint64_t start = rp.place((uint32_t)(no > 0 ? no : 1) * cx.rec_F, cx.ring_bytes);
+        const uint32_t q = rp.q++;
+        if (lane == 0) poff[sl] = (uint32_t)(start % cx.ring_bytes);
+        if (!wait_bar_warp_inl(bar_full(q % kNB), (q / kNB) & 1)) return RunState{rp.head, rp.q, st.tasks, 0u};
+    }
+    __syncwarp();
+    const int cps = cx.F / VALS, npair = cx.S * cps, cb = cx.F * BITS / 8;
+    const uint8_t *hf = SM<uint8_t>(cx.sm_hf);
+    const float *hsc = SM<float>(cx.sm_hsc), *hhat = SM<float>(cx.sm_hhat);
+    const float *rw = SM<float>(cx.sm_rw) + N * cx.K;
+    const float *stream = SM<float>(cx.sm_stream) + (size_t)(N & 1) * cx.d;
+    const float *sc = prep_of(N, cx.pp_scale);
+    const bool last = N + 1 >= cx.depth;
+    const bool vp = cx.gu_slot >= 0 && !last;
+    const int r2 = cx.rg + cx.ru;
+    float vn = 0.0f;
+#pragma unroll 1
+    for (int ol = warp; ol < no; ol += kNW) {
+        const int o = t.o_lo + ol;
+        float acc = 0.0f;
+        // the lane's (slot, chunk) pairs: lane, lane + 32, ...
+        int sl = lane / cps, c = lane - sl * cps;
+#pragma unroll 1
+        for (int pi = lane; pi < npair; pi += 32) {
+            const uint8_t *rec = ring + poff[sl] + (size_t)ol * cx.rec_F;
+            const uint4 q = *reinterpret_cast<const uint4 *>(rec + (size_t)kChunk * c);
+            const uint32_t sbw = *reinterpret_cast<const uint32_t *>(rec + cb + 4 * ((c * VALS) / kGroup));
+            int dq;
+            chunk_dot_fix<BITS, 1>(&q, reinterpret_cast<const uint4 *>(hf + (size_t)sl * cx.F * 2), cps, c, &dq);
+            const float2 sb = sb_f(sbw);
+            const float y = fmaf(sb.x, (float)dq * hsc[sl * cps + c], sb.y * hhat[sl * cps + c]);
+            acc = fmaf(sl < cx.K ? rw[sl] : 1.0f, y, acc);
+            c += 32;
+            while (c >= cps && sl < cx.S) {
+                c -= cps;
+                sl++;
+            }
+        }
+        // down LoRA of the slots that have one: lane k holds component k
+        if (cx.dl_mask) {
+            const float *bd = prep_of(N, cx.pp_bd);
+            const float *vd = SM<float>(cx.sm_vd);
+#pragma unroll 1
+            for (int s2 = 0; s2 < cx.S; s2++) {
+                if (!(cx.dl_mask >> s2 & 1u)) continue;
+                const int j = dl_index(s2);
+                if (lane < dl_rank(s2))
+                    acc = fmaf((s2 < cx.K ? rw[s2] : 1.0f) * sc[s2 < cx.K ? SC_DR : SC_DS] *
+                                   bd[(j * cx.max_orows + ol) * cx.rd + lane],
+                               vd[j * kMaxR + lane], acc);
+            }
+        }
+        const float outv = stream[o] + warp_sum(acc, 32);
+        if (lane == 0) {
+            if (!last) put_tagged(tagged(cx.off_out) + o, tag_of(N), outv);
+            else cx.out[o] = outv;
+        }
+        if (vp && lane < r2) vn = fmaf(prep_of(N, cx.pp_agu)[ol * r2 + lane], outv, vn);
+    }
+    if (vp) SM<float>(cx.sm_vnw)[warp * 2 * kMaxR + lane] += vn;
+    __syncwarp();
+    if (lane < cx.S) mbar_arrive(bar_empty((q0 + lane) % kNB));
+    return RunState{rp.head, rp.q, st.tasks, 1u};
 }
 
 template <int BITS>
@@ -1533,7 +1555,12 @@ struct Consumer {
         if (!phase_h<BITS>(N, warp, lane)) return false;
         if (!sync()) return false;               // h and vd visible to all warps
         if (warp == 0 && lane == 0) stamp_at(c, N, ST_H);
-        if (!run(N, T_B, inv)) return false;     // down rows + combine
+        {                                        // down rows + combine
+            const RunState rs = run_down<BITS>(N, warp, lane, RunState{rp.head, rp.q, tasks, 1u});
+            rp.head = rs.head;
+            rp.q = rs.q;
+            if (!rs.ok) return false;
+        }
         if (N + 1 < cx.depth) publish_d(N, c, lane);
         if (warp == 0 && lane == 0) stamp_at(c, N, ST_D);
         __syncwarp();
@@ -1981,6 +2008,7 @@ static int launch_decode_step(const moe_stack_desc *sd, const float *x0, float *
     cx.sm_hraw = take((size_t)cx.S * cx.F * 4);
     cx.sm_graw = take((size_t)(cx.H ? cx.H : 32) * 4);
     cx.sm_vdpl = take((size_t)2 * std::max(cx.n_dl, 1) * sms * 4);
+    cx.sm_poff = take((size_t)kNW * kMaxSlots * 4);
     cx.sm_ring = (uint32_t)al(off, 1024);
     long long room = (long long)smem_max - (long long)cx.sm_ring;
     room = room / 1024 * 1024;
@@ -1992,6 +2020,10 @@ static int launch_decode_step(const moe_stack_desc *sd, const float *x0, float *
     // always fit the ring with room to spare
     cx.inflight = std::min(cx.inflight, cx.ring_bytes / 2);
 
+    // a slot's down rows of one CTA are one piece
+    if ((size_t)cx.max_orows * cx.rec_F > (size_t)kMaxPiece)
+        return fail(MOE_EUNSUPPORTED, "decode_step: %d down rows of %u bytes exceed a %d-byte piece",
+                    cx.max_orows, cx.rec_F, kMaxPiece);
     // every item must fit a piece
     if (2 * cx.rec_d > (uint32_t)kMaxPiece || cx.rec_dh > (uint32_t)kMaxPiece)
         return fail(MOE_EUNSUPPORTED, "decode_step: d=%d rows exceed a %d-byte piece", cx.d,
