@@ -78,7 +78,7 @@ constexpr size_t kCtrlBytes = 256;
 // mbarriers after the kNB full / kNB empty pairs
 enum Bar : int {
     B_ROUTE = 0, B_CONS, B_END, B_PREP_FULL0, B_PREP_FULL1, B_PREP_EMPTY0, B_PREP_EMPTY1, B_X, B_H,
-    B_COUNT
+    B_AUX, B_COUNT
 };
 
 // last-warp counters and small values in the misc area (ints / floats)
@@ -119,7 +119,7 @@ struct LayerP {
 // shared memory at the start of the kernel.
 struct Ctx {
     int d, F, E, K, H, S, depth, n_res, self_predict, own0, t, n_cta;
-    int max_orows, max_erows, max_pairs, max_hrows;
+    int max_orows, max_erows, max_pairs, max_hrows, max_owners;
     int rg, ru, rd, rdr, rds, gu_slot, n_dl;   // LoRA ranks: gate, up (on gu_slot), down (max,
                                                // routed, shared); down-LoRA slot count
     uint32_t dl_mask;                          // slots with a down LoRA
@@ -138,8 +138,8 @@ struct Ctx {
     // shared-memory layout (byte offsets from the dynamic base)
     uint32_t sm_ring, sm_bar, sm_pend, sm_tmpl, sm_xf, sm_xsc, sm_xhat, sm_xf4, sm_xsc4, sm_xhat4,
         sm_stream, sm_hf, sm_hsc, sm_hhat, sm_vpw, sm_vx, sm_vdw, sm_vd, sm_vdacc, sm_vnw, sm_comb,
-        sm_prep, sm_gf, sm_gsc, sm_ghat, sm_frec, sm_rcur, sm_rprev, sm_rw, sm_misc, sm_hraw, sm_graw,
-        sm_vdpl, sm_poff;
+        sm_prep, sm_gf, sm_gsc, sm_ghat, sm_frec, sm_rcur, sm_rprev, sm_rw, sm_misc, sm_stage, sm_graw,
+        sm_poff;
     // one prep buffer: bytes, and float offsets of its parts
     uint32_t prep_bytes, pp_tsum, pp_bgu, pp_adn, pp_bd, pp_agu, pp_scale;
 };
@@ -255,6 +255,30 @@ __device__ __forceinline__ const uint64_t *ws_words() {
     return reinterpret_cast<const uint64_t *>(CX().ws);
 }
 
+// A word the staged copy held with an old tag (its writer's data became
+// visible after its flag): read again from global memory until current
+// (bounded; NaN and the error recorded on expiry, which ends the step).
+__device__ __noinline__ float refetch_word(uint32_t widx, uint32_t tag) {
+    const uint64_t *w = ws_words() + widx;
+    const uint64_t t0 = now_ns();
+#pragma unroll 1
+    for (int it = 0;; it++) {
+        const uint64_t v = get_word(w);
+        if ((uint32_t)(v >> 32) == tag) return __uint_as_float((uint32_t)v);
+        if ((it & 7) == 7 && (aborted() || now_ns() - t0 > CX().timeout_ns)) {
+            if (!aborted()) raise_error(MOE_ETIMEOUT);
+            return __int_as_float(0x7fc00000);
+        }
+        __nanosleep(128);
+    }
+}
+
+// Value of tagged word widx, copied into stage[i]; refetched if stale.
+__device__ __forceinline__ float staged(const uint64_t *stage, int i, uint32_t widx, uint32_t tag) {
+    const uint64_t v = stage[i];
+    return (uint32_t)(v >> 32) == tag ? __uint_as_float((uint32_t)v) : refetch_word(widx, tag);
+}
+
 __device__ __forceinline__ uint32_t *flag_of(uint32_t off, int c) {
     return reinterpret_cast<uint32_t *>(CX().ws + off) + c;
 }
@@ -291,38 +315,48 @@ __device__ __forceinline__ bool poll_vals(const uint64_t *base, const uint32_t (
     return true;
 }
 
-// Reads the tagged words base[idx(i)], i < n, of this lane (loads four at a
-// time, in flight together) and hands their values to sink(i, value) in
-// order.  Called after the flags of the words' writers, so their tags are
-// normally current; if any word still carried an old tag, the whole read is
-// repeated (reset() first) after a short sleep, bounded.  Warp-uniform result.
+// Reads the tagged words base[idx(i)], i < n, of this lane and hands their
+// values to sink(i, value) in order.  Called after the flags of the words'
+// writers, so their tags are normally current: the first pass uses plain L2
+// loads, eight in flight at a time.  If any word still carried an old tag,
+// the whole read is repeated (reset() first) with strong loads after a short
+// sleep, bounded.  Warp-uniform result.
 template <typename Idx, typename Sink, typename Reset>
 __device__ __forceinline__ bool read_words(const uint64_t *base, int n, uint32_t tag, Idx idx,
                                            Sink sink, Reset reset) {
-    uint64_t t0 = 0;
+    bool stale = false;
 #pragma unroll 1
-    for (int attempt = 0;; attempt++) {
-        bool stale = false;
+    for (int i0 = 0; i0 < n; i0 += 8) {
+        uint64_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            w[k] = i0 + k < n ? __ldcg(reinterpret_cast<const unsigned long long *>(base + idx(i0 + k)))
+                              : 0ull;
+#pragma unroll
+        for (int k = 0; k < 8; k++)
+            if (i0 + k < n) {
+                stale |= (uint32_t)(w[k] >> 32) != tag;
+                sink(i0 + k, __uint_as_float((uint32_t)w[k]));
+            }
+    }
+    if (!__any_sync(0xffffffffu, stale)) return true;
+    const uint64_t t0 = now_ns();
 #pragma unroll 1
-        for (int i0 = 0; i0 < n; i0 += 4) {
-            uint64_t w[4];
-#pragma unroll
-            for (int k = 0; k < 4; k++) w[k] = i0 + k < n ? get_word(base + idx(i0 + k)) : 0ull;
-#pragma unroll
-            for (int k = 0; k < 4; k++)
-                if (i0 + k < n) {
-                    stale |= (uint32_t)(w[k] >> 32) != tag;
-                    sink(i0 + k, __uint_as_float((uint32_t)w[k]));
-                }
+    for (;;) {
+        __nanosleep(256);
+        reset();
+        stale = false;
+#pragma unroll 1
+        for (int i = 0; i < n; i++) {
+            const uint64_t w = get_word(base + idx(i));
+            stale |= (uint32_t)(w >> 32) != tag;
+            sink(i, __uint_as_float((uint32_t)w));
         }
         if (!__any_sync(0xffffffffu, stale)) return true;
-        if (attempt == 0) t0 = now_ns();
-        else if (aborted() || now_ns() - t0 > CX().timeout_ns) {
+        if (aborted() || now_ns() - t0 > CX().timeout_ns) {
             if (!aborted()) raise_error(MOE_ETIMEOUT);
             return false;
         }
-        __nanosleep(256);
-        reset();
     }
 }
 
@@ -537,25 +571,24 @@ __device__ __noinline__ bool build_templates(int c, Tmplt *T) {
         split_bytes(t, c, cx.n_cta);
     }
     bool ok = true;
+#pragma unroll 1
     for (int head = 1; head >= 0; head--) {
         Tmplt &t = T[head ? T_A_HEAD : T_A_NOHEAD];
         t.n = 0;
         t.f1lo = t.f1hi = t.llo = t.lhi = 0;
+        #pragma unroll 1
         for (int s = 0; s < cx.S; s++) add_group(t, 2u * cx.rec_d, cx.F, KGU, s, cx.d);
         if (head) {
             if (cx.H) add_group(t, cx.rec_dh, cx.H, KFC1, 0, cx.d);
             add_group(t, cx.rec_dh, cx.E, KLX, 0, cx.d);
         }
         split_bytes(t, c, cx.n_cta);
-        // the (slot, owner) words of the down-LoRA partials, slot by slot
-        uint32_t *list = SM<uint32_t>(cx.sm_vdpl) + (head ? 0 : cx.n_dl * cx.n_cta);
-        int nl = 0;
+        // the down-LoRA owner partials must fit the stage
+#pragma unroll 1
         for (int s = 0; s < cx.S; s++)
-            if (cx.dl_mask >> s & 1u)
-                for (int o = t.own0[s]; o <= t.own1[s] && nl < cx.n_dl * cx.n_cta; o++)
-                    list[nl++] = (uint32_t)s << 16 | (uint32_t)o;
-        misc_i()[head ? M_VDP_N0 : M_VDP_N1] = nl;
+            if ((cx.dl_mask >> s & 1u) && t.own1[s] - t.own0[s] + 1 > cx.max_owners) ok = false;
         int pairs = 0;
+        #pragma unroll 1
         for (int s = 0; s < cx.S; s++) pairs += t.phi[s] - t.plo[s];
         ok = ok && pairs <= cx.max_pairs && (t.f1hi - t.f1lo) + (t.lhi - t.llo) <= cx.max_hrows;
     }
@@ -565,6 +598,7 @@ __device__ __noinline__ bool build_templates(int c, Tmplt *T) {
     t.o_hi = (int)((long long)cx.d * (c + 1) / cx.n_cta);
     t.e_lo = (int)((long long)cx.E * c / cx.n_cta);
     t.e_hi = (int)((long long)cx.E * (c + 1) / cx.n_cta);
+#pragma unroll 1
     for (int s = 0; s < cx.S; s++) add_group(t, cx.rec_F, cx.d, KDOWN, s, cx.F, t.o_lo, t.o_hi);
     return ok && t.o_hi - t.o_lo <= cx.max_orows && t.e_hi - t.e_lo <= cx.max_erows;
 }
@@ -574,13 +608,22 @@ __device__ __forceinline__ int tmpl_A_index(int N) { return head_runs(N) ? T_A_H
 // ---------------------------------------------------------------- ring
 // Byte ring of pieces: a piece never straddles the end of the ring; producer
 // and consumers place pieces with the same rule, so they agree on offsets.
+// head: absolute position (monotonic; for the producer's space accounting),
+// off: head within the ring (kept alongside, so no division is needed).
 struct RingPos {
     uint64_t head = 0;
-    uint32_t q = 0;
-    __device__ __forceinline__ uint64_t place(uint32_t bytes, uint32_t rb) {
-        uint64_t start = head;
-        if ((uint32_t)(start % rb) + bytes > rb) start = (start / rb + 1) * rb;
-        head = start + bytes;
+    uint32_t off = 0, q = 0;
+    // places a piece; returns its absolute start, its ring offset in *at
+    __device__ __forceinline__ uint64_t place(uint32_t bytes, uint32_t rb, uint32_t *at) {
+        if (off + bytes > rb) {
+            head += rb - off;
+            off = 0;
+        }
+        *at = off;
+        const uint64_t start = head;
+        head += bytes;
+        off += bytes;
+        if (off == rb) off = 0;
         return start;
     }
 };
@@ -602,6 +645,7 @@ __device__ __forceinline__ void rows_dot(const uint8_t *rec, uint32_t stride, in
 #pragma unroll
     for (int r = 0; r < R; r++) acc[r] = 0.0f;
     const uint4 *xq = reinterpret_cast<const uint4 *>(xf);
+#pragma unroll 1
     for (int c = sub; c < nch; c += lpr) {
         uint4 q[R];
         uint32_t sbw[R];
@@ -712,7 +756,7 @@ struct Producer {
     uint32_t bbytes = 0;
     uint64_t bend = 0;
     const uint8_t *my_src = nullptr;
-    uint32_t my_bytes = 0;
+    uint32_t my_bytes = 0, my_off = 0;
     uint64_t my_start = 0;
 
     __device__ __forceinline__ bool flush() {
@@ -740,7 +784,7 @@ struct Producer {
             const uint32_t q = qb + lane;
             pend[q % kNB] = my_start + my_bytes;
             mbar_arrive_expect_tx(bar_full(q % kNB), my_bytes);
-            bulk_g2s(SM<uint8_t>(cx.sm_ring) + my_start % cx.ring_bytes, my_src, my_bytes,
+            bulk_g2s(SM<uint8_t>(cx.sm_ring) + my_off, my_src, my_bytes,
                      bar_full(q % kNB));
         }
         __syncwarp();
@@ -756,12 +800,14 @@ struct Producer {
         const uint32_t cap = cx.inflight / 2 > bytes ? cx.inflight / 2 : bytes;
         if (nb == 32 || (nb > 0 && bbytes + bytes > cap))
             if (!flush()) return false;
-        const uint64_t start = rp.place(bytes, cx.ring_bytes);
+        uint32_t at;
+        const uint64_t start = rp.place(bytes, cx.ring_bytes, &at);
         rp.q++;
         if (lane == nb) {
             my_src = src;
             my_bytes = bytes;
             my_start = start;
+            my_off = at;
         }
         nb++;
         bbytes += bytes;
@@ -787,10 +833,12 @@ struct Producer {
         const Ctx &cx = CX();
         const Tmplt &t = tmpls()[ti];
         const int *route = SM<int>(cx.sm_rcur) + N * cx.K;
+        #pragma unroll 1
         for (int gi = 0; gi < t.n; gi++) {
             const Grp &g = t.g[gi];
             const uint8_t *src = group_src(N, g, route);
             const int per = piece_items<BITS>(g);
+            #pragma unroll 1
             for (int i0 = g.lo; i0 < g.hi; i0 += per) {
                 const uint32_t bytes = (uint32_t)min(per, g.hi - i0) * g.item_bytes;
                 if (!add(src + (size_t)i0 * g.item_bytes, bytes)) return false;
@@ -802,6 +850,7 @@ struct Producer {
     __device__ __forceinline__ bool routes_valid(int N) {
         const Ctx &cx = CX();
         bool ok = true;
+        #pragma unroll 1
         for (int k = 0; k < cx.K; k++)
             if ((unsigned)SM<int>(cx.sm_rcur)[N * cx.K + k] >= (unsigned)cx.E) ok = false;
         if (!ok && lane == 0) raise_error(MOE_EINVAL);
@@ -833,6 +882,7 @@ struct Producer {
         if (lane == 0) {
             const uint32_t q_end = qb;
             const uint32_t from = q_end > (uint32_t)kNB && landed < q_end - kNB ? q_end - kNB : landed;
+            #pragma unroll 1
             for (uint32_t q = from; q < q_end; q++) {
                 if (!mbar_try_wait(bar_full(q % kNB), (q / kNB) & 1)) {
                     const uint64_t t0 = now_ns();
@@ -859,7 +909,7 @@ __device__ __noinline__ void aux_load_agu(const LayerP *L, float *agu, int lane)
     const Tmplt &tb = tmpls()[T_B];
     const int r2 = cx.rg + cx.ru, no = tb.o_hi - tb.o_lo;
     const uint16_t *Ag = L->slora[0].A, *Au = L->slora[1].A;
-    #pragma unroll 1
+#pragma unroll 1
     for (int i = lane; i < no * r2; i += 32) {
         const int o = tb.o_lo + i / r2, k = i % r2;
         agu[i] = k < cx.rg ? half_f(Ag[(size_t)k * cx.d + o]) : half_f(Au[(size_t)(k - cx.rg) * cx.d + o]);
@@ -888,6 +938,7 @@ __device__ __noinline__ void aux_vp0(const LayerP *L0, int c, int lane) {
 __device__ __forceinline__ bool aux_routes_ok(int N) {
     const Ctx &cx = CX();
     bool ok = true;
+#pragma unroll 1
     for (int k = 0; k < cx.K; k++)
         ok = ok && (unsigned)SM<int>(cx.sm_rcur)[N * cx.K + k] < (unsigned)cx.E &&
              (unsigned)SM<int>(cx.sm_rprev)[N * cx.K + k] < (unsigned)cx.E;
@@ -920,7 +971,9 @@ __device__ __noinline__ void aux_prep(const LayerP *Lp, const LayerP *Lnext, int
             const uint16_t *bias = fc1 ? L.b1 : L.bl;
             float a = 0.0f;
             if (tab) {
+                #pragma unroll 1
                 for (int k = 0; k < cx.K; k++) a += half_f(tab[(size_t)cur[k] * width + row]);
+                #pragma unroll 1
                 for (int k = 0; k < cx.K; k++) a += half_f(tab[(size_t)(cx.E + prev[k]) * width + row]);
             }
             if (bias) a += half_f(bias[row]);
@@ -974,38 +1027,41 @@ __device__ __noinline__ bool aux_fc2(const LayerP *Lp, int N, int lane) {
     uint8_t *frec = SM<uint8_t>(cx.sm_frec);
     // records of this CTA's rows (plain 16-byte loads)
     const int q16 = cx.rec_H / 16;
-    #pragma unroll 1
+#pragma unroll 1
     for (int i = lane; i < ne * q16; i += 32)
         reinterpret_cast<uint4 *>(frec)[i] =
             *reinterpret_cast<const uint4 *>(Lp->fc2 + (size_t)tb.e_lo * cx.rec_H + (size_t)i * 16);
-    // every CTA has finished phase A of layer N (fc1 and l rows published)
+    // every CTA has finished phase A of layer N (fc1 and l rows published):
+    // gelu(fc1 f) in one bulk copy (into graw), l f of this CTA's rows (lane
+    // i: row i) with plain loads, then gelu(fc1 f) staged chunk by chunk
     if (!poll_flags(cx.off_hflag, tg, lane, 128)) return false;
-    // gelu(fc1 f) (lane j: value j of every 32-value chunk, into graw) and l f
-    // of this CTA's rows (lane i: row i), then staged chunk by chunk
     const int nch = cx.H / 32;
     uint8_t *gf = SM<uint8_t>(cx.sm_gf);
-    float *gsc = SM<float>(cx.sm_gsc), *ghat = SM<float>(cx.sm_ghat), *graw = SM<float>(cx.sm_graw);
+    float *gsc = SM<float>(cx.sm_gsc), *ghat = SM<float>(cx.sm_ghat);
+    const uint64_t *graw = SM<uint64_t>(cx.sm_graw);
+    const uint32_t gw = cx.off_ga / 8 + (uint32_t)(N * cx.H);
+    if (lane == 0) {
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar(B_AUX), (uint32_t)cx.H * 8);
+        bulk_g2s(SM<uint8_t>(cx.sm_graw), cx.ws + (size_t)gw * 8, (uint32_t)cx.H * 8, bar(B_AUX));
+    }
     float zl = 0.0f;
-    if (!read_words(ws_words(), nch + (lane < ne ? 1 : 0), tg,
-                    [&](int i) {
-                        return i < nch ? cx.off_ga / 8 + (uint32_t)(N * cx.H + i * 32 + lane)
-                                       : cx.off_zl / 8 + (uint32_t)(N * cx.E + tb.e_lo + lane);
-                    },
-                    [&](int i, float v) {
-                        if (i < nch) graw[i * 32 + lane] = v;
-                        else zl = v;
-                    },
-                    [] {}))
-        return false;
-    __syncwarp();
+    if (lane < ne) {
+        const uint32_t zw = cx.off_zl / 8 + (uint32_t)(N * cx.E + tb.e_lo + lane);
+        const uint64_t v = get_word(ws_words() + zw);
+        zl = (uint32_t)(v >> 32) == tg ? __uint_as_float((uint32_t)v) : refetch_word(zw, tg);
+    }
+    // the k-th fc2 call is for head k (heads run for N = 0, 1, ...)
+    if (!wait_bar_warp(bar(B_AUX), (uint32_t)N & 1u)) return false;
 #pragma unroll 1
     for (int ch = 0; ch < nch; ch++) {
-        const float v = graw[ch * 32 + lane];
+        const float v = staged(graw, ch * 32 + lane, gw + ch * 32 + lane, tg);
         stage_chunk<4>(&v, lane, gf, ch, nch, gsc, ghat);
     }
     __syncwarp();
     const int lpr = pow2_floor32(nch), rpw = 32 / lpr;
     const int sub = lane % lpr, rsub = lane / lpr;
+#pragma unroll 1
     for (int i0 = 0; i0 < ne; i0 += rpw) {
         const int i = i0 + rsub;
         float a;
@@ -1025,6 +1081,7 @@ template <int BITS>
 __device__ __noinline__ void aux_main(const Params &p, int c, int lane) {
     const Ctx &cx = CX();
     if (cx.gu_slot >= 0) aux_vp0(&p.layer[0], c, lane);
+#pragma unroll 1
     for (int N = 0; N < cx.depth; N++) {
         if (N >= 2 && !wait_bar_warp(bar(B_PREP_EMPTY0 + (N & 1)), ((N >> 1) - 1) & 1)) return;
         if (N == 0 && cx.own0 && !wait_bar_warp(bar(B_ROUTE), 0)) return;
@@ -1046,6 +1103,7 @@ __device__ __noinline__ void aux_main(const Params &p, int c, int lane) {
     if (head_runs(cx.depth - 1) && !aux_fc2(&layer_of(p, cx.depth - 1), cx.depth - 1, lane)) return;
     // top-K of the heads this CTA owns: routes for the next step
     const int nxt = (cx.t + 1) % 3;
+#pragma unroll 1
     for (int N = c; N < cx.depth; N += cx.n_cta) {
         if (!head_runs(N)) continue;
         const int tgt = N + 1 < cx.depth ? N + 1 : 0;
@@ -1073,40 +1131,23 @@ __device__ __forceinline__ bool last_warp(int *cnt) {
     return true;
 }
 
-// x of layer N (the previous layer's out, or x0), staged for the GEMVs (and,
-// with 2-bit experts, in the int4 layout for the heads); the raw values go to
-// the residual stream.  Warp w reads and stages chunks w, w+kNW, ... (lane j:
-// values j, j+32 of a chunk).  With want_vp also the partial A x of every CTA
-// for the gate/up LoRA (lane k: component k, warp w: CTAs w, w+kNW, ...),
-// summed per lane in CTA order; the last warp sums the warps' sums into vx and
-// the sums of squares into 1/rms.  Called after the flags of layer N-1.
+// x of layer N, staged for the GEMVs (and, with 2-bit experts, in the int4
+// layout for the heads); the raw values go to the residual stream.  x is the
+// previous layer's out (already copied into the stage with its tags) or x0.
+// Warp w stages chunks w, w+kNW, ... (lane j: values j, j+32 of a chunk).
+// With want_vp also the partial A x of every CTA for the gate/up LoRA (lane
+// k: component k, warp w: CTAs w, w+kNW, ...), summed per lane in CTA order;
+// the last warp sums the warps' sums into vx and the sums of squares into
+// 1/rms.
 template <int BITS>
 __device__ __noinline__ bool phase_x(int N, bool want_x, bool want_vp, int warp, int lane) {
     constexpr int VALS = 128 / BITS, PER = VALS / 32;
     const Ctx &cx = CX();
     const int d = cx.d, nch = d / VALS;
     float *stream = SM<float>(cx.sm_stream) + (size_t)(N & 1) * d;
+    const uint64_t *stage = SM<uint64_t>(cx.sm_stage);
+    const uint32_t tx = N > 0 ? tag_of(N - 1) : 0u;
     const int ncw = want_x && warp < nch ? (nch - warp + kNW - 1) / kNW : 0;   // chunks of this warp
-    const int nx = ncw * PER;
-    auto xpos = [&](int i) { return (warp + kNW * (i / PER)) * VALS + lane + 32 * (i % PER); };
-    if (N == 0) {
-#pragma unroll 1
-        for (int i = 0; i < nx; i++) stream[xpos(i)] = cx.x0[xpos(i)];
-    } else if (!read_words(ws_words(), nx, tag_of(N - 1),
-                           [&](int i) { return cx.off_out / 8 + (uint32_t)xpos(i); },
-                           [&](int i, float v) { stream[xpos(i)] = v; }, [] {})) {
-        return false;
-    }
-    float va = 0.0f;
-    if (want_vp) {
-        const int nvo = (cx.n_cta - warp + kNW - 1) / kNW;               // CTAs of this warp
-        const int n = lane < cx.rg + cx.ru ? nvo : 0;
-        if (!read_words(ws_words(), n, tag_of(N),
-                        [&](int j) { return cx.off_vp / 8 + (uint32_t)((warp + kNW * j) * 2 * kMaxR + lane); },
-                        [&](int, float v) { va += v; }, [&] { va = 0.0f; }))
-            return false;
-    }
-    __syncwarp();
     uint8_t *xf = SM<uint8_t>(cx.sm_xf), *xf4 = SM<uint8_t>(cx.sm_xf4);
     float *xsc = SM<float>(cx.sm_xsc), *xhat = SM<float>(cx.sm_xhat);
     float *xsc4 = SM<float>(cx.sm_xsc4), *xhat4 = SM<float>(cx.sm_xhat4);
@@ -1117,7 +1158,9 @@ __device__ __noinline__ bool phase_x(int N, bool want_x, bool want_vp, int warp,
         float v[PER];
 #pragma unroll
         for (int m = 0; m < PER; m++) {
-            v[m] = stream[ch * VALS + lane + 32 * m];
+            const int pos = ch * VALS + lane + 32 * m;
+            v[m] = N == 0 ? cx.x0[pos] : staged(stage, pos, cx.off_out / 8 + pos, tx);
+            stream[pos] = v[m];
             ss = fmaf(v[m], v[m], ss);
         }
         stage_chunk<BITS>(v, lane, xf, ch, nch, xsc, xhat);
@@ -1126,6 +1169,15 @@ __device__ __noinline__ bool phase_x(int N, bool want_x, bool want_vp, int warp,
             for (int m = 0; m < PER; m++)
                 stage_chunk<4>(&v[m], lane, xf4, ch * PER + m, d / 32, xsc4, xhat4);
         }
+    }
+    float va = 0.0f;
+    if (want_vp) {
+        const int nvo = (cx.n_cta - warp + kNW - 1) / kNW;               // CTAs of this warp
+        const int n = lane < cx.rg + cx.ru ? nvo : 0;
+        if (!read_words(ws_words(), n, tag_of(N),
+                        [&](int j) { return cx.off_vp / 8 + (uint32_t)((warp + kNW * j) * 2 * kMaxR + lane); },
+                        [&](int, float v) { va += v; }, [&] { va = 0.0f; }))
+            return false;
     }
     float *mf = misc_f();
     float *vpw = SM<float>(cx.sm_vpw);
@@ -1137,11 +1189,13 @@ __device__ __noinline__ bool phase_x(int N, bool want_x, bool want_vp, int warp,
     if (last_warp(misc_i() + M_CNT_X)) {
         if (want_x && lane == 0) {
             float tot = 0.0f;
+#pragma unroll 1
             for (int w = 0; w < kNW; w++) tot += mf[M_SS + w];
             mf[M_INV] = N > 0 ? 1.0f / sqrtf(tot / d + 1e-6f) : 1.0f;
         }
         if (want_vp) {
             float a = 0.0f;
+#pragma unroll 1
             for (int w = 0; w < kNW; w++) a += vpw[w * 2 * kMaxR + lane];
             SM<float>(cx.sm_vx)[lane] = a;
         }
@@ -1149,61 +1203,21 @@ __device__ __noinline__ bool phase_x(int N, bool want_x, bool want_vp, int warp,
     return true;
 }
 
-// h of every slot (read into hraw, then staged per slot: warp w takes chunks
-// w, w+kNW, ...); with down LoRA also the partial A_d h of every owner CTA
-// (lane k: component k; list entry e = slot << 16 | owner, warp w takes
-// entries w, w+kNW, ...), summed per warp in list order into vdw and over the
-// warps into vd by the last warp.  Called after the flags of phase A.
+// h of every slot, staged per slot (warp w takes chunks w, w+kNW, ... of the
+// concatenated slots), from the stage: the h words, then for each down-LoRA
+// slot the partial A_d h words of its owner CTAs (32 per owner, lane k:
+// component k), which warp w sums for owners w, w+kNW, ... in order into vdw;
+// the last warp sums the warps' sums into vd.
 template <int BITS>
 __device__ __noinline__ bool phase_h(int N, int warp, int lane) {
     constexpr int VALS = 128 / BITS, PER = VALS / 32;
     const Ctx &cx = CX();
-    const int ai = tmpl_A_index(N);
+    const Tmplt &ta = tmpls()[tmpl_A_index(N)];
     const int cps = cx.F / VALS;                    // chunks per slot
     const int nch = cx.S * cps;
     const int ncw = warp < nch ? (nch - warp + kNW - 1) / kNW : 0;
     const uint32_t tg = tag_of(N);
-    float *hraw = SM<float>(cx.sm_hraw);
-    // chunk ch of the concatenated slots covers h[ch * VALS, (ch+1) * VALS);
-    // after this warp's h words come its down-LoRA partial words (a lane at
-    // or above an entry's rank reads h[0] instead -- published in this phase,
-    // so current -- and ignores it)
-    auto hpos = [&](int i) { return (warp + kNW * (i / PER)) * VALS + lane + 32 * (i % PER); };
-    const int nx = ncw * PER;
-    int nv = 0;
-    const uint32_t *list = nullptr;
-    float *vdw = SM<float>(cx.sm_vdw) + warp * cx.n_dl * kMaxR;
-    auto zero = [&] {
-        for (int j = 0; j < cx.n_dl; j++) vdw[j * kMaxR + lane] = 0.0f;
-    };
-    if (cx.dl_mask) {
-        const int nlist = misc_i()[M_VDP_N0 + (ai == T_A_HEAD ? 0 : 1)];
-        list = SM<uint32_t>(cx.sm_vdpl) + (ai == T_A_HEAD ? 0 : cx.n_dl * cx.n_cta);
-        nv = warp < nlist ? (nlist - warp + kNW - 1) / kNW : 0;
-        zero();
-    }
-    if (!read_words(ws_words(), nx + nv, tg,
-                    [&](int i) {
-                        if (i < nx) return cx.off_h / 8 + (uint32_t)hpos(i);
-                        const uint32_t e = list[warp + kNW * (i - nx)];
-                        const uint32_t sl = e >> 16;
-                        return lane < dl_rank((int)sl)
-                                   ? cx.off_vdp / 8 + (sl * cx.n_cta + (e & 0xffffu)) * kMaxR + lane
-                                   : cx.off_h / 8;
-                    },
-                    [&](int i, float v) {
-                        if (i < nx) {
-                            hraw[hpos(i)] = v;
-                        } else {
-                            const int sl = (int)(list[warp + kNW * (i - nx)] >> 16);
-                            if (lane < dl_rank(sl)) vdw[dl_index(sl) * kMaxR + lane] += v;
-                        }
-                    },
-                    [&] {
-                        if (cx.dl_mask) zero();
-                    }))
-        return false;
-    __syncwarp();
+    const uint64_t *stage = SM<uint64_t>(cx.sm_stage);
     uint8_t *hf = SM<uint8_t>(cx.sm_hf);
     float *hsc = SM<float>(cx.sm_hsc), *hhat = SM<float>(cx.sm_hhat);
 #pragma unroll 1
@@ -1211,15 +1225,38 @@ __device__ __noinline__ bool phase_h(int N, int warp, int lane) {
         const int ch = warp + kNW * i, sc = ch / cps, cl = ch % cps;
         float v[PER];
 #pragma unroll
-        for (int m = 0; m < PER; m++) v[m] = hraw[ch * VALS + lane + 32 * m];
+        for (int m = 0; m < PER; m++) {
+            const int pos = ch * VALS + lane + 32 * m;
+            v[m] = staged(stage, pos, cx.off_h / 8 + pos, tg);
+        }
         stage_chunk<BITS>(v, lane, hf + (size_t)sc * cx.F * 2, cl, cps, hsc + sc * cps, hhat + sc * cps);
     }
-    if (cx.dl_mask && last_warp(misc_i() + M_CNT_H)) {
-        float *vd = SM<float>(cx.sm_vd), *vdw0 = SM<float>(cx.sm_vdw);
-        for (int j = 0; j < cx.n_dl; j++) {
+    if (cx.dl_mask) {
+        float *vdw = SM<float>(cx.sm_vdw) + warp * cx.n_dl * kMaxR;
+        int base = cx.S * cx.F;
+#pragma unroll 1
+        for (int sl = 0; sl < cx.S; sl++) {
+            if (!(cx.dl_mask >> sl & 1u)) continue;
+            const int no = ta.own1[sl] - ta.own0[sl] + 1, j = dl_index(sl);
             float a = 0.0f;
-            for (int w = 0; w < kNW; w++) a += vdw0[(w * cx.n_dl + j) * kMaxR + lane];
-            vd[j * kMaxR + lane] = a;
+            if (lane < dl_rank(sl)) {
+#pragma unroll 1
+                for (int i = warp; i < no; i += kNW)
+                    a += staged(stage, base + i * kMaxR + lane,
+                                cx.off_vdp / 8 + (uint32_t)((sl * cx.n_cta + ta.own0[sl] + i) * kMaxR + lane), tg);
+            }
+            vdw[j * kMaxR + lane] = a;
+            base += no * kMaxR;
+        }
+        if (last_warp(misc_i() + M_CNT_H)) {
+            float *vd = SM<float>(cx.sm_vd), *vdw0 = SM<float>(cx.sm_vdw);
+#pragma unroll 1
+            for (int j = 0; j < cx.n_dl; j++) {
+                float a = 0.0f;
+#pragma unroll 1
+                for (int w = 0; w < kNW; w++) a += vdw0[(w * cx.n_dl + j) * kMaxR + lane];
+                vd[j * kMaxR + lane] = a;
+            }
         }
     }
     return true;
@@ -1249,7 +1286,9 @@ __device__ __forceinline__ void task_gu(int N, int gi, const uint8_t *base, int 
         const float *vx = SM<float>(cx.sm_vx);
         float a = 0.0f, b = 0.0f;
         if (ok) {
+            #pragma unroll 1
             for (int k = sub; k < cx.rg; k += lpr) a = fmaf(bgu[k], vx[k], a);
+            #pragma unroll 1
             for (int k = sub; k < cx.ru; k += lpr) b = fmaf(bgu[cx.rg + k], vx[cx.rg + k], b);
         }
         gg += sc[SC_G] * inv * warp_sum(a, lpr);
@@ -1261,9 +1300,11 @@ __device__ __forceinline__ void task_gu(int N, int gi, const uint8_t *base, int 
         const int r = dl_rank(sl), j = dl_index(sl);
         const float *adn = prep_of(N, cx.pp_adn) + (t.pbase[sl] + (ok ? f - t.plo[sl] : 0)) * cx.rd;
         float *vdacc = SM<float>(cx.sm_vdacc) + (warp * cx.n_dl + j) * kMaxR;
+        #pragma unroll 1
         for (int k0 = 0; k0 < r; k0 += lpr) {
             const int k = k0 + sub;
             float a = (ok && k < r) ? adn[k] * h : 0.0f;
+            #pragma unroll 1
             for (int o = lpr; o < 32; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
             if (rsub == 0 && k < r) vdacc[k] += a;
         }
@@ -1310,11 +1351,13 @@ __device__ __noinline__ void publish_a(int N, int c, int lane) {
     const Ctx &cx = CX();
     const Tmplt &ta = tmpls()[tmpl_A_index(N)];
     const uint32_t tg = tag_of(N);
+#pragma unroll 1
     for (int sl = 0; sl < cx.S; sl++) {
         if (!(cx.dl_mask >> sl & 1u) || c < ta.own0[sl] || c > ta.own1[sl]) continue;
         const int r = dl_rank(sl), j = dl_index(sl);
         if (lane < r) {
             float a = 0.0f;
+            #pragma unroll 1
             for (int w = 0; w < kNW; w++) {
                 float *v = SM<float>(cx.sm_vdacc) + (w * cx.n_dl + j) * kMaxR + lane;
                 a += *v;
@@ -1338,6 +1381,7 @@ __device__ __noinline__ void publish_d(int N, int c, int lane) {
         const int r2 = cx.rg + cx.ru;
         float *vnw = SM<float>(cx.sm_vnw);
         float a = 0.0f;
+        #pragma unroll 1
         for (int w = 0; w < kNW; w++) {
             a += vnw[w * 2 * kMaxR + lane];
             vnw[w * 2 * kMaxR + lane] = 0.0f;
@@ -1352,7 +1396,7 @@ __device__ __noinline__ void publish_d(int N, int c, int lane) {
 // template's pieces to the next.
 struct RunState {
     uint64_t head;
-    uint32_t q, tasks, ok;
+    uint32_t off, q, tasks, ok;
 };
 
 // Consumes this CTA's pieces of template ti (phase R or A), in the producer's
@@ -1366,8 +1410,10 @@ __device__ __noinline__ RunState run_tmpl(int N, int ti, float inv, int warp, in
     const uint8_t *ring = SM<uint8_t>(cx.sm_ring);
     RingPos rp;
     rp.head = st.head;
+    rp.off = st.off;
     rp.q = st.q;
     uint32_t tasks = st.tasks;
+#pragma unroll 1
     for (int gi = 0; gi < t.n; gi++) {
         const Grp &g = t.g[gi];
         const int kind = g.kind, lo = g.lo, hi = g.hi;
@@ -1375,14 +1421,17 @@ __device__ __noinline__ RunState run_tmpl(int N, int ti, float inv, int warp, in
         const int per = piece_items<BITS>(g);
         const int lpr = pow2_floor32(item_chunks<BITS>(g));
         const int rpw = 32 / lpr;
+        #pragma unroll 1
         for (int i0 = lo; i0 < hi; i0 += per) {
             const int cnt = min(per, hi - i0);
-            const uint64_t start = rp.place((uint32_t)cnt * ib, cx.ring_bytes);
+            uint32_t at;
+            rp.place((uint32_t)cnt * ib, cx.ring_bytes, &at);
             const uint32_t q = rp.q++;
-            if (!wait_bar_warp_inl(bar_full(q % kNB), (q / kNB) & 1)) return RunState{rp.head, rp.q, tasks, 0u};
-            const uint8_t *base = ring + start % cx.ring_bytes;
+            if (!wait_bar_warp_inl(bar_full(q % kNB), (q / kNB) & 1)) return RunState{rp.head, rp.off, rp.q, tasks, 0u};
+            const uint8_t *base = ring + at;
             const int ntask = (cnt + rpw - 1) / rpw;
             const int k0 = (int)((kNW + warp - tasks % kNW) % kNW);
+            #pragma unroll 1
             for (int k = k0; k < ntask; k += kNW) {
                 const int li = k * rpw;
                 const uint8_t *b = base + (size_t)li * ib;
@@ -1395,7 +1444,7 @@ __device__ __noinline__ RunState run_tmpl(int N, int ti, float inv, int warp, in
             if (lane == 0) mbar_arrive(bar_empty(q % kNB));
         }
     }
-    return RunState{rp.head, rp.q, tasks, 1u};
+    return RunState{rp.head, rp.off, rp.q, tasks, 1u};
 }
 
 // Phase B in one pass per output row: the S pieces (one per slot) are waited
@@ -1413,15 +1462,17 @@ __device__ __noinline__ RunState run_down(int N, int warp, int lane, RunState st
     uint32_t *poff = SM<uint32_t>(cx.sm_poff) + warp * kMaxSlots;
     RingPos rp;
     rp.head = st.head;
+    rp.off = st.off;
     rp.q = st.q;
     const int no = t.o_hi - t.o_lo;
     const uint32_t q0 = rp.q;
 #pragma unroll 1
     for (int sl = 0; sl < cx.S; sl++) {
-        const uint64_t start = rp.place((uint32_t)(no > 0 ? no : 1) * cx.rec_F, cx.ring_bytes);
+        uint32_t at;
+        rp.place((uint32_t)(no > 0 ? no : 1) * cx.rec_F, cx.ring_bytes, &at);
         const uint32_t q = rp.q++;
-        if (lane == 0) poff[sl] = (uint32_t)(start % cx.ring_bytes);
-        if (!wait_bar_warp_inl(bar_full(q % kNB), (q / kNB) & 1)) return RunState{rp.head, rp.q, st.tasks, 0u};
+        if (lane == 0) poff[sl] = at;
+        if (!wait_bar_warp_inl(bar_full(q % kNB), (q / kNB) & 1)) return RunState{rp.head, rp.off, rp.q, st.tasks, 0u};
     }
     __syncwarp();
     const int cps = cx.F / VALS, npair = cx.S * cps, cb = cx.F * BITS / 8;
@@ -1480,7 +1531,7 @@ __device__ __noinline__ RunState run_down(int N, int warp, int lane, RunState st
     if (vp) SM<float>(cx.sm_vnw)[warp * 2 * kMaxR + lane] += vn;
     __syncwarp();
     if (lane < cx.S) mbar_arrive(bar_empty((q0 + lane) % kNB));
-    return RunState{rp.head, rp.q, st.tasks, 1u};
+    return RunState{rp.head, rp.off, rp.q, st.tasks, 1u};
 }
 
 template <int BITS>
@@ -1499,12 +1550,19 @@ struct Consumer {
         return ok;
     }
 
-    // Waits until every CTA's flag at `off` has reached `tg`: warp 0 polls the
-    // flags, the other warps sleep on the mbarrier `b`.
-    __device__ __forceinline__ bool flag_wait(uint32_t off, uint32_t tg, uint64_t *b, uint32_t &uses) {
+    // Waits until every CTA's flag at `off` has reached `tg` (warp 0 polls the
+    // flags), then warp 0 lane 0 copies the exchanged words into the stage
+    // with bulk copies completing on mbarrier `b` (issue(b) arms its byte
+    // count and starts them); every warp sleeps on `b` until they land.
+    template <typename Issue>
+    __device__ __forceinline__ bool flag_copy(uint32_t off, uint32_t tg, uint64_t *b, uint32_t &uses,
+                                              Issue issue) {
         if (warp == 0) {
             if (!poll_flags(off, tg, lane, 0)) return false;
-            if (lane == 0) mbar_arrive(b);
+            if (lane == 0) {
+                fence_proxy_async();
+                issue(b);
+            }
         }
         const bool ok = wait_bar_warp(b, uses & 1);
         uses++;
@@ -1519,8 +1577,9 @@ struct Consumer {
     }
 
     __device__ __forceinline__ bool run(int N, int ti, float inv) {
-        const RunState st = run_tmpl<BITS>(N, ti, inv, warp, lane, RunState{rp.head, rp.q, tasks, 1u});
+        const RunState st = run_tmpl<BITS>(N, ti, inv, warp, lane, RunState{rp.head, rp.off, rp.q, tasks, 1u});
         rp.head = st.head;
+        rp.off = st.off;
         rp.q = st.q;
         tasks = st.tasks;
         return st.ok != 0;
@@ -1531,7 +1590,13 @@ struct Consumer {
         if (warp == 0 && lane == 0) stamp_at(c, N, ST_L0);
         const bool r0 = N == 0 && cx.own0;
         const bool vp = gu_lora_here(N);
-        if (N > 0 && !flag_wait(cx.off_xflag, tag_of(N - 1), bar(B_X), xuses)) return false;
+        // every CTA's rows of the previous layer's out: one bulk copy
+        if (N > 0 && !flag_copy(cx.off_xflag, tag_of(N - 1), bar(B_X), xuses, [&](uint64_t *b) {
+                const uint32_t bytes = (uint32_t)cx.d * 8;
+                mbar_arrive_expect_tx(b, bytes);
+                bulk_g2s(SM<uint8_t>(cx.sm_stage), cx.ws + cx.off_out, bytes, b);
+            }))
+            return false;
         if (!phase_x<BITS>(N, true, vp && !r0, warp, lane)) return false;
         if (!sync()) return false;
         const float inv = misc_f()[M_INV];
@@ -1551,13 +1616,34 @@ struct Consumer {
         if (!run(N, tmpl_A_index(N), inv)) return false;
         publish_a(N, c, lane);
         if (warp == 0 && lane == 0) stamp_at(c, N, ST_A);
-        if (!flag_wait(cx.off_hflag, tag_of(N), bar(B_H), huses)) return false;
+        // every CTA's h rows, then each down-LoRA slot's owner partials
+        if (!flag_copy(cx.off_hflag, tag_of(N), bar(B_H), huses, [&](uint64_t *b) {
+                const Tmplt &ta = tmpls()[tmpl_A_index(N)];
+                uint32_t bytes = (uint32_t)cx.S * cx.F * 8;
+#pragma unroll 1
+                for (int sl = 0; sl < cx.S; sl++)
+                    if (cx.dl_mask >> sl & 1u) bytes += (uint32_t)(ta.own1[sl] - ta.own0[sl] + 1) * kMaxR * 8;
+                mbar_arrive_expect_tx(b, bytes);
+                uint8_t *stage = SM<uint8_t>(cx.sm_stage);
+                bulk_g2s(stage, cx.ws + cx.off_h, (uint32_t)cx.S * cx.F * 8, b);
+                uint32_t at = (uint32_t)cx.S * cx.F * 8;
+#pragma unroll 1
+                for (int sl = 0; sl < cx.S; sl++) {
+                    if (!(cx.dl_mask >> sl & 1u)) continue;
+                    const uint32_t nb = (uint32_t)(ta.own1[sl] - ta.own0[sl] + 1) * kMaxR * 8;
+                    bulk_g2s(stage + at,
+                             cx.ws + cx.off_vdp + ((size_t)sl * cx.n_cta + ta.own0[sl]) * kMaxR * 8, nb, b);
+                    at += nb;
+                }
+            }))
+            return false;
         if (!phase_h<BITS>(N, warp, lane)) return false;
         if (!sync()) return false;               // h and vd visible to all warps
         if (warp == 0 && lane == 0) stamp_at(c, N, ST_H);
         {                                        // down rows + combine
-            const RunState rs = run_down<BITS>(N, warp, lane, RunState{rp.head, rp.q, tasks, 1u});
+            const RunState rs = run_down<BITS>(N, warp, lane, RunState{rp.head, rp.off, rp.q, tasks, 1u});
             rp.head = rs.head;
+            rp.off = rs.off;
             rp.q = rs.q;
             if (!rs.ok) return false;
         }
@@ -1578,6 +1664,7 @@ struct Consumer {
                                                       1u, 0u, 0xFFFFFFFFu, 0xFFFFFFFFu, v)))
                 return;
         }
+        #pragma unroll 1
         for (int N = 0; N < cx.depth; N++)
             if (!layer(N)) return;
     }
@@ -1604,6 +1691,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
     {
         const uint32_t *src = reinterpret_cast<const uint32_t *>(&p.cx);
         uint32_t *dst = reinterpret_cast<uint32_t *>(g_smem);
+        #pragma unroll 1
         for (int i = threadIdx.x; i < (int)(sizeof(Ctx) / 4); i += blockDim.x) dst[i] = src[i];
     }
     __syncthreads();
@@ -1614,16 +1702,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
 
     // routes of this step (layer 0's own route is filled in later)
     const int use = p.cx.t % 3, prv = (p.cx.t + 2) % 3;
+#pragma unroll 1
     for (int i = threadIdx.x; i < p.cx.depth * p.cx.K; i += blockDim.x) {
         SM<int>(p.cx.sm_rcur)[i] = p.cx.ridx[(size_t)use * p.cx.depth * p.cx.K + i];
         SM<float>(p.cx.sm_rw)[i] = p.cx.rw[(size_t)use * p.cx.depth * p.cx.K + i];
         SM<int>(p.cx.sm_rprev)[i] = p.cx.ridx[(size_t)prv * p.cx.depth * p.cx.K + i];
     }
+#pragma unroll 1
     for (int i = threadIdx.x; i < kNW * p.cx.n_dl * kMaxR; i += blockDim.x)
         SM<float>(p.cx.sm_vdacc)[i] = 0.0f;
+#pragma unroll 1
     for (int i = threadIdx.x; i < kNW * 2 * kMaxR; i += blockDim.x) SM<float>(p.cx.sm_vnw)[i] = 0.0f;
     if (threadIdx.x == 0) {
         uint64_t *bars = SM<uint64_t>(p.cx.sm_bar);
+        #pragma unroll 1
         for (int i = 0; i < kNB; i++) {
             mbar_init(bars + i, 1);
             mbar_init(bars + kNB + i, kNW);
@@ -1634,11 +1726,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_step_kernel(const __grid_c
         mbar_init(b + B_END, kCons0 + kNW);
         mbar_init(b + B_X, 1);
         mbar_init(b + B_H, 1);
+        mbar_init(b + B_AUX, 1);
+        #pragma unroll 1
         for (int k = 0; k < 2; k++) {
             mbar_init(b + B_PREP_FULL0 + k, 1);
             mbar_init(b + B_PREP_EMPTY0 + k, kNW);
         }
         int *mi = SM<int>(p.cx.sm_misc);
+        #pragma unroll 1
         for (int i = M_CNT_A; i <= M_CNT_D; i++) mi[i] = 0;
         mbar_fence_init();
         mi[M_TMPL_OK] = build_templates(c, SM<Tmplt>(p.cx.sm_tmpl)) ? 1 : 0;
@@ -1942,6 +2037,10 @@ static int launch_decode_step(const moe_stack_desc *sd, const float *x0, float *
         const long long share = (total_a + sms - 1) / sms;
         cx.max_pairs = (int)(share / (2 * cx.rec_d)) + cx.S + 1;
         cx.max_hrows = (int)(share / cx.rec_dh) + 3;
+        // CTAs whose share holds some of one slot's gate/up rows: at most the
+        // slot's part of the phase without head rows (the smaller total)
+        cx.max_owners = sms / cx.S + 3;
+        if (cx.max_owners > sms) cx.max_owners = sms;
     }
     cx.max_orows = (cx.d + sms - 1) / sms;
     cx.max_erows = (cx.E + sms - 1) / sms;
@@ -2005,9 +2104,12 @@ static int launch_decode_step(const moe_stack_desc *sd, const float *x0, float *
     cx.sm_rprev = take((size_t)cx.depth * cx.K * 4);
     cx.sm_rw = take((size_t)cx.depth * cx.K * 4);
     cx.sm_misc = take((size_t)M_COUNT * 4);
-    cx.sm_hraw = take((size_t)cx.S * cx.F * 4);
-    cx.sm_graw = take((size_t)(cx.H ? cx.H : 32) * 4);
-    cx.sm_vdpl = take((size_t)2 * std::max(cx.n_dl, 1) * sms * 4);
+    // the stage: tagged words of one exchange (x; or h and the down-LoRA
+    // owner partials), 8 bytes each
+    cx.sm_stage = take((size_t)std::max((long long)cx.d, (long long)cx.S * cx.F +
+                                                           (long long)cx.n_dl * cx.max_owners * kMaxR) *
+                       8);
+    cx.sm_graw = take((size_t)(cx.H ? cx.H : 32) * 8);
     cx.sm_poff = take((size_t)kNW * kMaxSlots * 4);
     cx.sm_ring = (uint32_t)al(off, 1024);
     long long room = (long long)smem_max - (long long)cx.sm_ring;

@@ -66,6 +66,12 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
+// Orders this thread's generic-proxy view of global memory (e.g. what an
+// acquire just made visible) before its later async-proxy (bulk copy) reads.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
