@@ -23,7 +23,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 
 LIBS = {
-    "libmoe.so": ["abi.cu", "pack.cu", "ffn.cu", "head_route.cu", "noalloc.cu", "step.cu"],
+    "libmoe.so": ["abi.cu", "pack.cu", "ffn.cu", "grouped.cu", "head_route.cu", "noalloc.cu",
+                  "step.cu"],
     "libmoe_synth.so": ["synth.cu"],
 }
 

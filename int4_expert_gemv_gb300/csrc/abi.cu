@@ -41,17 +41,19 @@ static bool shape_ok(int d, int F, int bits) {
     return d > 0 && F > 0 && d % kGroup == 0 && F % kGroup == 0 && (bits == 2 || bits == 4);
 }
 
-// Workspace carving for the expert FFN.
+// Workspace carving for the expert FFN.  The LoRA partials, the histogram,
+// the offsets and the permutation are common; the per-token path's h and the
+// grouped path's {sum x, h (bf16), sum h, A_d h} share one region, since a
+// call takes one path or the other.
 struct FfnWs {
-    size_t h, v, counts, offsets, perm, total;
+    size_t h, v, counts, offsets, perm, xsum, h16, hsum, vd, total;
 };
 
 static FfnWs ffn_ws(const moe_experts_desc *ed, int T, int K) {
     FfnWs w;
     const size_t slots = (size_t)K + (ed->shared ? 1 : 0);
+    const size_t npos = (size_t)T * K + (ed->shared ? T : 0);
     size_t off = 0;
-    w.h = off;
-    off = align_up(off + (size_t)T * slots * ed->F * sizeof(float), 256);
     w.v = off;
     off = align_up(off + (size_t)T * slots * 3 * kMaxLoraRank * sizeof(float), 256);
     w.counts = off;
@@ -60,7 +62,19 @@ static FfnWs ffn_ws(const moe_experts_desc *ed, int T, int K) {
     off = align_up(off + (size_t)(ed->E + 2) * sizeof(int32_t), 256);
     w.perm = off;
     off = align_up(off + (size_t)T * K * sizeof(int32_t), 256);
-    w.total = off;
+    const size_t region = off;
+    w.h = region;
+    const size_t end_tok = align_up(region + (size_t)T * slots * ed->F * sizeof(float), 256);
+    size_t g = region;
+    w.xsum = g;
+    g = align_up(g + (size_t)T * (ed->d / kGroup) * sizeof(float), 256);
+    w.h16 = g;
+    g = align_up(g + npos * ed->F * sizeof(uint16_t), 256);
+    w.hsum = g;
+    g = align_up(g + npos * (ed->F / kGroup) * sizeof(float), 256);
+    w.vd = g;
+    g = align_up(g + npos * kMaxLoraRank * sizeof(float), 256);
+    w.total = end_tok > g ? end_tok : g;
     return w;
 }
 
@@ -302,6 +316,11 @@ int moe_expert_ffn_int4(const moe_experts_desc *ed, const void *x, int x_dtype,
     p.counts = reinterpret_cast<int32_t *>(w + wl.counts);
     p.offsets = reinterpret_cast<int32_t *>(w + wl.offsets);
     p.perm = reinterpret_cast<int32_t *>(w + wl.perm);
+    p.xb = static_cast<const __nv_bfloat16 *>(x);
+    p.xsum = reinterpret_cast<float *>(w + wl.xsum);
+    p.h16 = reinterpret_cast<__nv_bfloat16 *>(w + wl.h16);
+    p.hsum = reinterpret_cast<float *>(w + wl.hsum);
+    p.vd = reinterpret_cast<float *>(w + wl.vd);
     p.y = y_slots;
     for (int i = 0; i < 3; i++) {
         p.lora[i] = lora_dev(ed->lora[i]);
@@ -310,6 +329,9 @@ int moe_expert_ffn_int4(const moe_experts_desc *ed, const void *x, int x_dtype,
     p.any_gu_lora = ed->lora[0].r || ed->lora[1].r ||
                     (ed->shared && (ed->shared_lora[0].r || ed->shared_lora[1].r));
     p.L = blob_layout(ed->d, ed->F, ed->bits);
+    // Several tokens in bf16 (prefill, batched decode): sorted by expert and
+    // run as grouped GEMMs.  One token, or fp32 activations: per-token GEMVs.
+    if (T > 1 && x_dtype == MOE_DTYPE_BF16) return launch_expert_ffn_grouped(p, stream);
     return launch_expert_ffn(p, stream);
 }
 

@@ -238,6 +238,10 @@ static int launch_bits(const FfnParams &p, cudaStream_t st) {
     return MOE_OK;
 }
 
+void lora_ax_kernel_launch(const FfnParams &p, cudaStream_t st) {
+    lora_ax_kernel<<<dim3(p.slots, p.T), 256, p.d * sizeof(float), st>>>(p);
+}
+
 int launch_expert_ffn(const FfnParams &p, cudaStream_t st) {
     return p.bits == 4 ? launch_bits<4>(p, st) : launch_bits<2>(p, st);
 }

@@ -6,6 +6,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -34,10 +36,15 @@ struct FfnParams {
     LoraDev shared_lora[3];
     BlobLayout L;
     int any_gu_lora;             // some slot carries a gate or up adapter
-    // grouped (T > 1) path
-    int32_t *counts;             // workspace [E+1]
+    // grouped (T > 1, bf16) path
+    int32_t *counts;             // workspace [E+1]: entries per expert, then invalid ones
     int32_t *offsets;            // workspace [E+2]
-    int32_t *perm;               // workspace [T*K] (token*K + k), by expert
+    int32_t *perm;               // workspace [T*K] (token*K + k), by expert, in token order
+    const __nv_bfloat16 *xb;     // = x, [T][d]
+    float *xsum;                 // workspace [T][d/64]: sum of x per group
+    __nv_bfloat16 *h16;          // workspace [T*K + T][F]: h at sorted positions (shared: T*K + t)
+    float *hsum;                 // workspace [T*K + T][F/64]
+    float *vd;                   // workspace [T*K + T][kMaxLoraRank]: A_d h
 };
 
 struct HeadParams {
@@ -57,6 +64,8 @@ struct HeadParams {
 };
 
 int launch_expert_ffn(const FfnParams &p, cudaStream_t st);
+int launch_expert_ffn_grouped(const FfnParams &p, cudaStream_t st);
+void lora_ax_kernel_launch(const FfnParams &p, cudaStream_t st);
 int launch_prerouter_head(const HeadParams &p, cudaStream_t st);
 int launch_topk(const float *logits, int T, int E, int K, int32_t *idx, float *w,
                 float *margin, cudaStream_t st);

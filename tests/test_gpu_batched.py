@@ -1,0 +1,157 @@
+"""Batched / prefill expert FFN (T > 1 tokens, bf16 activations): the grouped
+path (counting sort by expert, grouped tensor-core GEMMs) against the oracle.
+
+Calls go through the C ABI; routes come from the seeded generator; expected
+values from the oracle only, with h rounded to bf16 on both sides (where
+the oracle's h sits within 1e-5 of a rounding midpoint either neighbour is
+accepted, and the bar widens by what that choice can move).  Up to
+T = 64 every token is compared; at T = 512 and 4096 a seeded sample of tokens
+(all their slots) is, since each (token, slot) output depends only on that
+token's row of x and its expert.  Bar: max|err| <= 2e-3 * rms(ref) per slot."""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from int4_expert_gemv_gb300 import synth
+from int4_expert_gemv_gb300.configs import ALL, TINY
+from _util import assert_close_bf16h, host_expert_from_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def m():
+    from int4_expert_gemv_gb300 import build
+    build.build()
+    from int4_expert_gemv_gb300 import moe
+    moe.lib()
+    synth._gpu()
+    return moe
+
+
+_MODELS = {}
+
+
+def _model(cfg):
+    from int4_expert_gemv_gb300.model import DeviceModel
+    key = (cfg.d, cfg.F, cfg.E, cfg.bits, cfg.shared, cfg.seed, cfg.lora_on, cfg.lora_r)
+    if key not in _MODELS:
+        _MODELS.clear()
+        torch.cuda.empty_cache()
+        _MODELS[key] = DeviceModel(replace(cfg, L=1, depth=1), heads=False)
+    return _MODELS[key]
+
+
+def _run(m, cfg, routes, x):
+    T, K = routes.shape
+    ed = _model(cfg).layers[0]["experts_desc"]
+    y = torch.full((T, K + cfg.shared, cfg.d), 7.0, device="cuda")
+    ws = torch.empty(m.moe_expert_ffn_workspace_bytes(ed, T, K), dtype=torch.uint8, device="cuda")
+    m.moe_expert_ffn_int4(ed, x, torch.from_numpy(routes).cuda(), T, K, y, ws)
+    torch.cuda.synchronize()
+    return y.cpu().double().numpy()
+
+
+def _x(cfg, T, tag=901):
+    return torch.from_numpy(synth.gauss(cfg.seed, tag, (T, cfg.d), 1.0)).cuda().to(torch.bfloat16)
+
+
+def _check(cfg, got, x, routes, tokens, what):
+    valid = (routes >= 0) & (routes < cfg.E)
+    safe = np.where(valid, routes, 0).astype(np.int32)
+    needed = sorted(set(safe[tokens].ravel().tolist()))
+    host = {e: host_expert_from_gpu(cfg, 0, e) for e in needed}
+    zero = next(iter(host.values()))
+    exps = [host.get(e, zero) for e in range(cfg.E)]
+    sh = host_expert_from_gpu(cfg, 0, synth.SHARED_EXPERT) if cfg.shared else None
+    xr = x.float().cpu().double().numpy()[tokens]
+    ref = orc.expert_ffn(exps, sh, xr, safe[tokens], round_h_bf16=True)
+    for i, t in enumerate(tokens):
+        for s in range(ref.shape[1]):
+            if s < cfg.K and not valid[t, s]:
+                assert np.isnan(got[t, s]).all(), f"{what}: token {t} slot {s} not NaN"
+                continue
+            ex = exps[safe[t, s]] if s < cfg.K else sh
+            assert_close_bf16h(got[t, s], ref[i, s], ex, xr[i], f"{what} token {t} slot {s}")
+
+
+@pytest.mark.parametrize("T,sample", [(8, 0), (64, 0), (512, 48), (4096, 24)])
+def test_batched_parity(m, T, sample):
+    cfg = ALL[f"batched-T{T}"]
+    routes = synth.routes(cfg.seed, 902, T, cfg.E, cfg.K)
+    x = _x(cfg, T)
+    got = _run(m, cfg, routes, x)
+    assert np.isfinite(got).all()
+    tokens = np.arange(T) if not sample else np.sort(
+        np.random.default_rng(T).choice(T, sample, replace=False))
+    _check(cfg, got, x, routes, tokens, f"batched T={T}")
+
+
+def test_batched_is_deterministic(m):
+    cfg = ALL["batched-T512"]
+    routes = synth.routes(cfg.seed, 903, 512, cfg.E, cfg.K)
+    x = _x(cfg, 512)
+    a = _run(m, cfg, routes, x)
+    b = _run(m, cfg, routes, x)
+    assert np.array_equal(a.view(np.int64), b.view(np.int64))
+
+
+def test_batched_ragged_tiny_with_invalid_and_repeated(m):
+    """T not a multiple of the 64-token tile, F below the 256-column chunk,
+    LoRA on the routed down projection, expert indices outside [0, E) (NaN
+    slots) and an expert repeated within a token."""
+    cfg = TINY
+    T = 100
+    routes = synth.routes(cfg.seed, 904, T, cfg.E, cfg.K)
+    routes[3] = [5, 5]
+    routes[10, 1] = -1
+    routes[57, 0] = cfg.E
+    routes[99] = [cfg.E + 7, 2]
+    x = _x(cfg, T)
+    got = _run(m, cfg, routes, x)
+    _check(cfg, got, x, routes, np.arange(T), "tiny ragged")
+    assert np.array_equal(got[3, 0], got[3, 1])
+
+
+def test_batched_one_expert_beyond_the_tile_grid(m):
+    """Every slot of every token on one expert: the expert has T*K entries,
+    more than the grid's ceil(T/64) tiles cover in one pass."""
+    cfg = TINY
+    T = 70
+    routes = np.full((T, cfg.K), 9, np.int32)
+    x = _x(cfg, T, 905)
+    got = _run(m, cfg, routes, x)
+    _check(cfg, got, x, routes, np.arange(0, T, 3), "one expert")
+    assert np.array_equal(got[:, 0], got[:, 1])
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_batched_wide(m, bits):
+    cfg = replace(ALL[f"wide-int{bits}"], T=64)
+    routes = synth.routes(cfg.seed, 906, 64, cfg.E, cfg.K)
+    for t in range(8):                   # one expert with 8 tokens, indices still distinct
+        row = [77] + [e for e in routes[t] if e != 77]
+        routes[t] = row[:cfg.K]
+    x = _x(cfg, 64)
+    got = _run(m, cfg, routes, x)
+    _check(cfg, got, x, routes, np.arange(0, 64, 4), f"wide int{bits}")
+
+
+def test_batched_matches_per_token_bf16_path(m):
+    """The grouped path and the per-token GEMV path (one call per token) take
+    the same arithmetic definition: both agree within the bar."""
+    cfg = ALL["batched-T64"]
+    routes = synth.routes(cfg.seed, 907, 64, cfg.E, cfg.K)
+    x = _x(cfg, 64)
+    got = _run(m, cfg, routes, x)
+    sh = host_expert_from_gpu(cfg, 0, synth.SHARED_EXPERT)
+    for t in (0, 17, 63):
+        one = _run(m, cfg, routes[t:t + 1], x[t:t + 1].contiguous())
+        xr = x[t].float().cpu().double().numpy()
+        for s in range(cfg.slots):
+            ex = host_expert_from_gpu(cfg, 0, int(routes[t, s])) if s < cfg.K else sh
+            assert_close_bf16h(got[t, s], one[0, s], ex, xr,
+                               f"grouped vs per-token token {t} slot {s}")

@@ -14,7 +14,7 @@ import torch
 import oracle as orc
 from int4_expert_gemv_gb300 import synth
 from int4_expert_gemv_gb300.configs import ALL, MOE35B, TINY
-from _util import TIE, assert_close, host_expert_from_gpu
+from _util import TIE, assert_close, assert_close_bf16h, host_expert_from_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -79,7 +79,7 @@ def _layer_model(cfg):
     return DeviceModel(replace(cfg, L=1, depth=1), heads=False)
 
 
-def _ffn_case(m, cfg, dm, routes, x_dtype=torch.float32):
+def _ffn_case(m, cfg, dm, routes, x_dtype=torch.float32, full=False):
     T, K = routes.shape
     ly = dm.layers[0]
     ed = ly["experts_desc"]
@@ -95,6 +95,8 @@ def _ffn_case(m, cfg, dm, routes, x_dtype=torch.float32):
     sh = host_expert_from_gpu(cfg, 0, synth.SHARED_EXPERT) if cfg.shared else None
     xr = x.float().cpu().double().numpy()
     ref = orc.expert_ffn(exps, sh, xr, routes, round_h_bf16=x_dtype == torch.bfloat16)
+    if full:
+        return _f64(y), ref, exps, sh, xr
     return _f64(y), ref
 
 
@@ -134,10 +136,11 @@ def test_expert_ffn_bf16_activations(m):
     cfg = replace(MOE35B, T=8)
     dm = _layer_model(cfg)
     routes = synth.routes(4, 1, 8, cfg.E, cfg.K)
-    got, ref = _ffn_case(m, cfg, dm, routes, x_dtype=torch.bfloat16)
+    got, ref, exps, sh, xr = _ffn_case(m, cfg, dm, routes, x_dtype=torch.bfloat16, full=True)
     for t in range(8):
         for s in range(cfg.slots):
-            assert_close(got[t, s], ref[t, s], f"bf16 token {t} slot {s}")
+            ex = exps[routes[t, s]] if s < cfg.K else sh
+            assert_close_bf16h(got[t, s], ref[t, s], ex, xr[t], f"bf16 token {t} slot {s}")
 
 
 # ------------------------------------------------------------ head
