@@ -10,6 +10,7 @@ layer and its top-K router (layer 0 routes with its own router).  Steady-state
 steps are replayed from captured CUDA graphs.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 35b]
+    python bench.py --config batched-T4096 ...   # one layer over T tokens
     python bench.py --impl reference ...   # the CPU oracle, same metric
 
 Prints one JSON line (rank 0).  N > 1 runs N independent replicas (the layer
@@ -351,6 +352,149 @@ def run_native(args, cfg):
         dist.destroy_process_group()
 
 
+def grouped_kernels_per_call(cfg) -> int:
+    """Kernels one batched expert-FFN call launches: sort (count, scatter),
+    NaN fill, sums of x, [LoRA A x], gate/up GEMM, sums of h, [LoRA A_d h],
+    down GEMM."""
+    gu = cfg.lora_r and cfg.lora_on == "shared_all"
+    dn = bool(cfg.lora_r)
+    return 7 + (1 if gu else 0) + (1 if dn else 0)
+
+
+def run_batched(args, cfg):
+    """One step = one MoE layer over T tokens (bf16 input): the prerouter
+    head and top-K over T rows, the expert FFN grouped by expert, and the
+    combine + residual.  Replayed from a captured CUDA graph; L2 is flushed
+    before every timed step (a small T touches fewer expert bytes than L2
+    holds), each step timed by its own events."""
+    import torch
+
+    from int4_expert_gemv_gb300 import synth
+    from int4_expert_gemv_gb300.model import BatchedLayer, DeviceModel
+    import __graft_entry__
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    T = cfg.T
+    dm = DeviceModel(cfg)
+    bl = BatchedLayer(dm, T)
+    x0 = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0), (T, cfg.d), 1.0))
+    bl.x.copy_(x0.cuda().to(torch.bfloat16))
+    bl.res.copy_(x0.cuda())
+    bl.route_own()
+    torch.cuda.synchronize()
+    cur = bl.cur_idx.cpu().numpy()
+    distinct = len(set(cur.ravel().tolist()))
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bl.enqueue()
+    ev = (torch.cuda.Event(enable_timing=True, external=True),
+          torch.cuda.Event(enable_timing=True, external=True))
+    gi = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gi):
+        bl.enqueue(ffn_events=ev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for a, b in pairs:
+            flush.fill_(1)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in pairs)
+    ms_step = ms / args.steps
+    tok_s = world * T * args.steps / (ms / 1000.0)
+
+    # the FFN call alone (events inside an instrumented graph), L2 flushed
+    ffn_ms = []
+    for _ in range(min(args.steps, 32)):
+        flush.fill_(1)
+        gi.replay()
+        torch.cuda.synchronize()
+        ffn_ms.append(ev[0].elapsed_time(ev[1]))
+    ffn_avg = statistics.mean(ffn_ms)
+
+    # end to end: x (bf16) and the residual from pinned host memory, the
+    # step, the layer output back to pinned host memory
+    pin_x = bl.x.cpu().pin_memory()
+    pin_r = bl.res.cpu().pin_memory()
+    pin_o = torch.empty((T, cfg.d), dtype=torch.float32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        bl.x.copy_(pin_x, non_blocking=True)
+        bl.res.copy_(pin_r, non_blocking=True)
+        g.replay()
+        pin_o.copy_(bl.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+
+    if rank == 0:
+        hbm, hbm_kind = peaks()
+        pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+        pk = json.load(open(pk_path)) if os.path.exists(pk_path) else {}
+        tensor_peak = float(pk.get("bf16_tflops", 1900.0))
+        tensor_kind = "measured" if "bf16_tflops" in pk else "fallback"
+        ffn_bytes = (distinct + (1 if cfg.shared else 0)) * cfg.expert_bytes()
+        ffn_flops = 2.0 * T * cfg.slots * 3 * cfg.d * cfg.F
+        t_hbm = ffn_bytes / (hbm * 1e9)
+        t_tc = ffn_flops / (tensor_peak * 1e12)
+        tensor_bound = t_tc > t_hbm
+        if tensor_bound:
+            achieved, peak, unit = ffn_flops / (ffn_avg / 1000.0) / 1e12, tensor_peak, "TFLOP/s"
+        else:
+            achieved, peak, unit = ffn_bytes / (ffn_avg / 1000.0) / 1e9, hbm, "GB/s"
+        head_k = 1 + (1 if cfg.H else 0)
+        line = {
+            "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": cfg.name, "batch": T, "layers": 1, "d_model": cfg.d,
+                "experts": cfg.E, "top_k": cfg.K, "expert_ffn": cfg.F,
+                "shared_expert": cfg.shared, "weight_bits": cfg.bits, "group": cfg.group,
+                "head_hidden": cfg.H,
+                "lora": f"r{cfg.lora_r} alpha{cfg.lora_alpha:g} {cfg.lora_on}" if cfg.lora_r else "none",
+                "distinct_experts": distinct,
+                "l2": "flushed (2x L2 written) before every timed step",
+                "graphs": "each step replayed from a captured CUDA graph",
+            },
+            "expert_weight_gbs": ffn_bytes / (ms_step / 1000.0) / 1e9,
+            "ffn_tflops": ffn_flops / (ffn_avg / 1000.0) / 1e12,
+            "roofline": {"bound": "tensor" if tensor_bound else "hbm",
+                         "kernel": "moe_expert_ffn_int4, grouped (sort, gate/up GEMM, down GEMM)",
+                         "achieved": achieved, "peak": peak,
+                         "peak_kind": tensor_kind if tensor_bound else hbm_kind,
+                         "unit": unit, "frac": achieved / peak, "traffic": None,
+                         "bytes_per_launch": ffn_bytes, "flops_per_launch": ffn_flops,
+                         "avg_launch_us": ffn_avg * 1000.0,
+                         "timing": "CUDA events around the FFN call in an instrumented graph, "
+                                   "L2 flushed before each"},
+            "e2e": {"value": world * T * args.steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+                    "h2d_bytes_per_step": T * cfg.d * (2 + 4),
+                    "d2h_bytes_per_step": T * cfg.d * 4},
+            "gpu_launches": (head_k + 1 + grouped_kernels_per_call(cfg) + 1) * args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(cfg, min(args.cpu_layers, 16))
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from int4_expert_gemv_gb300.configs import ALL
@@ -359,6 +503,8 @@ def main():
         import oracle
         oracle.build()
         run_reference(args, cfg)
+    elif cfg.T > 1:
+        run_batched(args, cfg)
     else:
         run_native(args, cfg)
 

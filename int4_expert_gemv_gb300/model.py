@@ -297,3 +297,67 @@ class DecodeStack:
         after step t, before step t+2 overwrites the rotation)."""
         u = t % 3
         return self.r_idx[u].clone(), self.r_w[u].clone(), self.r_margin[u].clone()
+
+
+class BatchedLayer:
+    """One MoE layer over T tokens at once (prefill, batched decode).
+
+    Inputs: x (bf16 [T][d], the layer's normalised input), the residual
+    stream (fp32 [T][d]), this layer's routes (cur_idx, cur_w: predicted by
+    the previous layer's head) and the previous token's routes (prev_idx).
+    One step enqueues, for all T tokens: the prerouter head and top-K that
+    predict the next layer's routes, the expert FFN on the current routes
+    (grouped by expert inside the call), and the combine + residual with the
+    next layer's fp32 input."""
+
+    def __init__(self, model: DeviceModel, T: int, layer: int = 0):
+        self.m = model
+        c = self.cfg = model.cfg
+        dev = model.device
+        self.T = T
+        self.ly = model.layers[layer]
+        f32 = dict(dtype=torch.float32, device=dev)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.x = torch.zeros((T, c.d), dtype=torch.bfloat16, device=dev)
+        self.res = torch.zeros((T, c.d), **f32)
+        self.out = torch.zeros((T, c.d), **f32)
+        self.x_next = torch.zeros((T, c.d), **f32)
+        self.cur_idx = torch.zeros((T, c.K), **i32)
+        self.cur_w = torch.zeros((T, c.K), **f32)
+        self.prev_idx = torch.zeros((T, c.K), **i32)
+        self.next_idx = torch.zeros((T, c.K), **i32)
+        self.next_w = torch.zeros((T, c.K), **f32)
+        self.next_margin = torch.zeros(T, **f32)
+        self.logits = torch.zeros((T, c.E), **f32)
+        self.y = torch.zeros((T, c.slots, c.d), **f32)
+        ed = self.ly["experts_desc"]
+        self.ffn_ws = torch.empty(moe.moe_expert_ffn_workspace_bytes(ed, T, c.K),
+                                  dtype=torch.uint8, device=dev)
+        self.head_ws = torch.empty(max(256, moe.moe_prerouter_head_workspace_bytes(
+            self.ly["head_desc"], T)), dtype=torch.uint8, device=dev)
+
+    def route_own(self):
+        """Routes for the current input from the layer's own router (for
+        inputs that have no predicted route yet); prev = the previous token's
+        route (token 0 takes its own)."""
+        c = self.cfg
+        moe.moe_prerouter_head(self.ly["router_desc"], self.x, None, None, c.K, self.T,
+                               self.logits, self.head_ws)
+        moe.moe_topk_route(self.logits, self.T, c.E, c.K, self.cur_idx, self.cur_w)
+        self.prev_idx[1:].copy_(self.cur_idx[:-1])
+        self.prev_idx[0].copy_(self.cur_idx[0])
+
+    def enqueue(self, ffn_events=None):
+        c, T = self.cfg, self.T
+        moe.moe_prerouter_head(self.ly["head_desc"], self.x, self.cur_idx, self.prev_idx, c.K,
+                               T, self.logits, self.head_ws)
+        moe.moe_topk_route(self.logits, T, c.E, c.K, self.next_idx, self.next_w,
+                           self.next_margin)
+        if ffn_events is not None:
+            ffn_events[0].record()
+        moe.moe_expert_ffn_int4(self.ly["experts_desc"], self.x, self.cur_idx, T, c.K, self.y,
+                                self.ffn_ws)
+        if ffn_events is not None:
+            ffn_events[1].record()
+        moe.moe_combine_residual(self.y, self.cur_w, T, c.K, c.shared, c.d, self.res, self.out,
+                                 self.x_next)

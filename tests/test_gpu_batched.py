@@ -17,7 +17,8 @@ import torch
 import oracle as orc
 from int4_expert_gemv_gb300 import synth
 from int4_expert_gemv_gb300.configs import ALL, TINY
-from _util import assert_close_bf16h, host_expert_from_gpu
+from _util import (TIE, TOL, assert_close, assert_close_bf16h, bf16_h_allowance,
+                   host_expert_from_gpu, rms)
 
 pytestmark = pytest.mark.gpu
 
@@ -155,3 +156,49 @@ def test_batched_matches_per_token_bf16_path(m):
             ex = host_expert_from_gpu(cfg, 0, int(routes[t, s])) if s < cfg.K else sh
             assert_close_bf16h(got[t, s], one[0, s], ex, xr,
                                f"grouped vs per-token token {t} slot {s}")
+
+
+def test_batched_layer_step(m):
+    """The whole batched layer (head + top-K over T rows, grouped expert FFN,
+    combine + residual) against the oracle, on sampled tokens: next-layer
+    routes as index sets where the oracle's margin exceeds the tie bar, their
+    weights, and the layer output (minus the residual)."""
+    from int4_expert_gemv_gb300.model import BatchedLayer, DeviceModel
+    _MODELS.clear()
+    cfg = ALL["batched-T64"]
+    T = cfg.T
+    bl = BatchedLayer(DeviceModel(cfg), T)
+    x0 = torch.from_numpy(synth.gauss(cfg.seed, 908, (T, cfg.d), 1.0)).cuda()
+    bl.x.copy_(x0.to(torch.bfloat16))
+    bl.res.copy_(x0)
+    bl.route_own()
+    bl.enqueue()
+    torch.cuda.synchronize()
+    cur, cw, prev = (a.cpu().numpy() for a in (bl.cur_idx, bl.cur_w, bl.prev_idx))
+    nidx, nw = bl.next_idx.cpu().numpy(), bl.next_w.cpu().double().numpy()
+    out = bl.out.cpu().double().numpy()
+    xb = bl.x.float().cpu().double().numpy()
+    res = x0.cpu().double().numpy()
+    head = synth.head_host(cfg, 0)
+    sh = host_expert_from_gpu(cfg, 0, synth.SHARED_EXPERT)
+    checked = 0
+    for t in range(0, T, 7):
+        z = orc.head_logits(head, xb[t], cur[t], prev[t], cfg.K)
+        idx, w, margin = orc.topk(z, cfg.K)
+        if margin > TIE:
+            checked += 1
+            assert set(idx.tolist()) == set(nidx[t].tolist()), t
+            gw = dict(zip(nidx[t].tolist(), nw[t]))
+            assert_close([gw[k] for k in idx.tolist()], w, f"next weights token {t}")
+        exps = {e: host_expert_from_gpu(cfg, 0, int(e)) for e in cur[t]}
+        lst = [exps.get(e, sh) for e in range(cfg.E)]
+        y = orc.expert_ffn(lst, sh, xb[t:t + 1], cur[t:t + 1], round_h_bf16=True)[0]
+        ref, _ = orc.combine(y, cw[t].astype(np.float64), True, res[t])
+        got_d, ref_d = out[t] - res[t], ref - res[t]
+        err = np.abs(got_d - ref_d)
+        bound = TOL * rms(ref_d)
+        if err.max() > bound:
+            allow = sum(float(cw[t, k]) * bf16_h_allowance(exps[cur[t, k]], xb[t])
+                        for k in range(cfg.K)) + bf16_h_allowance(sh, xb[t])
+            assert (err <= bound + allow).all(), f"layer output token {t}"
+    assert checked >= 6
