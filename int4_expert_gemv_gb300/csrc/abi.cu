@@ -42,18 +42,25 @@ static bool shape_ok(int d, int F, int bits) {
 }
 
 // Workspace carving for the expert FFN.  The LoRA partials, the histogram,
-// the offsets and the permutation are common; the per-token path's h and the
-// grouped path's {sum x, h (bf16), sum h, A_d h} share one region, since a
-// call takes one path or the other.
+// the offsets, the permutation and the work-item offsets are common; the
+// per-token path's h and the grouped path's {x in sorted order, its group
+// sums, h (bf16), sum h, A_d h} share one region, since a call takes one
+// path or the other.
 struct FfnWs {
-    size_t h, v, counts, offsets, perm, xsum, h16, hsum, vd, total;
+    size_t err, h, v, counts, offsets, perm, item_off, xg, xsum, h16, hsum, vd, total;
 };
+
+// Row stride (floats) of the per-group sums the batched kernels read through
+// tensor maps: padded to 16 bytes.
+static size_t gsum_ld(int cols) { return (size_t)((cols / kGroup + 3) / 4 * 4); }
 
 static FfnWs ffn_ws(const moe_experts_desc *ed, int T, int K) {
     FfnWs w;
     const size_t slots = (size_t)K + (ed->shared ? 1 : 0);
     const size_t npos = (size_t)T * K + (ed->shared ? T : 0);
     size_t off = 0;
+    w.err = off;
+    off = 256;
     w.v = off;
     off = align_up(off + (size_t)T * slots * 3 * kMaxLoraRank * sizeof(float), 256);
     w.counts = off;
@@ -62,16 +69,20 @@ static FfnWs ffn_ws(const moe_experts_desc *ed, int T, int K) {
     off = align_up(off + (size_t)(ed->E + 2) * sizeof(int32_t), 256);
     w.perm = off;
     off = align_up(off + (size_t)T * K * sizeof(int32_t), 256);
+    w.item_off = off;
+    off = align_up(off + 2 * (size_t)(ed->E + 2) * sizeof(int32_t), 256);
     const size_t region = off;
     w.h = region;
     const size_t end_tok = align_up(region + (size_t)T * slots * ed->F * sizeof(float), 256);
     size_t g = region;
+    w.xg = g;
+    g = align_up(g + npos * ed->d * sizeof(uint16_t), 256);
     w.xsum = g;
-    g = align_up(g + (size_t)T * (ed->d / kGroup) * sizeof(float), 256);
+    g = align_up(g + npos * gsum_ld(ed->d) * sizeof(float), 256);
     w.h16 = g;
     g = align_up(g + npos * ed->F * sizeof(uint16_t), 256);
     w.hsum = g;
-    g = align_up(g + npos * (ed->F / kGroup) * sizeof(float), 256);
+    g = align_up(g + npos * gsum_ld(ed->F) * sizeof(float), 256);
     w.vd = g;
     g = align_up(g + npos * kMaxLoraRank * sizeof(float), 256);
     w.total = end_tok > g ? end_tok : g;
@@ -218,8 +229,9 @@ int moe_debug_dequant(const void *blob, int d, int F, int bits, int which, float
 
 size_t moe_prerouter_head_workspace_bytes(const moe_head_desc *hd, int T) {
     if (hd == nullptr || T < 0) return 0;
-    return align_up((size_t)T * hd->H * sizeof(float), 256) +
-           align_up((size_t)T * hd->E * sizeof(float), 256);
+    return 256 + align_up((size_t)T * hd->H * sizeof(float), 256) +
+           align_up((size_t)T * hd->E * sizeof(float), 256) +
+           align_up((size_t)T * gsum_ld(hd->d) * sizeof(float), 256);
 }
 
 int moe_prerouter_head(const moe_head_desc *hd, const void *x, int x_dtype,
@@ -258,8 +270,11 @@ int moe_prerouter_head(const moe_head_desc *hd, const void *x, int x_dtype,
     p.cur = cur_idx;
     p.prev = prev_idx;
     uint8_t *w = static_cast<uint8_t *>(ws);
-    p.g = reinterpret_cast<float *>(w);
-    p.zl = reinterpret_cast<float *>(w + align_up((size_t)T * hd->H * sizeof(float), 256));
+    p.err = reinterpret_cast<int32_t *>(w);
+    p.g = reinterpret_cast<float *>(w + 256);
+    const size_t zl_off = 256 + align_up((size_t)T * hd->H * sizeof(float), 256);
+    p.zl = reinterpret_cast<float *>(w + zl_off);
+    p.xsum = reinterpret_cast<float *>(w + zl_off + align_up((size_t)T * hd->E * sizeof(float), 256));
     p.logits = logits;
     return launch_prerouter_head(p, stream);
 }
@@ -317,10 +332,13 @@ int moe_expert_ffn_int4(const moe_experts_desc *ed, const void *x, int x_dtype,
     p.offsets = reinterpret_cast<int32_t *>(w + wl.offsets);
     p.perm = reinterpret_cast<int32_t *>(w + wl.perm);
     p.xb = static_cast<const __nv_bfloat16 *>(x);
+    p.xg = reinterpret_cast<__nv_bfloat16 *>(w + wl.xg);
     p.xsum = reinterpret_cast<float *>(w + wl.xsum);
     p.h16 = reinterpret_cast<__nv_bfloat16 *>(w + wl.h16);
     p.hsum = reinterpret_cast<float *>(w + wl.hsum);
     p.vd = reinterpret_cast<float *>(w + wl.vd);
+    p.item_off = reinterpret_cast<int32_t *>(w + wl.item_off);
+    p.err = reinterpret_cast<int32_t *>(w + wl.err);
     p.y = y_slots;
     for (int i = 0; i < 3; i++) {
         p.lora[i] = lora_dev(ed->lora[i]);

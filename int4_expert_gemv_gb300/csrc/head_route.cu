@@ -11,6 +11,7 @@
 // fused expert-combine kernel of "Arquitectura del Sistema" (kerneldigest.dev).
 #include <cfloat>
 
+#include "gemm_pipe.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -148,9 +149,119 @@ __global__ void __launch_bounds__(256) head_fc2_kernel(HeadParams p, int rows_pe
     }
 }
 
+// ---------------------------------------------------------------- batched
+// The K-hot and bias terms of fc1 and l for every token: g[t][r] = the
+// gathered fc1 table rows + b1, zl[t][e] (logits when H = 0) = the gathered
+// l table rows + bl.  grid T, block 256; the batched head's GEMM epilogue
+// adds the x part.
+__global__ void __launch_bounds__(256) head_tab_kernel(HeadParams p) {
+    __shared__ int32_t rc[32];
+    const int t = blockIdx.x;
+    const int nk = (p.cur || p.prev) ? p.K : 0;     // K <= 16 is checked when a route is given
+    if (threadIdx.x < 2 * nk) {
+        const int32_t *src = threadIdx.x < nk ? p.cur : p.prev;
+        const int k = threadIdx.x < nk ? threadIdx.x : threadIdx.x - nk;
+        rc[threadIdx.x] = src ? src[(size_t)t * nk + k] : -1;
+    }
+    __syncthreads();
+    float *zl = p.H ? p.zl : p.logits;
+    for (int r = threadIdx.x; r < p.H + p.E; r += blockDim.x) {
+        const bool fc1 = r < p.H;
+        const int col = fc1 ? r : r - p.H, width = fc1 ? p.H : p.E;
+        const uint16_t *tab = fc1 ? p.fc1_tab : p.l_tab;
+        float a = bias_f(fc1 ? p.b1 : p.bl, col);
+        if (tab) {
+            // indices outside [0, E) contribute nothing (never read out of bounds)
+            for (int k = 0; k < 2 * nk; k++) {
+                const int c = rc[k];
+                if ((unsigned)c < (unsigned)p.E)
+                    a += half_f(tab[(size_t)(k < nk ? c : p.E + c) * width + col]);
+            }
+        }
+        if (fc1) p.g[(size_t)t * p.H + col] = a;
+        else zl[(size_t)t * p.E + col] = a;
+    }
+}
+
+// fc1 and l on x for T > 1 bf16 tokens (int4 head) as one job of the
+// persistent tensor-core engine: rows [0, H) are fc1 rows, then E l rows,
+// each against every token; the epilogue adds the x part to what
+// head_tab_kernel wrote and applies gelu to the fc1 rows, as head_x_kernel
+// does per token.
+struct HeadXJob {
+    pipe::Maps maps;
+    HeadParams p;
+    int32_t *err;
+    int RB0, RB, cols;
+
+    // Tensor maps (map 0: fc1x rows, map 1: l rows) and geometry.
+    __host__ int make(const HeadParams &pp) {
+        p = pp;
+        err = p.err;
+        RB0 = (p.H + pipe::kRB - 1) / pipe::kRB;
+        RB = RB0 + (p.E + pipe::kRB - 1) / pipe::kRB;
+        cols = p.d;
+        const size_t rec = record_bytes(p.d, 4);
+        if (int rc = pipe::weight_maps(maps, 1, p.lx, rec, p.E, 1, 0, 4)) return rc;
+        if (int rc = p.H ? pipe::weight_maps(maps, 0, p.fc1x, rec, p.H, 1, 0, 4)
+                         : pipe::weight_maps(maps, 0, p.lx, rec, p.E, 1, 0, 4))
+            return rc;
+        return pipe::act_maps(maps, p.x, p.xsum, p.T, p.d);
+    }
+    __device__ void init(int32_t *) const {}
+    __device__ int n_items(const int32_t *) const {
+        return RB * ((p.T + pipe::kTok - 1) / pipe::kTok);
+    }
+    __device__ pipe::Item item(const int32_t *, int i) const {
+        const int tile = i / RB;
+        pipe::Item it;
+        it.g = 0;
+        it.rb = i - tile * RB;
+        it.t0 = tile * pipe::kTok;
+        it.nt = min(pipe::kTok, p.T - it.t0);
+        return it;
+    }
+    __device__ void weights(const pipe::Item &it, int &map, int &row, int &blob) const {
+        map = it.rb < RB0 ? 0 : 1;
+        row = (it.rb < RB0 ? it.rb : it.rb - RB0) * pipe::kRB;
+        blob = 0;
+    }
+    __device__ int row0(const int32_t *, const pipe::Item &it) const { return it.t0; }
+    __device__ const int32_t *meta(const int32_t *, const pipe::Item &) const { return nullptr; }
+    __device__ void epilogue(const int32_t *, const pipe::Item &it, const float *out,
+                             const int32_t *, int tid) const {
+        const bool fc1 = it.rb < RB0;
+        const int base = (fc1 ? it.rb : it.rb - RB0) * pipe::kRB;
+        const int nr = min(pipe::kRB, (fc1 ? p.H : p.E) - base);
+        for (int o = tid; o < it.nt * pipe::kRB; o += pipe::kConsumers * 32) {
+            const int t = o / pipe::kRB, rl = o - t * pipe::kRB;
+            if (rl >= nr) continue;
+            const int tok = it.t0 + t, r = base + rl;
+            const float a = out[rl * pipe::kOutLd + t];
+            if (fc1) {
+                float *gp = p.g + (size_t)tok * p.H + r;
+                *gp = gelu_erf_f(a + *gp);
+            } else {
+                float *zp = (p.H ? p.zl : p.logits) + (size_t)tok * p.E + r;
+                *zp = a + *zp;
+            }
+        }
+    }
+};
+
 int launch_prerouter_head(const HeadParams &p, cudaStream_t st) {
     const int threads = 256;
-    {
+    if (p.T > 1 && p.x_dtype == MOE_DTYPE_BF16 && p.prec == MOE_PREC_AFFINE4) {
+        const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(p.x);
+        if (int rc = pipe::launch_group_sums(xb, p.T, p.d, p.xsum, st)) return rc;
+        head_tab_kernel<<<p.T, threads, 0, st>>>(p);
+        if (int rc = check_launch("head_tab_kernel")) return rc;
+        if (cudaMemsetAsync(p.err, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ECUDA;
+        HeadXJob job;
+        if (int rc = job.make(p)) return rc;
+        if (int rc = pipe::launch_pipe_gemm<4>(job, 0, num_sms(), st, "pipe_gemm_kernel (head fc1, l)"))
+            return rc;
+    } else {
         const int rows = 16;
         const size_t smem = (size_t)(p.d + p.d / 32) * sizeof(float);
         head_x_kernel<<<dim3((p.H + p.E + rows - 1) / rows, p.T), threads, smem, st>>>(p, rows);

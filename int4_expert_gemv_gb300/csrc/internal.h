@@ -41,10 +41,13 @@ struct FfnParams {
     int32_t *offsets;            // workspace [E+2]
     int32_t *perm;               // workspace [T*K] (token*K + k), by expert, in token order
     const __nv_bfloat16 *xb;     // = x, [T][d]
-    float *xsum;                 // workspace [T][d/64]: sum of x per group
+    __nv_bfloat16 *xg;           // workspace [T*K + T][d]: x rows in sorted order (shared: T*K + t)
+    float *xsum;                 // workspace [T*K + T][ld]: sum of xg per group
     __nv_bfloat16 *h16;          // workspace [T*K + T][F]: h at sorted positions (shared: T*K + t)
-    float *hsum;                 // workspace [T*K + T][F/64]
+    float *hsum;                 // workspace [T*K + T][ld]: sum of h per group
     float *vd;                   // workspace [T*K + T][kMaxLoraRank]: A_d h
+    int32_t *item_off;           // workspace [2][E+2]: work-item offsets per group (gate/up, down)
+    int32_t *err;                // workspace word 0: status of the device-side waits
 };
 
 struct HeadParams {
@@ -60,6 +63,8 @@ struct HeadParams {
     const int32_t *cur, *prev;
     float *g;                    // workspace [T][H]
     float *zl;                   // workspace [T][E]
+    float *xsum;                 // workspace [T][ld]: sum of x per group (batched path)
+    int32_t *err;                // workspace word 0: status of the device-side waits
     float *logits;               // [T][E]
 };
 

@@ -144,7 +144,7 @@ def test_expert_ffn_bf16_activations(m):
 
 
 # ------------------------------------------------------------ head
-def _head_case(m, cfg, prec, T, with_prev=True):
+def _head_case(m, cfg, prec, T, with_prev=True, x_dtype=torch.float32):
     from int4_expert_gemv_gb300.model import DeviceModel
     c = replace(cfg, L=1, depth=1, head_prec=prec, E=cfg.E)
     dm = DeviceModel.__new__(DeviceModel)
@@ -163,7 +163,7 @@ def _head_case(m, cfg, prec, T, with_prev=True):
                 bl=DeviceModel._f16(dm, tg(synth.BL), (c.E,), c.sigma_bias))
     for k, v in keep.items():
         setattr(hd, k, v.data_ptr())
-    x = torch.from_numpy(synth.gauss(c.seed, 55, (T, c.d), 1.0)).cuda()
+    x = torch.from_numpy(synth.gauss(c.seed, 55, (T, c.d), 1.0)).cuda().to(x_dtype)
     cur = synth.routes(c.seed, 56, T, c.E, c.K)
     prev = synth.routes(c.seed, 57, T, c.E, c.K)
     logits = torch.empty((T, c.E), device="cuda")
@@ -177,7 +177,7 @@ def _head_case(m, cfg, prec, T, with_prev=True):
     host["lx"] = synth.router_host(c, 0)["lx"]
     got = _f64(logits)
     for t in range(T):
-        ref = orc.head_logits(host, x[t].cpu().double().numpy(), cur[t],
+        ref = orc.head_logits(host, x[t].float().cpu().double().numpy(), cur[t],
                               prev[t] if with_prev else None, c.K)
         assert_close(got[t], ref, f"head {c.name} {prec} token {t}")
 
@@ -186,6 +186,14 @@ def _head_case(m, cfg, prec, T, with_prev=True):
 @pytest.mark.parametrize("cfg", [TINY, MOE35B], ids=lambda c: c.name)
 def test_prerouter_head_parity(m, cfg, prec):
     _head_case(m, cfg, prec, T=3)
+
+
+@pytest.mark.parametrize("cfg,T", [(TINY, 100), (MOE35B, 64), (ALL["wide-int4"], 70)],
+                         ids=["tiny-T100", "35b-T64", "wide-T70"])
+def test_prerouter_head_batched_bf16(m, cfg, T):
+    """Several bf16 tokens with an int4 head take the batched head (fc1 and l
+    as one tensor-core job over all tokens)."""
+    _head_case(m, cfg, "int4", T, x_dtype=torch.bfloat16)
 
 
 def test_prerouter_head_without_prev_route(m):
