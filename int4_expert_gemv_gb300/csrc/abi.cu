@@ -231,7 +231,9 @@ size_t moe_prerouter_head_workspace_bytes(const moe_head_desc *hd, int T) {
     if (hd == nullptr || T < 0) return 0;
     return 256 + align_up((size_t)T * hd->H * sizeof(float), 256) +
            align_up((size_t)T * hd->E * sizeof(float), 256) +
-           align_up((size_t)T * gsum_ld(hd->d) * sizeof(float), 256);
+           align_up((size_t)T * gsum_ld(hd->d) * sizeof(float), 256) +
+           align_up((size_t)2 * T * hd->H * sizeof(uint16_t), 256) +
+           align_up((size_t)2 * T * gsum_ld(hd->H) * sizeof(float), 256);
 }
 
 int moe_prerouter_head(const moe_head_desc *hd, const void *x, int x_dtype,
@@ -274,7 +276,11 @@ int moe_prerouter_head(const moe_head_desc *hd, const void *x, int x_dtype,
     p.g = reinterpret_cast<float *>(w + 256);
     const size_t zl_off = 256 + align_up((size_t)T * hd->H * sizeof(float), 256);
     p.zl = reinterpret_cast<float *>(w + zl_off);
-    p.xsum = reinterpret_cast<float *>(w + zl_off + align_up((size_t)T * hd->E * sizeof(float), 256));
+    const size_t xs_off = zl_off + align_up((size_t)T * hd->E * sizeof(float), 256);
+    p.xsum = reinterpret_cast<float *>(w + xs_off);
+    const size_t gg_off = xs_off + align_up((size_t)T * gsum_ld(hd->d) * sizeof(float), 256);
+    p.gg = reinterpret_cast<__nv_bfloat16 *>(w + gg_off);
+    p.ggsum = reinterpret_cast<float *>(w + gg_off + align_up((size_t)2 * T * hd->H * sizeof(uint16_t), 256));
     p.logits = logits;
     return launch_prerouter_head(p, stream);
 }

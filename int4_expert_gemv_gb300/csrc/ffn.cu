@@ -74,10 +74,11 @@ __device__ __forceinline__ void stage_x(const void *x, int dtype, size_t base, i
 
 // ---------------------------------------------------------------- LoRA A x
 // v[t*slots+s][which][i] = sum_k A[i][k] x[t][k] for the gate (which 0) and
-// up (which 1) adapters of slot s.  grid (slots, T), 256 threads.
-__global__ void __launch_bounds__(256) lora_ax_kernel(FfnParams p) {
+// up (which 1) adapters of slot s = s0 + blockIdx.x.  grid (slots from s0,
+// T), 256 threads.
+__global__ void __launch_bounds__(256) lora_ax_kernel(FfnParams p, int s0) {
     extern __shared__ float sm[];
-    const int s = blockIdx.x, t = blockIdx.y, d = p.d;
+    const int s = s0 + blockIdx.x, t = blockIdx.y, d = p.d;
     float *xs = sm;
     for (int i = threadIdx.x; i < d; i += blockDim.x)
         xs[i] = load_act(p.x, p.x_dtype, (size_t)t * d + i);
@@ -212,7 +213,7 @@ static int launch_bits(const FfnParams &p, cudaStream_t st) {
     constexpr int VALS = 128 / BITS;
     const int threads = 256;
     if (p.any_gu_lora) {
-        lora_ax_kernel<<<dim3(p.slots, p.T), threads, p.d * sizeof(float), st>>>(p);
+        lora_ax_kernel<<<dim3(p.slots, p.T), threads, p.d * sizeof(float), st>>>(p, 0);
         if (int rc = check_launch("lora_ax_kernel")) return rc;
     }
     {
@@ -238,8 +239,12 @@ static int launch_bits(const FfnParams &p, cudaStream_t st) {
     return MOE_OK;
 }
 
+// Only the slots that carry a gate or up adapter: all of them when the
+// routed experts do, else the shared slot alone.
 void lora_ax_kernel_launch(const FfnParams &p, cudaStream_t st) {
-    lora_ax_kernel<<<dim3(p.slots, p.T), 256, p.d * sizeof(float), st>>>(p);
+    const bool routed = p.lora[0].r || p.lora[1].r;
+    lora_ax_kernel<<<dim3(routed ? p.slots : 1, p.T), 256, p.d * sizeof(float), st>>>(
+        p, routed ? 0 : p.K);
 }
 
 int launch_expert_ffn(const FfnParams &p, cudaStream_t st) {

@@ -28,16 +28,30 @@ using namespace pipe;
 // ---------------------------------------------------------------- sort
 // counts[e] = entries routed to expert e (e < E); counts[E] = entries with an
 // index outside [0, E).  One warp per bucket.
+// Whether entry value e falls in bucket b (b = E: outside [0, E)).
+__device__ __forceinline__ bool in_bucket(int e, int b, int E) {
+    return b < E ? e == b : (unsigned)e >= (unsigned)E;
+}
+
+constexpr int kSortU = 8;         // entries per lane loaded before they are ranked
+
 __global__ void __launch_bounds__(256) sort_count_kernel(const int32_t *idx, int TK, int E,
                                                          int32_t *counts) {
     const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     if (b > E) return;
     int n = 0;
-    for (int i0 = 0; i0 < TK; i0 += 32) {
-        const int i = i0 + lane;
-        const int e = i < TK ? idx[i] : 0;
-        const bool m = i < TK && (b < E ? e == b : (unsigned)e >= (unsigned)E);
-        n += __popc(__ballot_sync(0xffffffffu, m));
+    for (int i0 = 0; i0 < TK; i0 += 32 * kSortU) {
+        int e[kSortU];
+#pragma unroll
+        for (int u = 0; u < kSortU; u++) {
+            const int i = i0 + 32 * u + lane;
+            e[u] = i < TK ? idx[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kSortU; u++) {
+            const bool m = i0 + 32 * u + lane < TK && in_bucket(e[u], b, E);
+            n += __popc(__ballot_sync(0xffffffffu, m));
+        }
     }
     if (lane == 0) counts[b] = n;
 }
@@ -59,13 +73,21 @@ __global__ void __launch_bounds__(256) sort_scatter_kernel(const int32_t *idx, i
     }
     int rank = 0;
     const uint32_t below = (1u << lane) - 1u;
-    for (int i0 = 0; i0 < TK; i0 += 32) {
-        const int i = i0 + lane;
-        const int e = i < TK ? idx[i] : 0;
-        const bool m = i < TK && (b < E ? e == b : (unsigned)e >= (unsigned)E);
-        const uint32_t mask = __ballot_sync(0xffffffffu, m);
-        if (m) perm[off + rank + __popc(mask & below)] = i;
-        rank += __popc(mask);
+    for (int i0 = 0; i0 < TK; i0 += 32 * kSortU) {
+        int e[kSortU];
+#pragma unroll
+        for (int u = 0; u < kSortU; u++) {
+            const int i = i0 + 32 * u + lane;
+            e[u] = i < TK ? idx[i] : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < kSortU; u++) {
+            const int i = i0 + 32 * u + lane;
+            const bool m = i < TK && in_bucket(e[u], b, E);
+            const uint32_t mask = __ballot_sync(0xffffffffu, m);
+            if (m) perm[off + rank + __popc(mask & below)] = i;
+            rank += __popc(mask);
+        }
     }
 }
 
@@ -296,12 +318,12 @@ struct FfnJob {
     }
 };
 
-// vd[pos][i] = sum_f A_d[i][f] h[pos][f] for every sorted position whose
-// slot has a down LoRA.  One warp per (position, i).
-__global__ void __launch_bounds__(256) lora_down_ax_kernel(FfnParams p, int npos) {
+// vd[pos][i] = sum_f A_d[i][f] h[pos][f] for the sorted positions p0 ..
+// npos - 1 whose slot has a down LoRA.  One warp per (position, i).
+__global__ void __launch_bounds__(256) lora_down_ax_kernel(FfnParams p, int p0, int npos) {
     const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (w >= npos * kMaxLoraRank) return;
-    const int ps = w / kMaxLoraRank, i = w % kMaxLoraRank;
+    if (w >= (npos - p0) * kMaxLoraRank) return;
+    const int ps = p0 + w / kMaxLoraRank, i = w % kMaxLoraRank;
     const int TK = p.T * p.K;
     int t, sl;
     if (ps >= TK) {
@@ -354,9 +376,11 @@ static int launch_bits(const FfnParams &p, cudaStream_t st) {
     if (int rc = launch_pipe_gemm<BITS>(gu, scratch, sms, st, "pipe_gemm_kernel (gate/up)"))
         return rc;
     if (int rc = launch_group_sums(p.h16, npos, p.F, p.hsum, st)) return rc;
-    if (p.lora[2].r || p.shared_lora[2].r) {
-        const int warps = npos * kMaxLoraRank;
-        lora_down_ax_kernel<<<(warps + 7) / 8, 256, 0, st>>>(p, npos);
+    if (p.lora[2].r || (p.shared && p.shared_lora[2].r)) {
+        // positions [p0, npos): all of them, or the shared expert's alone
+        const int p0 = p.lora[2].r ? 0 : TK;
+        const int warps = (npos - p0) * kMaxLoraRank;
+        lora_down_ax_kernel<<<(warps + 7) / 8, 256, 0, st>>>(p, p0, npos);
         if (int rc = check_launch("lora_down_ax_kernel")) return rc;
     }
     FfnJob<true> dn;

@@ -239,12 +239,69 @@ struct HeadXJob {
             const int tok = it.t0 + t, r = base + rl;
             const float a = out[rl * pipe::kOutLd + t];
             if (fc1) {
-                float *gp = p.g + (size_t)tok * p.H + r;
-                *gp = gelu_erf_f(a + *gp);
+                // g = gelu(.), split as hi + lo (two bf16 rows) for the fc2 job
+                const float gv = gelu_erf_f(a + p.g[(size_t)tok * p.H + r]);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(gv);
+                p.gg[(size_t)(2 * tok) * p.H + r] = hi;
+                p.gg[(size_t)(2 * tok + 1) * p.H + r] = __float2bfloat16_rn(gv - __bfloat162float(hi));
             } else {
                 float *zp = (p.H ? p.zl : p.logits) + (size_t)tok * p.E + r;
                 *zp = a + *zp;
             }
+        }
+    }
+};
+
+// fc2 on g for T > 1 bf16 tokens (int4 head): E records of H columns
+// against the 2T rows of g split as bf16 hi + lo (g = hi + lo to about 16
+// significant bits, so the logits keep fp32 accuracy); the epilogue adds a
+// token's two rows, b2 and zl: logits[t][e].
+struct Fc2Job {
+    pipe::Maps maps;
+    HeadParams p;
+    int32_t *err;
+    int RB, cols;
+
+    __host__ int make(const HeadParams &pp) {
+        p = pp;
+        err = p.err;
+        RB = (p.E + pipe::kRB - 1) / pipe::kRB;
+        cols = p.H;
+        const size_t rec = record_bytes(p.H, 4);
+        if (int rc = pipe::weight_maps(maps, 0, p.fc2, rec, p.E, 1, 0, 4)) return rc;
+        if (int rc = pipe::weight_maps(maps, 1, p.fc2, rec, p.E, 1, 0, 4)) return rc;
+        return pipe::act_maps(maps, p.gg, p.ggsum, 2 * p.T, p.H);
+    }
+    __device__ void init(int32_t *) const {}
+    __device__ int n_items(const int32_t *) const {
+        return RB * ((2 * p.T + pipe::kTok - 1) / pipe::kTok);
+    }
+    __device__ pipe::Item item(const int32_t *, int i) const {
+        const int tile = i / RB;
+        pipe::Item it;
+        it.g = 0;
+        it.rb = i - tile * RB;
+        it.t0 = tile * pipe::kTok;
+        it.nt = min(pipe::kTok, 2 * p.T - it.t0);
+        return it;
+    }
+    __device__ void weights(const pipe::Item &it, int &map, int &row, int &blob) const {
+        map = 0;
+        row = it.rb * pipe::kRB;
+        blob = 0;
+    }
+    __device__ int row0(const int32_t *, const pipe::Item &it) const { return it.t0; }
+    __device__ const int32_t *meta(const int32_t *, const pipe::Item &) const { return nullptr; }
+    __device__ void epilogue(const int32_t *, const pipe::Item &it, const float *out,
+                             const int32_t *, int tid) const {
+        const int base = it.rb * pipe::kRB;
+        const int nr = min(pipe::kRB, p.E - base);
+        for (int o = tid; o < (it.nt / 2) * pipe::kRB; o += pipe::kConsumers * 32) {
+            const int tl = o / pipe::kRB, rl = o - tl * pipe::kRB;
+            if (rl >= nr) continue;
+            const int tok = (it.t0 >> 1) + tl, e = base + rl;
+            const float a = out[rl * pipe::kOutLd + 2 * tl] + out[rl * pipe::kOutLd + 2 * tl + 1];
+            p.logits[(size_t)tok * p.E + e] = a + bias_f(p.b2, e) + p.zl[(size_t)tok * p.E + e];
         }
     }
 };
@@ -261,6 +318,13 @@ int launch_prerouter_head(const HeadParams &p, cudaStream_t st) {
         if (int rc = job.make(p)) return rc;
         if (int rc = pipe::launch_pipe_gemm<4>(job, 0, num_sms(), st, "pipe_gemm_kernel (head fc1, l)"))
             return rc;
+        if (p.H > 0) {
+            if (int rc = pipe::launch_group_sums(p.gg, 2 * p.T, p.H, p.ggsum, st)) return rc;
+            Fc2Job f2;
+            if (int rc = f2.make(p)) return rc;
+            return pipe::launch_pipe_gemm<4>(f2, 0, num_sms(), st, "pipe_gemm_kernel (head fc2)");
+        }
+        return MOE_OK;
     } else {
         const int rows = 16;
         const size_t smem = (size_t)(p.d + p.d / 32) * sizeof(float);

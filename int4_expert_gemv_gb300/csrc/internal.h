@@ -64,6 +64,8 @@ struct HeadParams {
     float *g;                    // workspace [T][H]
     float *zl;                   // workspace [T][E]
     float *xsum;                 // workspace [T][ld]: sum of x per group (batched path)
+    __nv_bfloat16 *gg;           // workspace [2T][H]: g split as bf16 hi (row 2t) + lo (row 2t+1)
+    float *ggsum;                // workspace [2T][ld]: sum of gg per group
     int32_t *err;                // workspace word 0: status of the device-side waits
     float *logits;               // [T][E]
 };

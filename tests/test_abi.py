@@ -140,10 +140,13 @@ def test_head_workspace_and_k_checks(m):
     hd = _head_desc(m)
     need = m.moe_prerouter_head_workspace_bytes(hd, 3)
     # status word (256 bytes), g [T][H] fp32, zl [T][E] fp32, sums of x per group
-    # [T][ld] fp32 (ld = d/64 padded to 4), each 256-aligned
+    # [T][ld] fp32 (ld = d/64 padded to 4), g split into bf16 hi/lo rows
+    # [2T][H], their sums per group [2T][ldh], each 256-aligned
     a256 = lambda n: (n + 255) // 256 * 256
     ld = (hd.d // 64 + 3) // 4 * 4
-    assert need == 256 + a256(3 * 512 * 4) + a256(3 * 256 * 4) + a256(3 * ld * 4)
+    ldh = (hd.H // 64 + 3) // 4 * 4
+    assert need == (256 + a256(3 * 512 * 4) + a256(3 * 256 * 4) + a256(3 * ld * 4)
+                    + a256(6 * 512 * 2) + a256(6 * ldh * 4))
     rc = m.lib().moe_prerouter_head(C.byref(hd), 1 << 20, 0, None, None, 4, 3, 1 << 20,
                                     1 << 20, need - 1, None)
     assert rc == m.MOE_ENOSPACE
