@@ -58,6 +58,30 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_traffic(layers: int):
+    """DRAM bytes (read + write) of one fused decode-step launch over `layers`
+    layers, scaled from the ncu capture summarised in
+    profiles/decode_step_35b_L4.md; None when the kernel's sources have
+    changed since that capture."""
+    import hashlib
+    import re
+    p = os.path.join(ROOT, "profiles", "decode_step_35b_L4.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    per_layer = re.search(r"traffic_bytes_per_layer: (\d+)", text)
+    files = re.search(r"kernel_sources: (.+)", text)
+    digest = re.search(r"kernel_sources_sha256_16: ([0-9a-f]+)", text)
+    if not (per_layer and files and digest):
+        return None
+    h = hashlib.sha256()
+    for f in files.group(1).split():
+        h.update(open(os.path.join(ROOT, "int4_expert_gemv_gb300", "csrc", f), "rb").read())
+    if h.hexdigest()[:16] != digest.group(1):
+        return None
+    return int(per_layer.group(1)) * layers
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -334,7 +358,8 @@ def run_native(args, cfg):
             "expert_weight_frac_of_hbm": expert_gbs / hbm,
             "roofline": {"bound": "hbm", "kernel": kname,
                          "achieved": achieved, "peak": hbm, "peak_kind": hbm_kind,
-                         "unit": "GB/s", "frac": achieved / hbm, "traffic": None,
+                         "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": measured_traffic(cfg.depth) if st.fused else None,
                          "bytes_per_launch": launch_bytes,
                          "avg_launch_us": launch_avg_ms * 1000.0,
                          "timing": f"CUDA events around each layer's call in {n_inst} "

@@ -165,7 +165,12 @@ size_t moe_prerouter_head_workspace_bytes(const moe_head_desc *hd, int T);
  * may be NULL (an all-zero vector).  logits: fp32 [T][E].
  *   a = fc1x x + sum_{c in cur} fc1_tab[c] + sum_{c in prev} fc1_tab[E+c] + b1
  *   logits = fc2 gelu_erf(a) + b2 + lx x + sum l_tab rows (same rule) + bl
- * With H == 0 only the l branch is computed (a plain linear router). */
+ * With H == 0 only the l branch is computed (a plain linear router).
+ * T > 1 tokens in bf16 with an int4 head run fc1 + l and fc2 as tensor-core
+ * GEMMs over all tokens (fc2's input g carried as bf16 hi + lo parts, so the
+ * logits keep fp32 accuracy); ws word 0 then holds the status of their
+ * bounded device-side waits (MOE_OK or MOE_ETIMEOUT) once the stream
+ * completes. */
 int moe_prerouter_head(const moe_head_desc *hd, const void *x, int x_dtype,
                        const int32_t *cur_idx, const int32_t *prev_idx, int K,
                        int T, float *logits, void *ws, size_t ws_bytes,
@@ -208,7 +213,15 @@ size_t moe_expert_ffn_workspace_bytes(const moe_experts_desc *ed, int T, int K);
  * k < K holds expert idx[t][k]'s output y = W_d h (+ LoRA), the last slot the
  * shared expert's.  h = silu(W_g x + LoRA) * (W_u x + LoRA) is kept in fp32
  * for x_dtype == MOE_DTYPE_F32 and rounded to bf16 for MOE_DTYPE_BF16.
- * T == 1 is the decode path; T > 1 groups tokens by expert first. */
+ * An index outside [0, E) is never read: that slot's output is NaN.
+ * T == 1, or fp32 x, is the decode path (per-token GEMVs).  T > 1 with bf16 x
+ * is the batched path: the (token, slot) entries are sorted by expert (a
+ * stable counting sort, "tokens sorted/grouped by expert" of the batched
+ * configuration in xyznot.com/es/paper/2609.18063's workload list) and each
+ * expert's tokens run as grouped tensor-core GEMMs that read its weights
+ * once.  Results are deterministic.  The batched path's device-side waits
+ * are bounded: after the stream completes, int32 word 0 of ws holds MOE_OK,
+ * or MOE_ETIMEOUT if one expired (the outputs are then invalid). */
 int moe_expert_ffn_int4(const moe_experts_desc *ed, const void *x, int x_dtype,
                         const int32_t *idx, int T, int K, float *y_slots,
                         void *ws, size_t ws_bytes, cudaStream_t stream);

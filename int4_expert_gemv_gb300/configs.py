@@ -83,6 +83,10 @@ def batched(T: int) -> MoEConfig:
 ALL = {
     "tiny": TINY,
     "35b": MOE35B,
+    # the 35B-like stack with 4 resident layers (1.8 GB of experts): the
+    # profiling case of the fused decode step (its traffic per layer is the
+    # 40-layer stack's)
+    "35b-L4": replace(MOE35B, name="35b-like-d2048-E256-K4-F512-shared-L4", L=4, depth=4),
     "35b-K2": k_sweep(2),
     "35b-K8": k_sweep(8),
     "8b": MOE8B,
