@@ -88,4 +88,7 @@ int launch_debug_dequant(const uint8_t *sec, size_t rec, size_t first_record,
 
 int num_sms();
 
+// Validation of a decode-stack descriptor shared by the decode-step paths.
+int check_decode_stack(const moe_stack_desc *sd);
+
 }  // namespace moe

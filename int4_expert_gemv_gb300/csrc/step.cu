@@ -1859,6 +1859,10 @@ static int check_stack(const moe_stack_desc *sd) {
     return MOE_OK;
 }
 
+namespace moe {
+int check_decode_stack(const moe_stack_desc *sd) { return check_stack(sd); }
+}  // namespace moe
+
 extern "C" size_t moe_decode_step_workspace_bytes(const moe_stack_desc *sd) {
     if (check_stack(sd) != MOE_OK) return 0;
     const moe_experts_desc &e0 = sd->experts[0];

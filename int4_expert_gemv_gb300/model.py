@@ -173,10 +173,12 @@ class DecodeStack:
     """Batch-1 decode over `depth` layers (resident layers cycled).
 
     fused=True runs steady-state steps (t >= 1) as one persistent kernel
-    (moe_decode_step); step 0, where every layer routes with its own router,
-    always runs through the four per-layer calls."""
+    (moe_decode_step); fused="chain" as two kernels per layer chained by
+    programmatic dependent launch (moe_decode_step_chain); step 0, where every
+    layer routes with its own router, always runs through the four per-layer
+    calls."""
 
-    def __init__(self, model: DeviceModel, fused: bool = False):
+    def __init__(self, model: DeviceModel, fused=False):
         self.m = model
         c = self.cfg = model.cfg
         dev = model.device
@@ -200,7 +202,8 @@ class DecodeStack:
                                    dtype=torch.uint8, device=dev)
         self.t = 0
         self.graphs = {}
-        self.fused = fused
+        self.fused = bool(fused)
+        self.chain = False
         if fused:
             L = model.layers
             self._ed = (moe.ExpertsDesc * c.L)(*[ly["experts_desc"] for ly in L])
@@ -210,8 +213,10 @@ class DecodeStack:
             self.sd = moe.StackDesc(C.cast(self._ed, C.c_void_p), C.cast(self._rd, C.c_void_p),
                                     C.cast(self._hd, C.c_void_p) if has_heads else None,
                                     c.L, c.depth, c.K, int(c.self_predict), 0, 0, None)
-            self.step_ws = torch.zeros(moe.moe_decode_step_workspace_bytes(self.sd),
-                                       dtype=torch.uint8, device=dev)
+            self.chain = fused == "chain"
+            nbytes = (moe.moe_decode_step_chain_workspace_bytes(self.sd) if self.chain
+                      else moe.moe_decode_step_workspace_bytes(self.sd))
+            self.step_ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
 
     def _layer(self, N: int):
         return self.m.layers[N % self.cfg.L]
@@ -228,8 +233,8 @@ class DecodeStack:
         """Enqueue step t >= 1 as one moe_decode_step launch."""
         if events is not None:
             events[0].record()
-        moe.moe_decode_step(self.sd, self.xin, self.stream, self.r_idx, self.r_w, self.r_margin,
-                            t, self.step_ws)
+        call = moe.moe_decode_step_chain if self.chain else moe.moe_decode_step
+        call(self.sd, self.xin, self.stream, self.r_idx, self.r_w, self.r_margin, t, self.step_ws)
         if events is not None:
             events[1].record()
 

@@ -86,6 +86,8 @@ def lib():
                 "moe_decode_step_workspace_bytes": (S, [C.POINTER(StackDesc)]),
                 "moe_decode_step": (I, [C.POINTER(StackDesc), P, P, P, P, P, I, P, S, P]),
                 "moe_decode_step_status": (I, [P, C.POINTER(C.c_int), P]),
+                "moe_decode_step_chain_workspace_bytes": (S, [C.POINTER(StackDesc)]),
+                "moe_decode_step_chain": (I, [C.POINTER(StackDesc), P, P, P, P, P, I, P, S, P]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -229,6 +231,17 @@ def moe_decode_step(sd: StackDesc, x0, out, route_idx, route_w, route_margin, t:
     _check(lib().moe_decode_step(C.byref(sd), _ptr(x0), _ptr(out), _ptr(route_idx),
                                  _ptr(route_w), _ptr(route_margin), t, _ptr(ws), _nbytes(ws),
                                  _stream(stream)), "moe_decode_step")
+
+
+def moe_decode_step_chain_workspace_bytes(sd: StackDesc) -> int:
+    return lib().moe_decode_step_chain_workspace_bytes(C.byref(sd))
+
+
+def moe_decode_step_chain(sd: StackDesc, x0, out, route_idx, route_w, route_margin, t: int, ws,
+                          stream=None):
+    _check(lib().moe_decode_step_chain(C.byref(sd), _ptr(x0), _ptr(out), _ptr(route_idx),
+                                       _ptr(route_w), _ptr(route_margin), t, _ptr(ws), _nbytes(ws),
+                                       _stream(stream)), "moe_decode_step_chain")
 
 
 def moe_decode_step_status(ws, stream=None) -> int:

@@ -84,7 +84,8 @@ def check_stack(cfg, steps, fused=False):
     return forced
 
 
-PATHS = [pytest.param(False, id="per-call"), pytest.param(True, id="fused")]
+PATHS = [pytest.param(False, id="per-call"), pytest.param(True, id="fused"),
+         pytest.param("chain", id="chain")]
 
 
 @pytest.mark.parametrize("fused", PATHS)
