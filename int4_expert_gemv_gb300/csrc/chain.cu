@@ -27,15 +27,21 @@
 #include <cstring>
 
 #include "internal.h"
+#include "step_common.cuh"
 
 namespace moe {
 namespace chain {
+
+using step::chunk_dot_fix;
+using step::Fix;
+using step::stage_chunk;
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxR = 32;                 // LoRA rank bound
 constexpr int kMaxK = 16;
 constexpr uint64_t kCopyWaitNs = 1000000000ull;
+constexpr int kMaxHPass = 8;              // h of all slots: at most 8 * 512 float4 (16 Ki floats)
 
 struct CLayer {
     const uint8_t *pool, *shared;
@@ -71,9 +77,11 @@ struct CP {
     float *g, *zl, *z;        // [H], [E], [E] of layer N
     const float *vp;          // [n_cta][2 kMaxR] partials of layer N's gate/up LoRA
     float *vp_next;           // [n_cta][2 kMaxR] the next layer's
-    const float *topk_z;      // logits to rank in A (head N-1's), or null
+    const float *topk_z;      // logits the router top-K ranks
     int topk_set, topk_tgt;   // where the route goes
     int32_t *err;
+    unsigned long long *trace;   // debug: per launch 8 stamps of CTA 0 (start, waited, end, ...)
+    int launch_id;
 };
 
 // ---------------------------------------------------------------- device helpers
@@ -122,6 +130,15 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, int32_t *err) {
     }
 }
 
+// Debug stamp k of this launch (CTA 0, thread 0), when tracing.
+__device__ __forceinline__ void stamp(const CP &p, int k) {
+    if (p.trace && blockIdx.x == 0 && threadIdx.x == 0) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        p.trace[(size_t)p.launch_id * 8 + k] = t;
+    }
+}
+
 __device__ __forceinline__ float block_sum(float v, float *red) {
     v = warp_sum(v, 32);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -153,62 +170,169 @@ __device__ __forceinline__ float rec_dot(const uint8_t *rec, int cols, const flo
 // Stages n floats (global) into shared memory in chunks of `vals` values,
 // chunk c at dst + c * (vals + 1): the lanes of a warp each take one chunk,
 // and the one-float pad puts lane l's j-th value in bank (l + j) mod 32 (no
-// conflicts).  Also the per-chunk sums.  Returns the sum of squares (every
-// thread).
+// conflicts).  The per-chunk sums come from the same pass: a chunk's vals / 4
+// float4 loads sit in consecutive lanes, reduced with shuffles (in a fixed
+// order).  Returns the sum of squares (every thread).  n: a multiple of 4 *
+// blockDim.x is not needed, vals: 32 or 64.
 __device__ __forceinline__ float stage_vec(const float *src, int n, int vals, float *dst,
                                            float *sums, float *red) {
     float ss = 0.0f;
-    for (int i = threadIdx.x; i < n / 4; i += blockDim.x) {      // n and vals: multiples of 4
-        const float4 v = reinterpret_cast<const float4 *>(src)[i];
+    const int per = vals / 4;                                 // lanes per chunk (8 or 16)
+    for (int base = 0; base < n / 4; base += blockDim.x) {    // whole warps per pass (shuffles)
+        const int i = base + threadIdx.x;
+        float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (i < n / 4) v = reinterpret_cast<const float4 *>(src)[i];
         const int c = (4 * i) / vals, j = 4 * i - c * vals;
-        float *d = dst + c * (vals + 1) + j;
-        d[0] = v.x;
-        d[1] = v.y;
-        d[2] = v.z;
-        d[3] = v.w;
+        if (i < n / 4) {
+            float *d = dst + c * (vals + 1) + j;
+            d[0] = v.x;
+            d[1] = v.y;
+            d[2] = v.z;
+            d[3] = v.w;
+        }
         ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-    }
-    __syncthreads();
-    for (int c = threadIdx.x; c < n / vals; c += blockDim.x) {
-        float a = 0.0f;
-        for (int j = 0; j < vals; j++) a += dst[c * (vals + 1) + j];
-        sums[c] = a;
+        float a = (v.x + v.y) + (v.z + v.w);
+        for (int o = 1; o < per; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (i < n / 4 && (i & (per - 1)) == 0) sums[c] = a;
     }
     return block_sum(ss, red);
 }
 
 __host__ __device__ inline size_t padded(int n, int vals) { return (size_t)(n / vals) * (vals + 1); }
 
+// stage_vec in two halves, so that several vectors' loads are in flight
+// together: load_vec issues this thread's float4 loads (at most MAXP passes of
+// the block), store_vec stores them padded with the per-chunk sums (as
+// stage_vec, without the sum of squares).
+template <int MAXP>
+__device__ __forceinline__ void load_vec(const float *src, int n, float4 (&v)[MAXP]) {
+#pragma unroll
+    for (int k = 0; k < MAXP; k++) {
+        const int i = k * blockDim.x + threadIdx.x;
+        v[k] = i < n / 4 ? reinterpret_cast<const float4 *>(src)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+template <int MAXP>
+__device__ __forceinline__ void store_vec(const float4 (&v)[MAXP], int n, int vals, float *dst,
+                                          float *sums) {
+    const int per = vals / 4;
+#pragma unroll
+    for (int k = 0; k < MAXP; k++) {
+        const int i = k * blockDim.x + threadIdx.x;
+        if (k * (int)blockDim.x >= n / 4) break;                 // whole block: uniform
+        const int c = (4 * i) / vals, j = 4 * i - c * vals;
+        if (i < n / 4) {
+            float *d = dst + c * (vals + 1) + j;
+            d[0] = v[k].x;
+            d[1] = v[k].y;
+            d[2] = v[k].z;
+            d[3] = v[k].w;
+        }
+        float a = (v[k].x + v[k].y) + (v[k].z + v[k].w);
+        for (int o = 1; o < per; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+        if (i < n / 4 && (i & (per - 1)) == 0) sums[c] = a;
+    }
+}
+
+// The vector staged padded by stage_vec (chunks of 128 / BITS values), again
+// as 16-bit fixed point per chunk for the dp4a dot (one chunk per warp pass;
+// layout and scales as the persistent decode kernel's): xf bytes, the chunk
+// scale 2^(e-15) and xhat = sum of the fixed-point values times the scale.
+template <int BITS>
+__device__ __forceinline__ void stage_fix(const float *xp, int n, uint8_t *xf, float *xsc,
+                                          float *xhat) {
+    constexpr int VALS = 128 / BITS, PER = VALS / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nch = n / VALS;
+    for (int c = warp; c < nch; c += kWarps) {
+        float v[PER];
+#pragma unroll
+        for (int m = 0; m < PER; m++) v[m] = xp[c * (VALS + 1) + lane + 32 * m];
+        stage_chunk<BITS>(v, lane, xf, c, nch, xsc, xhat);
+    }
+}
+
+__host__ __device__ inline size_t fix_bytes(int n, int bits) {
+    return (size_t)(n / (128 / bits)) * (bits == 4 ? 4 : 8) * 16;
+}
+
+// Dots of R consecutive records (rec0, rec0 + stride, ...; cols columns) with
+// a vector staged by stage_fix, over this lane's chunks (exact integer chunk
+// dots, then fma(scale, dot * 2^(e-15), bias * xhat)).
+template <int BITS, int R>
+__device__ __forceinline__ void fix_dot(const uint8_t *rec0, uint32_t stride, int cols,
+                                        const uint8_t *xf, const float *xsc, const float *xhat,
+                                        int lane, float (&out)[R]) {
+    constexpr int VALS = 128 / BITS;
+    const int nch = cols / VALS;
+    const size_t cb = code_bytes(cols, BITS);
+    const uint4 *xq = reinterpret_cast<const uint4 *>(xf);
+#pragma unroll
+    for (int r = 0; r < R; r++) out[r] = 0.0f;
+    for (int c = lane; c < nch; c += 32) {
+        uint4 q[R];
+        uint32_t sbw[R];
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            q[r] = *reinterpret_cast<const uint4 *>(rec0 + (size_t)r * stride + (size_t)kChunk * c);
+            sbw[r] = *reinterpret_cast<const uint32_t *>(rec0 + (size_t)r * stride + cb + 4 * ((c * VALS) / kGroup));
+        }
+        int dq[R];
+        chunk_dot_fix<BITS, R>(q, xq, nch, c, dq);
+        const float sc = xsc[c], X = xhat[c];
+#pragma unroll
+        for (int r = 0; r < R; r++) {
+            const float2 sb = sb_f(sbw[r]);
+            out[r] += fmaf(sb.x, (float)dq[r] * sc, sb.y * X);
+        }
+    }
+}
+
 __device__ __forceinline__ float half_at(const uint16_t *p, size_t i) { return half_f(p[i]); }
 
 // Ranks E <= 1024 logits (value desc, index asc; NaN last) in one warp:
 // route of layer tgt in set `set` (indices, softmax weights over the kept K,
-// margin z_(K) - z_(K+1)).  Lane l holds logits l, l + 32, ...
-__device__ void warp_route(const float *z, int E, int K, int32_t *ridx, float *rw, float *rmargin,
-                           int set, int depth, int tgt) {
+// margin z_(K) - z_(K+1)).  Lane l holds logits l, l + 32, ... (vals, loaded
+// by load_logits); each lane keeps its best remaining one, every round takes
+// the warp's best of those (ties: lower index) and only the winning lane
+// rescans.  The k-th winner ends in lane k (registers only).
+struct Logits {
+    float v[32];
+};
+
+__device__ __forceinline__ void load_logits(const float *z, int E, Logits &L) {
     const int lane = threadIdx.x & 31;
-    float vals[32];
 #pragma unroll
     for (int i = 0; i < 32; i++) {
         const int e = lane + 32 * i;
-        const float v = e < E ? z[e] : -INFINITY;
-        vals[i] = v == v ? v : -INFINITY;
+        const float x = e < E ? z[e] : -INFINITY;
+        L.v[i] = x == x ? x : -INFINITY;
     }
-    float topv[kMaxK + 1];
-    int topi[kMaxK + 1];
-    const int rounds = K < E ? K + 1 : K;
+}
+
+__device__ void warp_route(const Logits &L, int E, int K, int32_t *ridx, float *rw, float *rmargin,
+                           int set, int depth, int tgt) {
+    const int lane = threadIdx.x & 31;
     uint32_t taken = 0;
-    for (int k = 0; k < rounds; k++) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+    auto best_of_lane = [&](float &bv, int &bi) {
+        bv = -INFINITY;
+        bi = 0x7fffffff;
 #pragma unroll
         for (int i = 0; i < 32; i++) {
             const int e = lane + 32 * i;
-            if (e < E && !(taken >> i & 1u) && (vals[i] > bv || (vals[i] == bv && e < bi))) {
-                bv = vals[i];
+            if (e < E && !(taken >> i & 1u) && (L.v[i] > bv || (L.v[i] == bv && e < bi))) {
+                bv = L.v[i];
                 bi = e;
             }
         }
+    };
+    float lv, mv = -INFINITY;       // this lane's best remaining; my winner's value (lane k)
+    int li, mi = 0;
+    best_of_lane(lv, li);
+    const int rounds = K < E ? K + 1 : K;
+    for (int k = 0; k < rounds; k++) {
+        float bv = lv;
+        int bi = li;
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
             const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
@@ -217,37 +341,41 @@ __device__ void warp_route(const float *z, int E, int K, int32_t *ridx, float *r
                 bi = oi;
             }
         }
-        topv[k] = bv;
-        topi[k] = bi;
-        if (bi < E && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    }
-    if (lane == 0) {
-        float sum = 0.0f;
-        for (int k = 0; k < K; k++) sum += expf(topv[k] - topv[0]);
-        for (int k = 0; k < K; k++) {
-            ridx[((size_t)set * depth + tgt) * K + k] = topi[k];
-            rw[((size_t)set * depth + tgt) * K + k] = expf(topv[k] - topv[0]) / sum;
+        if (lane == k) {
+            mv = bv;
+            mi = bi;
         }
-        rmargin[(size_t)set * depth + tgt] = K < E ? topv[K - 1] - topv[K] : INFINITY;
+        if (bi < E && (bi & 31) == lane) {      // the winner's lane takes it and rescans
+            taken |= 1u << (bi >> 5);
+            best_of_lane(lv, li);
+        }
     }
+    // softmax over the kept K (lane k < K), margin from lanes K - 1 and K
+    const float top = __shfl_sync(0xffffffffu, mv, 0);
+    const float ex = lane < K ? expf(mv - top) : 0.0f;
+    const float sum = warp_sum(ex, 32);
+    const float vk1 = __shfl_sync(0xffffffffu, mv, K - 1);
+    const float vk = __shfl_sync(0xffffffffu, mv, K < 32 ? K : 0);
+    if (lane < K) {
+        ridx[((size_t)set * depth + tgt) * K + lane] = mi;
+        rw[((size_t)set * depth + tgt) * K + lane] = ex / sum;
+    }
+    if (lane == 0) rmargin[(size_t)set * depth + tgt] = K < E ? vk1 - vk : INFINITY;
 }
 
 // ---------------------------------------------------------------- A work split
-// Units: the gate/up row pairs of every slot (slot-major, P bytes each), then
-// (if the head runs) the fc1 rows and the l rows (R bytes each).  CTA c takes
-// the units that start in its byte range [c T / n, (c + 1) T / n).
+// CTA c takes an even share of the gate/up row pairs of every slot
+// (slot-major, P bytes each) and an even share of the head rows (fc1 rows,
+// then l rows, R bytes each; none when the head does not run): the same mix
+// of work on every CTA.  Its units, in order: its pairs, then its head rows.
 struct ASplit {
-    long long gu_units, total, P, R;
-    __host__ __device__ long long start(long long u) const {
-        return u < gu_units ? u * P : gu_units * P + (u - gu_units) * R;
-    }
-    __host__ __device__ long long first_at(long long b) const {   // first unit starting at >= b
-        if (b <= gu_units * P) return (b + P - 1) / P;
-        return gu_units + (b - gu_units * P + R - 1) / R;
-    }
-    __host__ __device__ void range(int c, int n, long long &u0, long long &u1) const {
-        u0 = first_at(total * c / n);
-        u1 = first_at(total * (c + 1) / n);
+    long long gu_units, P, R;
+    int head_rows;
+    __host__ __device__ void range(int c, int n, long long &g0, long long &g1, int &r0, int &r1) const {
+        g0 = gu_units * c / n;
+        g1 = gu_units * (c + 1) / n;
+        r0 = (int)((long long)head_rows * c / n);
+        r1 = (int)((long long)head_rows * (c + 1) / n);
     }
 };
 
@@ -257,7 +385,7 @@ __host__ __device__ inline ASplit a_split(int S, int F, int H, int E, int head, 
     s.gu_units = (long long)S * F;
     s.P = 2LL * rec_d;
     s.R = rec_dh;
-    s.total = s.gu_units * s.P + (head ? (long long)(H + E) * s.R : 0);
+    s.head_rows = head ? H + E : 0;
     return s;
 }
 
@@ -274,14 +402,17 @@ __device__ __forceinline__ const uint8_t *slot_blob(const CP &p, const int32_t *
 
 // ---------------------------------------------------------------- kernel A
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_constant__ CP p) {
+__global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_constant__ CP p) {
     constexpr int VALS = 128 / BITS;
     extern __shared__ __align__(128) uint8_t sm[];
     const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const ASplit sp = a_split(p.S, p.F, p.H, p.E, p.head, p.rec_d, p.rec_dh);
-    long long u0, u1;
-    sp.range(c, p.n_cta, u0, u1);
-    const uint32_t wbytes = (uint32_t)(sp.start(u1) - sp.start(u0));
+    long long g0, g1;
+    int r0, r1;
+    sp.range(c, p.n_cta, g0, g1, r0, r1);
+    const int ng = (int)(g1 - g0), nh = r1 - r0;
+    const uint32_t gbytes = (uint32_t)(ng * sp.P);
+    const uint32_t wbytes = gbytes + (uint32_t)(nh * sp.R);
     // shared memory: weights, x, chunk sums of x (4-bit chunks for the head),
     // table sums of the head rows, LoRA v, misc
     uint8_t *wts = sm;
@@ -294,8 +425,18 @@ __global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_const
     if (BITS != 4) off += padded(p.d, 32) * 4;
     float *xs4 = reinterpret_cast<float *>(sm + off);         // 4-bit chunks (head rows)
     off += (size_t)(p.d / 32) * 4;
-    const long long h0 = u0 > sp.gu_units ? u0 : sp.gu_units;  // first head unit
-    const int nh = u1 > h0 ? (int)(u1 - h0) : 0;
+    uint8_t *xf = sm + off;                                   // x as fixed point (BITS chunks)
+    off += fix_bytes(p.d, BITS);
+    float *xsc = reinterpret_cast<float *>(sm + off);
+    off += (size_t)(p.d / VALS) * 4;
+    float *xhat = reinterpret_cast<float *>(sm + off);
+    off += (size_t)(p.d / VALS) * 4;
+    uint8_t *xf4 = BITS == 4 ? xf : sm + off;                 // ... and in 4-bit chunks (head)
+    if (BITS != 4) off += fix_bytes(p.d, 4);
+    float *xsc4 = BITS == 4 ? xsc : reinterpret_cast<float *>(sm + off);
+    if (BITS != 4) off += (size_t)(p.d / 32) * 4;
+    float *xhat4 = BITS == 4 ? xhat : reinterpret_cast<float *>(sm + off);
+    if (BITS != 4) off += (size_t)(p.d / 32) * 4;
     float *tsum = reinterpret_cast<float *>(sm + off);
     off += (size_t)(nh + 1) * 4;
     float *tterm = reinterpret_cast<float *>(sm + off);       // [nh][2K + 1] table terms
@@ -304,6 +445,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_const
     off += 2 * kMaxR * 4;
     float *vwarp = reinterpret_cast<float *>(sm + off);       // per-warp sums of the partials
     off += kWarps * 32 * 4;
+    // the shared expert's gate / up B rows of this CTA's units of that slot
+    const int gs = p.S - 1;
+    const long long f_lo = max(g0, (long long)gs * p.F), f_hi = min(g1, (long long)(gs + 1) * p.F);
+    const int nlf = p.gu_lora && f_hi > f_lo ? (int)(f_hi - f_lo) : 0;
+    float *bgu = reinterpret_cast<float *>(sm + off);         // [nlf][2 kMaxR]
+    off += (size_t)(nlf * 2 * kMaxR + 1) * 4;
     float *red = reinterpret_cast<float *>(sm + off);
     off += 32 * 4;
     int32_t *route = reinterpret_cast<int32_t *>(sm + off);
@@ -311,39 +458,30 @@ __global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_const
     off = (off + 7) / 8 * 8;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + off);
 
+    stamp(p, 0);
     const int32_t *rcur = p.ridx + ((size_t)p.cur * p.depth + p.N) * p.K;
     const int32_t *rprv = p.ridx + ((size_t)p.prv * p.depth + p.N) * p.K;
     auto issue = [&]() {
-        // the unit range's segments: per slot a run of pairs, fc1 rows, l rows
+        // segments: per slot a run of pairs, then fc1 rows, then l rows
         if (threadIdx.x == 0) {
             bool bad = false;
             bar_expect(bar, wbytes);
             uint32_t at = 0;
-            long long u = u0;
-            while (u < u1) {
-                const uint8_t *src;
-                long long n;
-                if (u < sp.gu_units) {
-                    const int s = (int)(u / p.F), f = (int)(u % p.F);
-                    n = (long long)min((long long)(p.F - f), u1 - u);
-                    src = slot_blob(p, route, s, bad) + p.gu_off + (size_t)f * sp.P;
-                    n *= sp.P;
-                } else {
-                    const long long r = u - sp.gu_units;
-                    if (r < p.H) {
-                        const long long m = min((long long)p.H - r, u1 - u);
-                        src = p.L.fc1x + (size_t)r * sp.R;
-                        n = m * sp.R;
-                    } else {
-                        const long long m = u1 - u;
-                        src = p.L.lx + (size_t)(r - p.H) * sp.R;
-                        n = m * sp.R;
-                    }
-                }
-                bulk_copy(wts + at, src, (uint32_t)n, bar);
-                at += (uint32_t)n;
-                u = sp.first_at(sp.start(u) + n);
+            for (long long u = g0; u < g1;) {
+                const int s = (int)(u / p.F), f = (int)(u % p.F);
+                const long long n = min((long long)(p.F - f), g1 - u);
+                bulk_copy(wts + at, slot_blob(p, route, s, bad) + p.gu_off + (size_t)f * sp.P,
+                          (uint32_t)(n * sp.P), bar);
+                at += (uint32_t)(n * sp.P);
+                u += n;
             }
+            const int f1 = min(r1, p.H);
+            if (f1 > r0) {
+                bulk_copy(wts + at, p.L.fc1x + (size_t)r0 * sp.R, (uint32_t)((f1 - r0) * sp.R), bar);
+                at += (uint32_t)((f1 - r0) * sp.R);
+            }
+            const int l0 = max(r0, p.H);
+            if (r1 > l0) bulk_copy(wts + at, p.L.lx + (size_t)(l0 - p.H) * sp.R, (uint32_t)((r1 - l0) * sp.R), bar);
             if (bad) atomicExch(p.err, MOE_EINVAL);
         }
     };
@@ -359,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_const
         const int nt = 2 * p.K + 1;
         for (int it = threadIdx.x; it < nh * nt; it += blockDim.x) {
             const int i = it / nt, j = it - i * nt;
-            const long long r = h0 - sp.gu_units + i;
+            const int r = r0 + i;
             const bool fc1 = r < p.H;
             const int row = fc1 ? (int)r : (int)(r - p.H);
             const int width = fc1 ? p.H : p.E;
@@ -382,41 +520,50 @@ __global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_const
         }
     };
     if (!p.route_late) tables();
+    // B rows of the shared gate / up adapters for this CTA's rows of that slot
+    for (int it = threadIdx.x; it < nlf * 2 * kMaxR; it += blockDim.x) {
+        const int i = it / (2 * kMaxR), k = it - i * 2 * kMaxR;
+        const int f = (int)(f_lo - (long long)gs * p.F) + i, rg = p.L.sr[0], ru = p.L.sr[1];
+        float v = 0.0f;
+        if (k < rg) v = half_at(p.L.sb[0], (size_t)f * rg + k);
+        else if (k < rg + ru) v = half_at(p.L.sb[1], (size_t)f * ru + (k - rg));
+        bgu[it] = v;
+    }
     grid_launch_dependents();
     grid_wait();
+    stamp(p, 1);
+    // the partials of the shared gate/up LoRA's A x: loads first (they
+    // overlap the staging of x)
+    const bool lora_here = nlf > 0;
+    constexpr int kPer = 16;                    // up to 256 CTAs
+    float vpl[kPer];
+    if (lora_here) {
+#pragma unroll
+        for (int j = 0; j < kPer; j++) {
+            const int q = warp + j * kWarps;
+            vpl[j] = q < p.n_cta ? p.vp[(size_t)q * 2 * kMaxR + lane] : 0.0f;
+        }
+    }
     if (p.route_late) {
         if (threadIdx.x < p.K) route[threadIdx.x] = rcur[threadIdx.x];
         __syncthreads();
         issue();
         tables();
     }
-    // head N-1's route (the next token's route of layer N)
-    if (c == 0 && warp == kWarps - 1 && p.topk_z)
-        warp_route(p.topk_z, p.E, p.K, p.ridx, p.rw, p.rmargin, p.topk_set, p.depth, p.topk_tgt);
     // x and its chunk sums; 1/rms when x is an out
     const float ss = stage_vec(p.x_in, p.d, VALS, x, xs, red);
-    if (BITS == 4) {
-        for (int ch = threadIdx.x; ch < p.d / 32; ch += blockDim.x) xs4[ch] = xs[ch];
-    } else {
-        stage_vec(p.x_in, p.d, 32, x4, xs4, red);
-    }
+    if (BITS != 4) stage_vec(p.x_in, p.d, 32, x4, xs4, red);
+    stage_fix<BITS>(x, p.d, xf, xsc, xhat);
+    if (BITS != 4) stage_fix<4>(x4, p.d, xf4, xsc4, xhat4);
     const float inv = p.x_is_out ? 1.0f / sqrtf(ss / p.d + 1e-6f) : 1.0f;
-    // the shared expert's gate/up LoRA: A x from the previous layer's partials
-    const int gs = p.S - 1;
-    const bool lora_here = p.gu_lora && u0 < (long long)(gs + 1) * p.F && u1 > (long long)gs * p.F;
+    stamp(p, 3);
+    // the shared expert's gate/up LoRA: A x from the previous layer's
+    // partials (warp w summed CTAs w, w + kWarps, ... in order; warp 0 sums
+    // the warps')
     if (lora_here) {
-        // warp w sums the partials of CTAs w, w + kWarps, ... (loads first,
-        // then the sum in order), then warp 0 the warps' sums
-        constexpr int kPer = 16;                    // up to 256 CTAs
-        float v[kPer];
-#pragma unroll
-        for (int j = 0; j < kPer; j++) {
-            const int q = warp + j * kWarps;
-            v[j] = q < p.n_cta ? p.vp[(size_t)q * 2 * kMaxR + lane] : 0.0f;
-        }
         float a = 0.0f;
 #pragma unroll
-        for (int j = 0; j < kPer; j++) a += v[j];
+        for (int j = 0; j < kPer; j++) a += vpl[j];
         vwarp[warp * 32 + lane] = a;
     }
     __syncthreads();
@@ -427,24 +574,30 @@ __global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_const
     }
     __syncthreads();
     if (!bar_wait(bar, p.err)) return;
-    // units: warp w takes u0 + w, u0 + w + kWarps, ...
-    for (long long u = u0 + warp; u < u1; u += kWarps) {
-        const uint8_t *rec = wts + (sp.start(u) - sp.start(u0));
-        if (u < sp.gu_units) {
+    // units v = w, w + kWarps, ... of the CTA's list (its pairs, then its head rows)
+    stamp(p, 4);
+    for (int v = warp; v < ng + nh; v += kWarps) {
+        const uint8_t *rec = wts + (v < ng ? (size_t)v * sp.P : gbytes + (size_t)(v - ng) * sp.R);
+        const long long u = v < ng ? g0 + v : sp.gu_units + r0 + (v - ng);
+        if (v < ng) {
             const int s = (int)(u / p.F), f = (int)(u % p.F);
-            float gg = warp_sum(rec_dot<BITS>(rec, p.d, x, xs, lane), 32) * inv;
-            float uu = warp_sum(rec_dot<BITS>(rec + p.rec_d, p.d, x, xs, lane), 32) * inv;
+            float gu[2];
+            fix_dot<BITS, 2>(rec, p.rec_d, p.d, xf, xsc, xhat, lane, gu);
+            float gg = warp_sum(gu[0], 32) * inv;
+            float uu = warp_sum(gu[1], 32) * inv;
             if (s == gs && p.gu_lora) {
-                const int rg = p.L.sr[0], ru = p.L.sr[1];
-                float a = lane < rg ? half_at(p.L.sb[0], (size_t)f * rg + lane) * vx[lane] : 0.0f;
-                float b = lane < ru ? half_at(p.L.sb[1], (size_t)f * ru + lane) * vx[rg + lane] : 0.0f;
-                gg += p.L.ss[0] * warp_sum(a, 32);
-                uu += p.L.ss[1] * warp_sum(b, 32);
+                // lane k < rg: gate term k; rg <= k < rg + ru: up term k - rg
+                const int rg = p.L.sr[0];
+                const float t = bgu[(size_t)(u - f_lo) * 2 * kMaxR + lane] * vx[lane];
+                gg += p.L.ss[0] * warp_sum(lane < rg ? t : 0.0f, 32);
+                uu += p.L.ss[1] * warp_sum(lane < rg ? 0.0f : t, 32);
             }
             if (lane == 0) p.h[(size_t)s * p.F + f] = silu_f(gg) * uu;
         } else {
             const long long r = u - sp.gu_units;
-            const float a = warp_sum(rec_dot<4>(rec, p.d, x4, xs4, lane), 32) * inv + tsum[u - h0];
+            float hd[1];
+            fix_dot<4, 1>(rec, 0, p.d, xf4, xsc4, xhat4, lane, hd);
+            const float a = warp_sum(hd[0], 32) * inv + tsum[v - ng];
             if (lane == 0) {
                 if (r < p.H) p.g[r] = gelu_erf_f(a);
                 else if (p.H > 0) p.zl[r - p.H] = a;
@@ -452,12 +605,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_a_kernel(const __grid_const
             }
         }
     }
+    stamp(p, 6);
+    if (p.trace) __syncthreads();          // debug: the stamp marks the whole CTA's end
+    stamp(p, 2);
 }
 
 // ---------------------------------------------------------------- kernel B
 // Output rows [o0, o1) and logit rows [e0, e1) of CTA c (even splits).
 template <int BITS>
-__global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_constant__ CP p) {
+__global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_constant__ CP p) {
     constexpr int VALS = 128 / BITS;
     extern __shared__ __align__(128) uint8_t sm[];
     const int c = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -478,6 +634,18 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
     off += (p.H > 0 ? padded(p.H, 32) : 1) * 4;
     float *gsum = reinterpret_cast<float *>(sm + off);        // [H / 32]
     off += (size_t)(p.H > 0 ? p.H / 32 : 1) * 4;
+    uint8_t *hf = sm + off;                                   // h as fixed point per chunk
+    off += fix_bytes(p.S * p.F, BITS);
+    float *hsc = reinterpret_cast<float *>(sm + off);
+    off += (size_t)(p.S * p.F / VALS) * 4;
+    float *hhat = reinterpret_cast<float *>(sm + off);
+    off += (size_t)(p.S * p.F / VALS) * 4;
+    uint8_t *gf = sm + off;                                   // g as fixed point (4-bit chunks)
+    off += p.H > 0 ? fix_bytes(p.H, 4) : 16;
+    float *gsc = reinterpret_cast<float *>(sm + off);
+    off += (size_t)(p.H > 0 ? p.H / 32 : 1) * 4;
+    float *ghat = reinterpret_cast<float *>(sm + off);
+    off += (size_t)(p.H > 0 ? p.H / 32 : 1) * 4;
     float *vd = reinterpret_cast<float *>(sm + off);          // [S][kMaxR] down LoRA A_d h
     off += (size_t)p.S * kMaxR * 4;
     // the down adapters' A (fp16 [r][F] per adapter slot), copied with the weights
@@ -490,6 +658,14 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
     off += (size_t)2 * kMaxR * (no + 1) * 4;
     float *outs = reinterpret_cast<float *>(sm + off);        // [no] this CTA's out rows
     off += (size_t)(no + 1) * 4;
+    float *resid = reinterpret_cast<float *>(sm + off);       // [no] residual rows
+    off += (size_t)(no + 1) * 4;
+    float *zls = reinterpret_cast<float *>(sm + off);         // [ne] l f rows
+    off += (size_t)(ne + 1) * 4;
+    float *b2s = reinterpret_cast<float *>(sm + off);         // [ne] fc2 bias rows
+    off += (size_t)(ne + 1) * 4;
+    float *bdn = reinterpret_cast<float *>(sm + off);         // [S][no][kMaxR] down B rows
+    off += (size_t)p.S * (no + 1) * kMaxR * 4;
     float *wk = reinterpret_cast<float *>(sm + off);          // combine weights
     off += (kMaxK + 1) * 4;
     int32_t *route = reinterpret_cast<int32_t *>(sm + off);
@@ -499,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
     off = (off + 7) / 8 * 8;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + off);
 
+    stamp(p, 0);
     const int32_t *rcur = p.ridx + ((size_t)p.cur * p.depth + p.N) * p.K;
     const float *wcur = p.rw + ((size_t)p.cur * p.depth + p.N) * p.K;
     auto issue = [&]() {
@@ -530,6 +707,26 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
     }
     __syncthreads();
     if (!p.route_late) issue();
+    // fc2 biases, down B rows of this CTA's outputs (the routed adapters' need
+    // the route: with it, or after the wait)
+    auto load_b = [&]() {
+        for (int it = threadIdx.x; it < p.S * no * kMaxR; it += blockDim.x) {
+            const int s = it / (no * kMaxR), rem = it - s * no * kMaxR, i = rem / kMaxR, k = rem - i * kMaxR;
+            const bool shared = s >= p.K;
+            const int r = shared ? p.L.sr[2] : p.L.r_d;
+            float v = 0.0f;
+            if (k < r) {
+                const int e = shared ? 0 : route[s];
+                if (shared || (unsigned)e < (unsigned)p.E) {
+                    const uint16_t *B = shared ? p.L.sb[2] : p.L.lb_d + (size_t)e * p.L.lb_ds;
+                    v = half_at(B, (size_t)(o0 + i) * r + k);
+                }
+            }
+            bdn[it] = v;
+        }
+    };
+    for (int i = threadIdx.x; i < ne; i += blockDim.x) b2s[i] = p.L.b2 ? half_at(p.L.b2, e0 + i) : 0.0f;
+    if (!p.route_late) load_b();
     // the next layer's gate/up A columns of this CTA's rows (static data)
     const int r2n = p.vp_next ? p.nr[0] + p.nr[1] : 0;
     for (int it = threadIdx.x; it < r2n * no; it += blockDim.x) {
@@ -539,6 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
     }
     grid_launch_dependents();
     grid_wait();
+    stamp(p, 1);
     if (p.route_late) {
         if (threadIdx.x < p.K) {
             route[threadIdx.x] = rcur[threadIdx.x];
@@ -546,10 +744,24 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
         }
         __syncthreads();
         issue();
+        load_b();
     }
-    // h of every slot with its chunk sums; g (head fc2 input) with 4-bit chunk sums
-    stage_vec(p.h, p.S * p.F, VALS, hs, hsum, red);
-    if (p.head && p.H > 0) stage_vec(p.g, p.H, 32, gs, gsum, red);
+    // h of every slot, g (head fc2 input), this CTA's residual rows and l f
+    // rows: every load issued before any is used
+    float4 hv[kMaxHPass], gv[1];
+    load_vec<kMaxHPass>(p.h, p.S * p.F, hv);
+    const bool gh = p.head && p.H > 0;
+    if (gh) load_vec<1>(p.g, p.H, gv);
+    float resv = 0.0f, zlv = 0.0f;
+    if (threadIdx.x < no) resv = p.x_in[o0 + threadIdx.x];
+    if (threadIdx.x >= 32 && threadIdx.x < 32 + ne) zlv = p.zl[e0 + threadIdx.x - 32];
+    store_vec<kMaxHPass>(hv, p.S * p.F, VALS, hs, hsum);
+    if (gh) store_vec<1>(gv, p.H, 32, gs, gsum);
+    if (threadIdx.x < no) resid[threadIdx.x] = resv;
+    if (threadIdx.x >= 32 && threadIdx.x < 32 + ne) zls[threadIdx.x - 32] = zlv;
+    __syncthreads();
+    stage_fix<BITS>(hs, p.S * p.F, hf, hsc, hhat);
+    if (p.head && p.H > 0) stage_fix<4>(gs, p.H, gf, gsc, ghat);
     __syncthreads();
     if (!bar_wait(bar, p.err)) return;
     // down LoRA: vd[s][k] = A_d[k] h_s (routed adapter slots, then the shared
@@ -579,26 +791,26 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
         for (int q = lane; q < npair; q += 32) {
             const int s = q / cps, ch = q - s * cps;
             const uint8_t *rec = wts + (size_t)s * dbytes + (size_t)i * p.rec_F;
-            const uint4 w4 = *reinterpret_cast<const uint4 *>(rec + (size_t)kChunk * ch);
+            const uint4 w4[1] = {*reinterpret_cast<const uint4 *>(rec + (size_t)kChunk * ch)};
             const float2 sb = sb_f(*reinterpret_cast<const uint32_t *>(rec + cb + 4 * ((ch * VALS) / kGroup)));
-            const float y = fmaf(sb.x, chunk_dot<BITS>(w4, hs + (size_t)(s * cps + ch) * (VALS + 1)),
-                                 sb.y * hsum[s * cps + ch]);
+            int dq[1];
+            const int hc = s * cps + ch;
+            chunk_dot_fix<BITS, 1>(w4, reinterpret_cast<const uint4 *>(hf), npair, hc, dq);
+            const float y = fmaf(sb.x, (float)dq[0] * hsc[hc], sb.y * hhat[hc]);
             acc = fmaf(s < p.K ? wk[s] : 1.0f, y, acc);
         }
-        // down LoRA: lane k < r of each adapter slot
+        // down LoRA: lane k < r of each adapter slot (B rows from shared memory)
         for (int s = 0; s < p.S; s++) {
             const bool shared = s >= p.K;
             const int r = shared ? p.L.sr[2] : p.L.r_d;
             if (r == 0 || lane >= r) continue;
-            const int e = shared ? 0 : route[s];
-            if (!shared && (unsigned)e >= (unsigned)p.E) continue;
-            const uint16_t *B = shared ? p.L.sb[2] : p.L.lb_d + (size_t)e * p.L.lb_ds;
             const float sc = shared ? p.L.ss[2] : p.L.s_d;
-            acc = fmaf((shared ? 1.0f : wk[s]) * sc, half_at(B, (size_t)o * r + lane) * vd[s * kMaxR + lane], acc);
+            acc = fmaf((shared ? 1.0f : wk[s]) * sc,
+                       bdn[((size_t)s * no + i) * kMaxR + lane] * vd[s * kMaxR + lane], acc);
         }
         acc = warp_sum(acc, 32);
         if (lane == 0) {
-            const float v = p.x_in[o] + acc;
+            const float v = resid[i] + acc;
             outs[i] = v;
             p.out[o] = v;
         }
@@ -607,8 +819,12 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
     for (int i = warp; i < ne; i += kWarps) {
         const int e = e0 + i;
         float a = 0.0f;
-        if (p.H > 0) a = warp_sum(rec_dot<4>(wts + (size_t)p.S * dbytes + (size_t)i * p.rec_H, p.H, gs, gsum, lane), 32);
-        if (lane == 0) p.z[e] = a + (p.L.b2 ? half_at(p.L.b2, e) : 0.0f) + p.zl[e];
+        if (p.H > 0) {
+            float f2[1];
+            fix_dot<4, 1>(wts + (size_t)p.S * dbytes + (size_t)i * p.rec_H, 0, p.H, gf, gsc, ghat, lane, f2);
+            a = warp_sum(f2[0], 32);
+        }
+        if (lane == 0) p.z[e] = a + b2s[i] + zls[i];
     }
     // the next layer's gate/up LoRA partial over this CTA's rows of out
     if (p.vp_next) {
@@ -620,6 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_b_kernel(const __grid_const
             p.vp_next[(size_t)c * 2 * kMaxR + lane] = a;
         }
     }
+    if (p.trace) __syncthreads();          // debug: the stamp marks the whole CTA's end
+    stamp(p, 2);
 }
 
 // ---------------------------------------------------------------- router kernel
@@ -632,7 +850,9 @@ __global__ void __launch_bounds__(kThreads, 1) chain_r_kernel(const __grid_const
     float *x = reinterpret_cast<float *>(sm);                 // padded per 4-bit chunk
     float *xs = x + padded(p.d, 32);
     float *red = xs + p.d / 32;
+    stamp(p, 0);
     grid_wait();
+    stamp(p, 1);
     stage_vec(p.x_in, p.d, 32, x, xs, red);
     __syncthreads();
     if (do_router) {
@@ -654,10 +874,33 @@ __global__ void __launch_bounds__(kThreads, 1) chain_r_kernel(const __grid_const
     }
 }
 
+// The next token's routes from every head of the step: warp w of CTA b
+// ranks head N = b * kWarps + w (heads 0 .. n_heads - 1; head N's logits at
+// z + N * E, its target layer N + 1, or 0 for the last one).
+__global__ void __launch_bounds__(kThreads) chain_rank_kernel(const __grid_constant__ CP p,
+                                                              const float *z, int n_heads) {
+    stamp(p, 0);
+    grid_wait();
+    stamp(p, 1);
+    const int N = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (N < n_heads) {
+        Logits zv;
+        load_logits(z + (size_t)N * p.E, p.E, zv);
+        warp_route(zv, p.E, p.K, p.ridx, p.rw, p.rmargin, p.topk_set, p.depth,
+                   N + 1 < p.depth ? N + 1 : 0);
+    }
+    stamp(p, 2);
+}
+
 // One warp: the route of layer tgt from logits z.
 __global__ void __launch_bounds__(32) chain_topk_kernel(const __grid_constant__ CP p) {
+    stamp(p, 0);
     grid_wait();
-    warp_route(p.topk_z, p.E, p.K, p.ridx, p.rw, p.rmargin, p.topk_set, p.depth, p.topk_tgt);
+    stamp(p, 1);
+    Logits zv;
+    load_logits(p.topk_z, p.E, zv);
+    warp_route(zv, p.E, p.K, p.ridx, p.rw, p.rmargin, p.topk_set, p.depth, p.topk_tgt);
+    stamp(p, 2);
 }
 
 }  // namespace chain
@@ -742,15 +985,18 @@ static void smem_need(const Shapes &s, int n_cta, size_t *sa, size_t *sb) {
     for (int head = 0; head < 2; head++) {
         const ASplit sp = a_split(s.S, s.F, s.H, s.E, head, rec_d, rec_dh);
         for (int c = 0; c < n_cta; c++) {
-            long long u0, u1;
-            sp.range(c, n_cta, u0, u1);
-            const size_t wb = (size_t)(sp.start(u1) - sp.start(u0));
-            const long long h0 = u0 > sp.gu_units ? u0 : sp.gu_units;
-            const size_t nh = u1 > h0 ? (size_t)(u1 - h0) : 0;
+            long long g0, g1;
+            int r0, r1;
+            sp.range(c, n_cta, g0, g1, r0, r1);
+            const size_t wb = (size_t)((g1 - g0) * sp.P + (long long)(r1 - r0) * sp.R);
+            const size_t nh = (size_t)(r1 - r0);
             size_t need = (wb + 127) / 128 * 128 + padded(s.d, VALS) * 4 + (size_t)(s.d / VALS) * 4 +
                           (s.bits != 4 ? padded(s.d, 32) * 4 : 0) +
+                          fix_bytes(s.d, s.bits) + (size_t)(s.d / VALS) * 8 +
+                          (s.bits != 4 ? fix_bytes(s.d, 4) + (size_t)(s.d / 32) * 8 : 0) +
                           (size_t)(s.d / 32) * 4 + (nh + 1) * 4 + (nh * (2 * s.K + 1) + 1) * 4 +
-                          2 * kMaxR * 4 + kWarps * 32 * 4 + 32 * 4 + (kMaxK + 1) * 4 + 16;
+                          2 * kMaxR * 4 + kWarps * 32 * 4 + ((wb / sp.P + 2) * 2 * kMaxR + 1) * 4 +
+                          32 * 4 + (kMaxK + 1) * 4 + 16;
             if (need > a) a = need;
         }
     }
@@ -758,9 +1004,13 @@ static void smem_need(const Shapes &s, int n_cta, size_t *sa, size_t *sb) {
     *sa = a;
     *sb = ((size_t)s.S * no * rec_F + (size_t)ne * rec_H + 127) / 128 * 128 + padded(s.S * s.F, VALS) * 4 +
           (size_t)s.S * (s.F / VALS) * 4 + (s.H > 0 ? padded(s.H, 32) : 1) * 4 +
-          (size_t)(s.H > 0 ? s.H / 32 : 1) * 4 + (size_t)s.S * kMaxR * 4 +
+          (size_t)(s.H > 0 ? s.H / 32 : 1) * 4 + fix_bytes(s.S * s.F, s.bits) +
+          (size_t)(s.S * s.F / VALS) * 8 + (s.H > 0 ? fix_bytes(s.H, 4) : 16) +
+          (size_t)(s.H > 0 ? s.H / 32 : 1) * 8 + (size_t)s.S * kMaxR * 4 +
           ((size_t)(s.K * s.rd_routed + s.rd_shared) * s.F * 2 + 15) / 16 * 16 +
-          (size_t)2 * kMaxR * (no + 1) * 4 + (size_t)(no + 1) * 4 + 2 * (kMaxK + 1) * 4 + 32 * 4 + 16;
+          (size_t)2 * kMaxR * (no + 1) * 4 + (size_t)(no + 1) * 12 + (size_t)(ne + 1) * 8 +
+          (size_t)s.S * (no + 1) * kMaxR * 4 +
+          2 * (kMaxK + 1) * 4 + 32 * 4 + 16;
 }
 
 static CLayer layer_of(const moe_stack_desc *sd, int N, const Shapes &s) {
@@ -865,6 +1115,8 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
     b.rw = rw;
     b.rmargin = rmargin;
     b.err = err;
+    b.trace = sd->debug_trace;
+    int lid = 0;
     const moe_experts_desc &e0 = sd->experts[0];
     b.gu_lora = e0.shared && (e0.shared_lora[0].r || e0.shared_lora[1].r);
     auto next_lora = [&](CP &p, int M) {       // layer M's shared gate / up A, its partials
@@ -881,6 +1133,7 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
     if (s.own0 || b.gu_lora) {
         CP p = b;
         p.N = 0;
+        p.launch_id = lid++;
         p.L = layer_of(sd, 0, s);
         p.x_in = x0;
         next_lora(p, 0);
@@ -894,6 +1147,7 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
         first = false;
         if (s.own0) {
             CP q = b;
+            q.launch_id = lid++;
             q.topk_z = zr;
             q.topk_set = cur;
             q.topk_tgt = 0;
@@ -915,24 +1169,30 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
         p.z = z + (size_t)N * s.E;
         p.vp = vp + (size_t)N * vps;
         next_lora(p, N + 1);
-        // A ranks head N - 1's logits: the next token's route of layer N
-        if (N >= 1 && head_runs(s, N - 1)) {
-            p.topk_z = z + (size_t)(N - 1) * s.E;
-            p.topk_set = nxt;
-            p.topk_tgt = N;
-        }
+        p.launch_id = lid++;
         if (int rc = launch(chain_a_kernel<BITS>, p, n_cta, kThreads, sa, !first, st, "A")) return rc;
         first = false;
-        p.topk_z = nullptr;
+        p.launch_id = lid++;
         if (int rc = launch(chain_b_kernel<BITS>, p, n_cta, kThreads, sb, true, st, "B")) return rc;
     }
-    // the last head (a single self-predicting layer: its own next route)
-    if (head_runs(s, s.depth - 1)) {
+    // the next token's routes: every head that ran (heads 0 .. depth - 2, and
+    // the last one for a single self-predicting layer)
+    const int n_heads = head_runs(s, s.depth - 1) ? s.depth : s.depth - 1;
+    if (n_heads > 0) {
         CP q = b;
-        q.topk_z = z + (size_t)(s.depth - 1) * s.E;
+        q.launch_id = lid++;
         q.topk_set = nxt;
-        q.topk_tgt = 0;
-        if (int rc = launch(chain_topk_kernel, q, 1, 32, 0, true, st, "last head top-K")) return rc;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((n_heads + kWarps - 1) / kWarps);
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, chain_rank_kernel, q, (const float *)z, n_heads);
+        if (e != cudaSuccess) return fail(MOE_ECUDA, "decode_step_chain: ranking launch: %s", cudaGetErrorString(e));
     }
     return MOE_OK;
 }
@@ -965,6 +1225,12 @@ extern "C" int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, 
     const chain::Shapes s = chain::shapes_of(sd);
     if (s.d % 256 && s.bits == 2)
         return fail(MOE_EUNSUPPORTED, "decode_step_chain: 2-bit needs d a multiple of 256");
+    const int n = chain::sms_of_device();
+    if (n <= 0) return fail(MOE_ECUDA, "decode_step_chain: no device");
+    if ((long long)s.S * s.F > (long long)chain::kMaxHPass * chain::kThreads * 4 ||
+        (s.d + n - 1) / n > chain::kThreads || (s.E + n - 1) / n > chain::kThreads - 32)
+        return fail(MOE_EUNSUPPORTED, "decode_step_chain: slots x F = %d x %d (or d, E) too large "
+                                      "for %d SMs", s.S, s.F, n);
     uint8_t *w = static_cast<uint8_t *>(ws);
     return s.bits == 4 ? chain::run<4>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream)
                        : chain::run<2>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream);
