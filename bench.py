@@ -44,8 +44,10 @@ def parse():
     ap.add_argument("--cpu-layers", type=int, default=40,
                     help="layer samples the oracle baseline times (native arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="fused", choices=["fused", "per-call"],
-                    help="fused: one persistent kernel per step; per-call: the four calls per layer")
+    ap.add_argument("--path", default="chain", choices=["chain", "fused", "per-call"],
+                    help="chain: two kernels per layer chained by programmatic dependent "
+                         "launch; fused: one persistent kernel per step; per-call: the "
+                         "four calls per layer")
     return ap.parse_args()
 
 
@@ -58,18 +60,21 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def measured_traffic(layers: int):
-    """DRAM bytes (read + write) of one fused decode-step launch over `layers`
-    layers, scaled from the ncu capture summarised in
-    profiles/decode_step_35b_L4.md; None when the kernel's sources have
-    changed since that capture."""
+def measured_traffic(layers: int, path: str):
+    """DRAM bytes (read + write) of one whole decode step over `layers`
+    layers on `path` ("fused" or "chain"), scaled from the ncu capture of the
+    4-layer stack summarised under profiles/ (per-layer bytes x layers + the
+    step's fixed launches); None when the kernel sources have changed since
+    that capture."""
     import hashlib
     import re
-    p = os.path.join(ROOT, "profiles", "decode_step_35b_L4.md")
-    if not os.path.exists(p):
+    name = {"fused": "decode_step_35b_L4.md", "chain": "decode_chain_35b_L4.md"}.get(path)
+    p = os.path.join(ROOT, "profiles", name) if name else ""
+    if not p or not os.path.exists(p):
         return None
     text = open(p).read()
     per_layer = re.search(r"traffic_bytes_per_layer: (\d+)", text)
+    fixed = re.search(r"traffic_bytes_fixed: (\d+)", text)
     files = re.search(r"kernel_sources: (.+)", text)
     digest = re.search(r"kernel_sources_sha256_16: ([0-9a-f]+)", text)
     if not (per_layer and files and digest):
@@ -79,7 +84,7 @@ def measured_traffic(layers: int):
         h.update(open(os.path.join(ROOT, "int4_expert_gemv_gb300", "csrc", f), "rb").read())
     if h.hexdigest()[:16] != digest.group(1):
         return None
-    return int(per_layer.group(1)) * layers
+    return int(per_layer.group(1)) * layers + (int(fixed.group(1)) if fixed else 0)
 
 
 # ---------------------------------------------------------------- clocks
@@ -208,9 +213,16 @@ def run_reference(args, cfg):
 def kernels_per_step(cfg, stack) -> int:
     """Kernel launches of one steady-state step (counted from the calls the
     driver makes; the kernels per call are fixed by the library)."""
+    ed = stack.m.layers[0]["experts_desc"]
+    if stack.chain:
+        # layer-0 router (+ its top-K) when layer 0 routes itself or the shared
+        # expert carries a gate/up adapter, A and B per layer, one ranking launch
+        sh_gu = cfg.shared and any(ed.shared_lora[i].r for i in range(2))
+        n = (1 if (not cfg.self_predict or sh_gu) else 0) + (0 if cfg.self_predict else 1)
+        heads = cfg.depth if cfg.self_predict else cfg.depth - 1
+        return n + 2 * cfg.depth + (1 if heads > 0 else 0)
     if stack.fused:
         return 1
-    ed = stack.m.layers[0]["experts_desc"]
     gu_lora = any(ed.lora[i].r for i in range(2)) or any(ed.shared_lora[i].r for i in range(2))
     ffn = 2 + (1 if gu_lora else 0)
     head = 1 + (1 if cfg.H else 0)
@@ -241,7 +253,7 @@ def run_native(args, cfg):
     __graft_entry__.build()
 
     dm = DeviceModel(cfg)
-    st = DecodeStack(dm, fused=args.path == "fused")
+    st = DecodeStack(dm, fused={"chain": "chain", "fused": True, "per-call": False}[args.path])
     total = args.warmup + args.steps
     xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
                                        (total + 64, cfg.d), 1.0)).cuda()
@@ -304,9 +316,13 @@ def run_native(args, cfg):
         launch_ms += [a.elapsed_time(b) for a, b in evs]
     st.t = t_next + n_inst
     launch_avg_ms = statistics.mean(launch_ms)
-    # algorithmic bytes of one launch: the experts a launch reads
+    # algorithmic bytes of one timed unit: the expert weights it reads (the
+    # chain's unit is the whole step -- events between its PDL-chained kernels
+    # would serialise them -- and adds the head weights its kernels stream)
     unit_layers = cfg.depth if st.fused else 1
     launch_bytes = cfg.expert_bytes_per_layer() * unit_layers
+    if st.chain:
+        launch_bytes += dm.head_bytes_per_token() * cfg.depth
 
     # ---- end to end: host input -> device, step, result -> host, per step
     pin_in = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 1),
@@ -335,8 +351,13 @@ def run_native(args, cfg):
         expert_gbs = ffn_bytes * cfg.depth / (ms_step / 1000.0) / 1e9
         achieved = launch_bytes / (launch_avg_ms / 1000.0) / 1e9
         head_bytes = dm.head_bytes_per_token()
-        kname = ("decode_step_kernel (whole step: experts, combine, heads, top-K)" if st.fused
-                 else "moe_expert_ffn_int4 (gate/up+SwiGLU, down)")
+        if st.chain:
+            kname = ("chain_a_kernel + chain_b_kernel (whole step: experts, combine, heads; "
+                     f"{kernels_per_step(cfg, st)} PDL-chained launches)")
+        elif st.fused:
+            kname = "decode_step_kernel (whole step: experts, combine, heads, top-K)"
+        else:
+            kname = "moe_expert_ffn_int4 (gate/up+SwiGLU, down)"
         line = {
             "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -359,11 +380,14 @@ def run_native(args, cfg):
             "roofline": {"bound": "hbm", "kernel": kname,
                          "achieved": achieved, "peak": hbm, "peak_kind": hbm_kind,
                          "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": measured_traffic(cfg.depth) if st.fused else None,
+                         "traffic": measured_traffic(cfg.depth, args.path)
+                         if st.fused else None,
                          "bytes_per_launch": launch_bytes,
                          "avg_launch_us": launch_avg_ms * 1000.0,
-                         "timing": f"CUDA events around each layer's call in {n_inst} "
-                                   f"instrumented graph replays after the timed region"},
+                         "timing": (f"CUDA events around each whole step in {n_inst} "
+                                    if st.fused else
+                                    f"CUDA events around each layer's call in {n_inst} ")
+                              + "instrumented graph replays after the timed region"},
             "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "tokens/s",
                     "h2d_bytes_per_step": cfg.d * 4, "d2h_bytes_per_step": cfg.d * 4},
             "gpu_launches": kernels_per_step(cfg, st) * args.steps,

@@ -285,9 +285,13 @@ typedef struct {
     int debug_unset_wait;             /* test hook: 1 makes the kernel wait on
                                          a flag nothing sets (-> MOE_ETIMEOUT) */
     unsigned long long *debug_trace;  /* profiling hook: NULL, or a device
-                                         buffer of n_SM * depth * 16 u64 that
-                                         receives %globaltimer stamps per CTA
-                                         and layer at phase boundaries        */
+                                         buffer of %globaltimer stamps.
+                                         moe_decode_step: n_SM * depth * 16
+                                         u64, per CTA and layer at phase
+                                         boundaries.  moe_decode_step_chain:
+                                         2048 + 65536 u64, 8 stamps of CTA 0
+                                         per launch, then every CTA's end
+                                         (256 per launch)                     */
     unsigned inflight_bytes;          /* tuning: weight-copy bytes in flight
                                          per SM (0 = 32 KiB; at least 16 KiB) */
 } moe_stack_desc;

@@ -35,6 +35,7 @@ namespace chain {
 using step::chunk_dot_fix;
 using step::Fix;
 using step::stage_chunk;
+using step::fix_place;
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
@@ -136,6 +137,15 @@ __device__ __forceinline__ void stamp(const CP &p, int k) {
         unsigned long long t;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
         p.trace[(size_t)p.launch_id * 8 + k] = t;
+    }
+}
+
+// Debug: every CTA's end, after 256 launches x 8 stamps of CTA 0.
+__device__ __forceinline__ void stamp_end(const CP &p) {
+    if (p.trace && threadIdx.x == 0 && blockIdx.x < 256) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        p.trace[2048 + (size_t)p.launch_id * 256 + blockIdx.x] = t;
     }
 }
 
@@ -249,6 +259,62 @@ __device__ __forceinline__ void stage_fix(const float *xp, int n, uint8_t *xf, f
 #pragma unroll
         for (int m = 0; m < PER; m++) v[m] = xp[c * (VALS + 1) + lane + 32 * m];
         stage_chunk<BITS>(v, lane, xf, c, nch, xsc, xhat);
+    }
+}
+
+// One pass of stage_fix straight from registers: thread i holds positions
+// 4i .. 4i+3 of the vector (v), the 128 / BITS / 4 consecutive lanes of a
+// chunk find its max |x| and sum with shuffles, and each lane writes its four
+// fixed-point values (same scale, rounding and layout as stage_chunk).  Every
+// lane of the warp calls it (in: whether position 4i exists).
+template <int BITS>
+__device__ __forceinline__ void quant4(const float4 &v, int i, bool in, uint8_t *xf, int nch,
+                                       float *xsc, float *xhat) {
+    constexpr int VALS = 128 / BITS, PER = VALS / 4;
+    uint32_t mb = max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
+                      max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w))));
+#pragma unroll
+    for (int o = 1; o < PER; o <<= 1) mb = max(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const bool nz = (mb >> 23) != 0;
+    const int e = nz ? (int)((mb >> 23) & 0xff) - 126 : 0;
+    const float f = nz ? __uint_as_float((uint32_t)(127 + 15 - e) << 23) : 0.0f;
+    int q[4];
+    const float vv[4] = {v.x, v.y, v.z, v.w};
+    int sum = 0;
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+        q[k] = max(-32767, min(32767, (int)rintf(vv[k] * f)));
+        sum += q[k];
+    }
+#pragma unroll
+    for (int o = 1; o < PER; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (!in) return;
+    const int c = (4 * i) / VALS, pos = 4 * i - c * VALS;
+    if (BITS == 4) {
+        // positions 8j + 4b + {0..3}: (q0, q2) are high/low bytes 2b, 2b+1 of
+        // the A words, (q1, q3) of the B words
+        const int j = pos >> 3, b = (pos >> 2) & 1;
+        uint8_t *w = xf + ((size_t)j * nch + c) * 16 + 2 * b;
+        const auto hi = [](int x) { return (uint32_t)((x >> 8) & 0xff); };
+        const auto lo = [](int x) { return (uint32_t)(x & 0xff); };
+        *reinterpret_cast<uint16_t *>(w) = (uint16_t)(hi(q[0]) | hi(q[2]) << 8);
+        *reinterpret_cast<uint16_t *>(w + 4) = (uint16_t)(lo(q[0]) | lo(q[2]) << 8);
+        *reinterpret_cast<uint16_t *>(w + 8) = (uint16_t)(hi(q[1]) | hi(q[3]) << 8);
+        *reinterpret_cast<uint16_t *>(w + 12) = (uint16_t)(lo(q[1]) | lo(q[3]) << 8);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+            int slot, byte;
+            fix_place<BITS>(pos + k, slot, byte);
+            uint8_t *w = xf + ((size_t)slot * nch + c) * 16;
+            w[byte] = (uint8_t)((q[k] >> 8) & 0xff);
+            w[byte + 4] = (uint8_t)(q[k] & 0xff);
+        }
+    }
+    if ((i & (PER - 1)) == 0) {
+        const float sc = nz ? __uint_as_float((uint32_t)(127 + e - 15) << 23) : 0.0f;
+        xsc[c] = sc;
+        xhat[c] = (float)sum * sc;
     }
 }
 
@@ -413,18 +479,10 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
     const int ng = (int)(g1 - g0), nh = r1 - r0;
     const uint32_t gbytes = (uint32_t)(ng * sp.P);
     const uint32_t wbytes = gbytes + (uint32_t)(nh * sp.R);
-    // shared memory: weights, x, chunk sums of x (4-bit chunks for the head),
-    // table sums of the head rows, LoRA v, misc
+    // shared memory: weights, x as fixed point (and in 4-bit chunks for the
+    // head), table sums of the head rows, LoRA v, misc
     uint8_t *wts = sm;
     size_t off = (wbytes + 127) / 128 * 128;
-    float *x = reinterpret_cast<float *>(sm + off);          // padded per BITS chunk
-    off += padded(p.d, VALS) * 4;
-    float *xs = reinterpret_cast<float *>(sm + off);          // BITS chunks
-    off += (size_t)(p.d / VALS) * 4;
-    float *x4 = BITS == 4 ? x : reinterpret_cast<float *>(sm + off);   // padded per 4-bit chunk (head)
-    if (BITS != 4) off += padded(p.d, 32) * 4;
-    float *xs4 = reinterpret_cast<float *>(sm + off);         // 4-bit chunks (head rows)
-    off += (size_t)(p.d / 32) * 4;
     uint8_t *xf = sm + off;                                   // x as fixed point (BITS chunks)
     off += fix_bytes(p.d, BITS);
     float *xsc = reinterpret_cast<float *>(sm + off);
@@ -550,12 +608,19 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
         issue();
         tables();
     }
-    // x and its chunk sums; 1/rms when x is an out
-    const float ss = stage_vec(p.x_in, p.d, VALS, x, xs, red);
-    if (BITS != 4) stage_vec(p.x_in, p.d, 32, x4, xs4, red);
-    stage_fix<BITS>(x, p.d, xf, xsc, xhat);
-    if (BITS != 4) stage_fix<4>(x4, p.d, xf4, xsc4, xhat4);
-    const float inv = p.x_is_out ? 1.0f / sqrtf(ss / p.d + 1e-6f) : 1.0f;
+    // x as fixed point straight from the loads; per-warp sums of x^2 (1/rms
+    // when x is an out, summed over the warps in order after the barrier)
+    float ss = 0.0f;
+    for (int base = 0; base < p.d / 4; base += blockDim.x) {     // uniform over the block
+        const int i = base + threadIdx.x;
+        const bool in = i < p.d / 4;
+        const float4 v = in ? reinterpret_cast<const float4 *>(p.x_in)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        quant4<BITS>(v, i, in, xf, p.d / VALS, xsc, xhat);
+        if (BITS != 4) quant4<4>(v, i, in, xf4, p.d / 32, xsc4, xhat4);
+    }
+    ss = warp_sum(ss, 32);
+    if (lane == 0) red[warp] = ss;
     stamp(p, 3);
     // the shared expert's gate/up LoRA: A x from the previous layer's
     // partials (warp w summed CTAs w, w + kWarps, ... in order; warp 0 sums
@@ -567,6 +632,12 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
         vwarp[warp * 32 + lane] = a;
     }
     __syncthreads();
+    float inv = 1.0f;
+    if (p.x_is_out) {
+        float t = 0.0f;
+        for (int w = 0; w < kWarps; w++) t += red[w];
+        inv = 1.0f / sqrtf(t / p.d + 1e-6f);
+    }
     if (lora_here && warp == 0) {
         float a = 0.0f;
         for (int w = 0; w < kWarps; w++) a += vwarp[w * 32 + lane];
@@ -608,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
     stamp(p, 6);
     if (p.trace) __syncthreads();          // debug: the stamp marks the whole CTA's end
     stamp(p, 2);
+    stamp_end(p);
 }
 
 // ---------------------------------------------------------------- kernel B
@@ -626,14 +698,8 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
     const uint32_t fbytes = p.H ? (uint32_t)ne * p.rec_H : 0u;
     uint8_t *wts = sm;                                        // [S][no] down records, then fc2 rows
     size_t off = ((size_t)p.S * dbytes + fbytes + 127) / 128 * 128;
-    float *hs = reinterpret_cast<float *>(sm + off);          // [S][F] padded per chunk
+    float *hs = reinterpret_cast<float *>(sm + off);          // [S][F] padded per chunk (LoRA)
     off += padded(p.S * p.F, VALS) * 4;
-    float *hsum = reinterpret_cast<float *>(sm + off);        // [S][F / VALS]
-    off += (size_t)p.S * (p.F / VALS) * 4;
-    float *gs = reinterpret_cast<float *>(sm + off);          // [H] padded per 4-bit chunk
-    off += (p.H > 0 ? padded(p.H, 32) : 1) * 4;
-    float *gsum = reinterpret_cast<float *>(sm + off);        // [H / 32]
-    off += (size_t)(p.H > 0 ? p.H / 32 : 1) * 4;
     uint8_t *hf = sm + off;                                   // h as fixed point per chunk
     off += fix_bytes(p.S * p.F, BITS);
     float *hsc = reinterpret_cast<float *>(sm + off);
@@ -670,8 +736,6 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
     off += (kMaxK + 1) * 4;
     int32_t *route = reinterpret_cast<int32_t *>(sm + off);
     off += (kMaxK + 1) * 4;
-    float *red = reinterpret_cast<float *>(sm + off);
-    off += 32 * 4;
     off = (off + 7) / 8 * 8;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + off);
 
@@ -755,15 +819,32 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
     float resv = 0.0f, zlv = 0.0f;
     if (threadIdx.x < no) resv = p.x_in[o0 + threadIdx.x];
     if (threadIdx.x >= 32 && threadIdx.x < 32 + ne) zlv = p.zl[e0 + threadIdx.x - 32];
-    store_vec<kMaxHPass>(hv, p.S * p.F, VALS, hs, hsum);
-    if (gh) store_vec<1>(gv, p.H, 32, gs, gsum);
+    // fixed point straight from the loads (h also padded as floats, for the
+    // down LoRA)
+    const int nh4 = p.S * p.F / 4;
+#pragma unroll
+    for (int k = 0; k < kMaxHPass; k++) {
+        if (k * (int)blockDim.x >= nh4) break;                   // whole block: uniform
+        const int i = k * blockDim.x + threadIdx.x;
+        const bool in = i < nh4;
+        if (in) {
+            const int ch = (4 * i) / VALS;
+            float *d = hs + ch * (VALS + 1) + (4 * i - ch * VALS);
+            d[0] = hv[k].x;
+            d[1] = hv[k].y;
+            d[2] = hv[k].z;
+            d[3] = hv[k].w;
+        }
+        quant4<BITS>(hv[k], i, in, hf, p.S * p.F / VALS, hsc, hhat);
+    }
+    stamp(p, 7);
+    if (gh) quant4<4>(gv[0], threadIdx.x, (int)threadIdx.x < p.H / 4, gf, p.H / 32, gsc, ghat);
     if (threadIdx.x < no) resid[threadIdx.x] = resv;
     if (threadIdx.x >= 32 && threadIdx.x < 32 + ne) zls[threadIdx.x - 32] = zlv;
     __syncthreads();
-    stage_fix<BITS>(hs, p.S * p.F, hf, hsc, hhat);
-    if (p.head && p.H > 0) stage_fix<4>(gs, p.H, gf, gsc, ghat);
-    __syncthreads();
+    stamp(p, 3);
     if (!bar_wait(bar, p.err)) return;
+    stamp(p, 4);
     // down LoRA: vd[s][k] = A_d[k] h_s (routed adapter slots, then the shared
     // one), one (slot, k) row per warp, A from shared memory
     {
@@ -776,12 +857,14 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
             const uint16_t *A = adn + (size_t)it * p.F;
             float a = 0.0f;
             const float *hrow = hs + (size_t)s * (p.F / VALS) * (VALS + 1);
+#pragma unroll 4
             for (int f = lane; f < p.F; f += 32) a = fmaf(half_f(A[f]), hrow[f + f / VALS], a);
             a = warp_sum(a, 32);
             if (lane == 0) vd[s * kMaxR + k] = (!shared && (unsigned)route[s] >= (unsigned)p.E) ? 0.0f : a;
         }
     }
     __syncthreads();
+    stamp(p, 5);
     // out rows: warp per row; lanes over the (slot, chunk) pairs
     const int cps = p.F / VALS, npair = p.S * cps;
     const size_t cb = code_bytes(p.F, BITS);
@@ -815,8 +898,10 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
             p.out[o] = v;
         }
     }
-    // head N's fc2 rows: z = fc2 g + b2 + l f
-    for (int i = warp; i < ne; i += kWarps) {
+    stamp(p, 6);
+    // head N's fc2 rows: z = fc2 g + b2 + l f (row i on warp (no + i) mod
+    // 16: the warps without an out row first)
+    for (int i = (warp - no % kWarps + kWarps) % kWarps; i < ne; i += kWarps) {
         const int e = e0 + i;
         float a = 0.0f;
         if (p.H > 0) {
@@ -838,6 +923,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
     }
     if (p.trace) __syncthreads();          // debug: the stamp marks the whole CTA's end
     stamp(p, 2);
+    stamp_end(p);
 }
 
 // ---------------------------------------------------------------- router kernel
@@ -990,11 +1076,10 @@ static void smem_need(const Shapes &s, int n_cta, size_t *sa, size_t *sb) {
             sp.range(c, n_cta, g0, g1, r0, r1);
             const size_t wb = (size_t)((g1 - g0) * sp.P + (long long)(r1 - r0) * sp.R);
             const size_t nh = (size_t)(r1 - r0);
-            size_t need = (wb + 127) / 128 * 128 + padded(s.d, VALS) * 4 + (size_t)(s.d / VALS) * 4 +
-                          (s.bits != 4 ? padded(s.d, 32) * 4 : 0) +
+            size_t need = (wb + 127) / 128 * 128 +
                           fix_bytes(s.d, s.bits) + (size_t)(s.d / VALS) * 8 +
                           (s.bits != 4 ? fix_bytes(s.d, 4) + (size_t)(s.d / 32) * 8 : 0) +
-                          (size_t)(s.d / 32) * 4 + (nh + 1) * 4 + (nh * (2 * s.K + 1) + 1) * 4 +
+                          (nh + 1) * 4 + (nh * (2 * s.K + 1) + 1) * 4 +
                           2 * kMaxR * 4 + kWarps * 32 * 4 + ((wb / sp.P + 2) * 2 * kMaxR + 1) * 4 +
                           32 * 4 + (kMaxK + 1) * 4 + 16;
             if (need > a) a = need;
@@ -1003,14 +1088,13 @@ static void smem_need(const Shapes &s, int n_cta, size_t *sa, size_t *sb) {
     const int no = (s.d + n_cta - 1) / n_cta, ne = (s.E + n_cta - 1) / n_cta;
     *sa = a;
     *sb = ((size_t)s.S * no * rec_F + (size_t)ne * rec_H + 127) / 128 * 128 + padded(s.S * s.F, VALS) * 4 +
-          (size_t)s.S * (s.F / VALS) * 4 + (s.H > 0 ? padded(s.H, 32) : 1) * 4 +
-          (size_t)(s.H > 0 ? s.H / 32 : 1) * 4 + fix_bytes(s.S * s.F, s.bits) +
+          fix_bytes(s.S * s.F, s.bits) +
           (size_t)(s.S * s.F / VALS) * 8 + (s.H > 0 ? fix_bytes(s.H, 4) : 16) +
           (size_t)(s.H > 0 ? s.H / 32 : 1) * 8 + (size_t)s.S * kMaxR * 4 +
           ((size_t)(s.K * s.rd_routed + s.rd_shared) * s.F * 2 + 15) / 16 * 16 +
           (size_t)2 * kMaxR * (no + 1) * 4 + (size_t)(no + 1) * 12 + (size_t)(ne + 1) * 8 +
           (size_t)s.S * (no + 1) * kMaxR * 4 +
-          2 * (kMaxK + 1) * 4 + 32 * 4 + 16;
+          2 * (kMaxK + 1) * 4 + 16;
 }
 
 static CLayer layer_of(const moe_stack_desc *sd, int N, const Shapes &s) {
@@ -1078,8 +1162,18 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
         return fail(MOE_EUNSUPPORTED, "decode_step_chain: %zu / %zu bytes of shared memory (at most %d)",
                     sa, sb, smem_max);
     const size_t sr = padded(s.d, 32) * 4 + (size_t)(s.d / 32) * 4 + 32 * 4 + 16;
+    // every kernel of the chain asks for the same (largest) shared-memory
+    // carveout: an SM only holds CTAs of one carveout at a time, and a kernel
+    // with a smaller one would wait for the SM to drain instead of starting
+    // beside its predecessor
+    const int co = cudaSharedmemCarveoutMaxShared;
     if (cudaFuncSetAttribute(chain_a_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa) != cudaSuccess ||
-        cudaFuncSetAttribute(chain_b_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb) != cudaSuccess)
+        cudaFuncSetAttribute(chain_b_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_a_kernel<BITS>, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_b_kernel<BITS>, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_r_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_rank_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess)
         return fail(MOE_ECUDA, "decode_step_chain: shared-memory attribute");
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     if (cudaMemsetAsync(err, 0, sizeof(int32_t), st) != cudaSuccess)
