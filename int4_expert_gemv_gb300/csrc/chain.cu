@@ -358,39 +358,59 @@ __device__ __forceinline__ float half_at(const uint16_t *p, size_t i) { return h
 
 // Ranks E <= 1024 logits (value desc, index asc; NaN last) in one warp:
 // route of layer tgt in set `set` (indices, softmax weights over the kept K,
-// margin z_(K) - z_(K+1)).  Lane l holds logits l, l + 32, ... (vals, loaded
-// by load_logits); each lane keeps its best remaining one, every round takes
-// the warp's best of those (ties: lower index) and only the winning lane
-// rescans.  The k-th winner ends in lane k (registers only).
+// margin z_(K) - z_(K+1)).  Lane l holds logits l, l + 32, ..., NV of them
+// (NV * 32 >= E); each lane keeps its best remaining one (a pairwise tree
+// over its values), every round takes the warp's best of those (ties: lower
+// index) and only the winning lane rescans.  The k-th winner ends in lane k
+// (registers only).
+template <int NV>
 struct Logits {
-    float v[32];
+    float v[NV];
 };
 
-__device__ __forceinline__ void load_logits(const float *z, int E, Logits &L) {
+template <int NV>
+__device__ __forceinline__ void load_logits(const float *z, int E, Logits<NV> &L) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < 32; i++) {
+    for (int i = 0; i < NV; i++) {
         const int e = lane + 32 * i;
         const float x = e < E ? z[e] : -INFINITY;
         L.v[i] = x == x ? x : -INFINITY;
     }
 }
 
-__device__ void warp_route(const Logits &L, int E, int K, int32_t *ridx, float *rw, float *rmargin,
-                           int set, int depth, int tgt) {
+// (value, index) a ranks before b
+__device__ __forceinline__ bool ranks_before(float av, int ai, float bv, int bi) {
+    return av > bv || (av == bv && ai < bi);
+}
+
+template <int NV>
+__device__ void warp_route(const Logits<NV> &L, int E, int K, int32_t *ridx, float *rw,
+                           float *rmargin, int set, int depth, int tgt) {
     const int lane = threadIdx.x & 31;
     uint32_t taken = 0;
+    // this lane's best remaining entry: taken and absent entries become
+    // (-inf, INT_MAX), after every real one
     auto best_of_lane = [&](float &bv, int &bi) {
-        bv = -INFINITY;
-        bi = 0x7fffffff;
+        float tv[NV];
+        int ti[NV];
 #pragma unroll
-        for (int i = 0; i < 32; i++) {
+        for (int i = 0; i < NV; i++) {
             const int e = lane + 32 * i;
-            if (e < E && !(taken >> i & 1u) && (L.v[i] > bv || (L.v[i] == bv && e < bi))) {
-                bv = L.v[i];
-                bi = e;
-            }
+            const bool ok = e < E && !(taken >> i & 1u);
+            tv[i] = ok ? L.v[i] : -INFINITY;
+            ti[i] = ok ? e : 0x7fffffff;
         }
+#pragma unroll
+        for (int w = 1; w < NV; w <<= 1)
+#pragma unroll
+            for (int i = 0; i + w < NV; i += 2 * w)
+                if (ranks_before(tv[i + w], ti[i + w], tv[i], ti[i])) {
+                    tv[i] = tv[i + w];
+                    ti[i] = ti[i + w];
+                }
+        bv = tv[0];
+        bi = ti[0];
     };
     float lv, mv = -INFINITY;       // this lane's best remaining; my winner's value (lane k)
     int li, mi = 0;
@@ -402,7 +422,7 @@ __device__ void warp_route(const Logits &L, int E, int K, int32_t *ridx, float *
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
             const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
+            if (ranks_before(ov, oi, bv, bi)) {
                 bv = ov;
                 bi = oi;
             }
@@ -427,6 +447,23 @@ __device__ void warp_route(const Logits &L, int E, int K, int32_t *ridx, float *
         rw[((size_t)set * depth + tgt) * K + lane] = ex / sum;
     }
     if (lane == 0) rmargin[(size_t)set * depth + tgt] = K < E ? vk1 - vk : INFINITY;
+}
+
+// The route of layer tgt from the E logits at z, by one warp.
+__device__ __forceinline__ void route_one(const CP &p, const float *z, int set, int tgt) {
+    if (p.E <= 256) {
+        Logits<8> zv;
+        load_logits(z, p.E, zv);
+        warp_route(zv, p.E, p.K, p.ridx, p.rw, p.rmargin, set, p.depth, tgt);
+    } else if (p.E <= 512) {
+        Logits<16> zv;
+        load_logits(z, p.E, zv);
+        warp_route(zv, p.E, p.K, p.ridx, p.rw, p.rmargin, set, p.depth, tgt);
+    } else {
+        Logits<32> zv;
+        load_logits(z, p.E, zv);
+        warp_route(zv, p.E, p.K, p.ridx, p.rw, p.rmargin, set, p.depth, tgt);
+    }
 }
 
 // ---------------------------------------------------------------- A work split
@@ -547,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
     if (threadIdx.x < p.K && !p.route_late) route[threadIdx.x] = rcur[threadIdx.x];
     __syncthreads();
     if (!p.route_late) issue();
+    stamp(p, 5);
     // table sums of this CTA's head rows (the routes of layer N at t and t - 1)
     auto tables = [&]() {
         // item (row i, term j): j < K the current route's table row, then the
@@ -579,14 +617,16 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
     };
     if (!p.route_late) tables();
     // B rows of the shared gate / up adapters for this CTA's rows of that slot
-    for (int it = threadIdx.x; it < nlf * 2 * kMaxR; it += blockDim.x) {
-        const int i = it / (2 * kMaxR), k = it - i * 2 * kMaxR;
+    // (entries 0..31 of a row: lane k reads entry k)
+    for (int it = threadIdx.x; it < nlf * 32; it += blockDim.x) {
+        const int i = it >> 5, k = it & 31;
         const int f = (int)(f_lo - (long long)gs * p.F) + i, rg = p.L.sr[0], ru = p.L.sr[1];
         float v = 0.0f;
         if (k < rg) v = half_at(p.L.sb[0], (size_t)f * rg + k);
         else if (k < rg + ru) v = half_at(p.L.sb[1], (size_t)f * ru + (k - rg));
-        bgu[it] = v;
+        bgu[(size_t)i * 2 * kMaxR + k] = v;
     }
+    stamp(p, 7);
     grid_launch_dependents();
     grid_wait();
     stamp(p, 1);
@@ -651,18 +691,19 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
         const uint8_t *rec = wts + (v < ng ? (size_t)v * sp.P : gbytes + (size_t)(v - ng) * sp.R);
         const long long u = v < ng ? g0 + v : sp.gu_units + r0 + (v - ng);
         if (v < ng) {
-            const int s = (int)(u / p.F), f = (int)(u % p.F);
+            const int s = (int)u / p.F, f = (int)u - s * p.F;
             float gu[2];
             fix_dot<BITS, 2>(rec, p.rec_d, p.d, xf, xsc, xhat, lane, gu);
-            float gg = warp_sum(gu[0], 32) * inv;
-            float uu = warp_sum(gu[1], 32) * inv;
+            float a0 = gu[0] * inv, a1 = gu[1] * inv;
             if (s == gs && p.gu_lora) {
                 // lane k < rg: gate term k; rg <= k < rg + ru: up term k - rg
+                // (added to the lanes' partials: one sum per projection)
                 const int rg = p.L.sr[0];
                 const float t = bgu[(size_t)(u - f_lo) * 2 * kMaxR + lane] * vx[lane];
-                gg += p.L.ss[0] * warp_sum(lane < rg ? t : 0.0f, 32);
-                uu += p.L.ss[1] * warp_sum(lane < rg ? 0.0f : t, 32);
+                a0 = fmaf(p.L.ss[0], lane < rg ? t : 0.0f, a0);
+                a1 = fmaf(p.L.ss[1], lane < rg ? 0.0f : t, a1);
             }
+            const float gg = warp_sum(a0, 32), uu = warp_sum(a1, 32);
             if (lane == 0) p.h[(size_t)s * p.F + f] = silu_f(gg) * uu;
         } else {
             const long long r = u - sp.gu_units;
@@ -773,20 +814,19 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
     if (!p.route_late) issue();
     // fc2 biases, down B rows of this CTA's outputs (the routed adapters' need
     // the route: with it, or after the wait)
+    // (only the slots with an adapter, k < r: the only entries read)
     auto load_b = [&]() {
-        for (int it = threadIdx.x; it < p.S * no * kMaxR; it += blockDim.x) {
-            const int s = it / (no * kMaxR), rem = it - s * no * kMaxR, i = rem / kMaxR, k = rem - i * kMaxR;
+        for (int s = 0; s < p.S; s++) {
             const bool shared = s >= p.K;
             const int r = shared ? p.L.sr[2] : p.L.r_d;
-            float v = 0.0f;
-            if (k < r) {
-                const int e = shared ? 0 : route[s];
-                if (shared || (unsigned)e < (unsigned)p.E) {
-                    const uint16_t *B = shared ? p.L.sb[2] : p.L.lb_d + (size_t)e * p.L.lb_ds;
-                    v = half_at(B, (size_t)(o0 + i) * r + k);
-                }
+            if (r == 0) continue;
+            const int e = shared ? 0 : route[s];
+            const bool ok = shared || (unsigned)e < (unsigned)p.E;
+            const uint16_t *B = shared ? p.L.sb[2] : p.L.lb_d + (size_t)(ok ? e : 0) * p.L.lb_ds;
+            for (int it = threadIdx.x; it < no * r; it += blockDim.x) {
+                const int i = it / r, k = it - i * r;
+                bdn[((size_t)s * no + i) * kMaxR + k] = ok ? half_at(B, (size_t)(o0 + i) * r + k) : 0.0f;
             }
-            bdn[it] = v;
         }
     };
     for (int i = threadIdx.x; i < ne; i += blockDim.x) b2s[i] = p.L.b2 ? half_at(p.L.b2, e0 + i) : 0.0f;
@@ -961,20 +1001,17 @@ __global__ void __launch_bounds__(kThreads, 1) chain_r_kernel(const __grid_const
 }
 
 // The next token's routes from every head of the step: warp w of CTA b
-// ranks head N = b * kWarps + w (heads 0 .. n_heads - 1; head N's logits at
-// z + N * E, its target layer N + 1, or 0 for the last one).
-__global__ void __launch_bounds__(kThreads) chain_rank_kernel(const __grid_constant__ CP p,
-                                                              const float *z, int n_heads) {
+// ranks head N = b * kRankWarps + w (heads 0 .. n_heads - 1; head N's logits
+// at z + N * E, its target layer N + 1, or 0 for the last one).  Small CTAs,
+// so that they fit beside the last layer's kernel B.
+constexpr int kRankWarps = 4;
+__global__ void __launch_bounds__(kRankWarps * 32) chain_rank_kernel(const __grid_constant__ CP p,
+                                                                     const float *z, int n_heads) {
     stamp(p, 0);
     grid_wait();
     stamp(p, 1);
-    const int N = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    if (N < n_heads) {
-        Logits zv;
-        load_logits(z + (size_t)N * p.E, p.E, zv);
-        warp_route(zv, p.E, p.K, p.ridx, p.rw, p.rmargin, p.topk_set, p.depth,
-                   N + 1 < p.depth ? N + 1 : 0);
-    }
+    const int N = blockIdx.x * kRankWarps + (threadIdx.x >> 5);
+    if (N < n_heads) route_one(p, z + (size_t)N * p.E, p.topk_set, N + 1 < p.depth ? N + 1 : 0);
     stamp(p, 2);
 }
 
@@ -983,9 +1020,7 @@ __global__ void __launch_bounds__(32) chain_topk_kernel(const __grid_constant__ 
     stamp(p, 0);
     grid_wait();
     stamp(p, 1);
-    Logits zv;
-    load_logits(p.topk_z, p.E, zv);
-    warp_route(zv, p.E, p.K, p.ridx, p.rw, p.rmargin, p.topk_set, p.depth, p.topk_tgt);
+    route_one(p, p.topk_z, p.topk_set, p.topk_tgt);
     stamp(p, 2);
 }
 
@@ -1277,8 +1312,8 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
         q.launch_id = lid++;
         q.topk_set = nxt;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((n_heads + kWarps - 1) / kWarps);
-        cfg.blockDim = dim3(kThreads);
+        cfg.gridDim = dim3((n_heads + kRankWarps - 1) / kRankWarps);
+        cfg.blockDim = dim3(kRankWarps * 32);
         cfg.stream = st;
         cudaLaunchAttribute at[1];
         at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -1839,6 +1839,10 @@ static int check_stack(const moe_stack_desc *sd) {
                 (r1 && (!e.shared_lora[j].A || !e.shared_lora[j].B)))
                 return fail(MOE_EINVAL, "decode_step: LoRA with NULL A or B");
         }
+        // the shared gate and up adapters' A x share one 32-lane vector
+        if (e.shared && e.shared_lora[0].r + e.shared_lora[1].r > kMaxR)
+            return fail(MOE_EUNSUPPORTED, "decode_step: shared gate + up LoRA ranks %d + %d above %d",
+                        e.shared_lora[0].r, e.shared_lora[1].r, kMaxR);
         if (e.lora[0].r || e.lora[1].r)
             return fail(MOE_EUNSUPPORTED,
                         "decode_step: gate/up LoRA on routed experts runs through the per-call path");

@@ -173,3 +173,34 @@ def test_pack_rejects_bad_arguments(m):
     assert L.moe_pack_matrix(1 << 20, 1 << 20, 1 << 20, 4, 128, 4, (1 << 20) + 16, None) == m.MOE_EINVAL
     assert L.moe_pack_experts(2048, 512, 4, 4, *([1 << 20] * 9), 1 << 20, 4096, None) == m.MOE_EINVAL
     assert L.moe_debug_dequant(1 << 20, 2048, 512, 4, 3, 1 << 20, None) == m.MOE_EINVAL
+
+
+def _stack(m, shared_ranks, depth=1):
+    """A one-layer decode stack descriptor with placeholder device pointers
+    (validation runs before any pointer is used)."""
+    eds = (m.ExpertsDesc * 1)()
+    ed = eds[0]
+    ed.d, ed.F, ed.E, ed.bits = 2048, 512, 256, 4
+    ed.pool, ed.shared = 1 << 20, 1 << 21
+    ed.expert_stride = m.moe_pool_expert_bytes(2048, 512, 4, 64)
+    for j, r in enumerate(shared_ranks):
+        ed.shared_lora[j] = m.LoraDesc(r, 1.0, 1 << 20, 1 << 20, 0, 0) if r else m.LoraDesc()
+    rts = (m.HeadDesc * 1)()
+    rts[0].d, rts[0].E, rts[0].prec, rts[0].lx = 2048, 256, m.MOE_PREC_AFFINE4, 1 << 20
+    sd = m.StackDesc()
+    sd.experts, sd.routers = C.addressof(eds), C.addressof(rts)
+    sd.n_layers, sd.depth, sd.K = 1, depth, 4
+    return sd, (eds, rts)
+
+
+@pytest.mark.parametrize("entry", ["moe_decode_step", "moe_decode_step_chain"])
+def test_decode_step_rejects_wide_shared_gate_up_lora(m, entry):
+    """The shared expert's gate and up adapters share one 32-wide A x vector:
+    ranks 20 + 20 are refused before anything is enqueued; 16 + 16 gets past
+    the descriptor checks (to the NULL-pointer check that follows)."""
+    p = 1 << 20
+    for ranks, want in (((20, 20, 0), m.MOE_EUNSUPPORTED), ((16, 16, 0), m.MOE_EINVAL)):
+        sd, keep = _stack(m, ranks)
+        rc = getattr(m.lib(), entry)(C.byref(sd), p, None, p, p, p, 1, p, 1 << 30, None)
+        assert rc == want, (ranks, m.last_error())
+    assert "NULL" in m.last_error()
