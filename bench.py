@@ -37,7 +37,10 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=256)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps; default 2400 for the decode stack (about a second, "
+                         "so that the clock sampler sees it), 256 for a batched layer, 16 "
+                         "oracle layer passes for --impl reference")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="35b")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
@@ -103,7 +106,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -548,6 +551,8 @@ def main():
     args = parse()
     from int4_expert_gemv_gb300.configs import ALL
     cfg = ALL[args.config]
+    if args.steps is None:
+        args.steps = 16 if args.impl == "reference" else (256 if cfg.T > 1 else 2400)
     if args.impl == "reference":
         import oracle
         oracle.build()
