@@ -53,7 +53,8 @@ def _run(m, cfg, routes, x):
     ws = torch.empty(m.moe_expert_ffn_workspace_bytes(ed, T, K), dtype=torch.uint8, device="cuda")
     m.moe_expert_ffn_int4(ed, x, torch.from_numpy(routes).cuda(), T, K, y, ws)
     torch.cuda.synchronize()
-    assert ws[:4].view(torch.int32).item() == m.MOE_OK     # no bounded wait expired
+    if T > 1:      # the batched path's status word (the decode path has none)
+        assert ws[:4].view(torch.int32).item() == m.MOE_OK     # no bounded wait expired
     return y.cpu().double().numpy()
 
 
