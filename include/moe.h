@@ -327,19 +327,22 @@ int moe_decode_step_status(const void *ws, int *status, cudaStream_t stream);
 
 /* The same decode step as moe_decode_step (same arguments, routes, results
  * and step-0 rule), run as two kernels per layer chained by programmatic
- * dependent launch instead of one persistent kernel: kernel A takes a
- * byte-balanced share of every layer's gate/up row pairs and head rows per
- * SM (h, gelu(fc1 f), l f; the previous head's top-K), kernel B a share of the
- * output rows (the down GEMV of every slot, combine + residual, down LoRA), of
- * the head's fc2 logits and of the next layer's gate/up LoRA partials.  Each
- * kernel copies its weights into shared memory before it waits for the one
- * before (the step's routes are known when it starts).  No kernel waits on
- * another's CTAs: the only device-side wait is a CTA's on its own copies
- * (bounded; MOE_ETIMEOUT in the status word on expiry).
+ * dependent launch instead of one persistent kernel: kernel A takes an even
+ * share of every layer's gate/up row pairs and head rows per SM (h,
+ * gelu(fc1 f), l f), kernel B a share of the output rows (the down GEMV of
+ * every slot, combine + residual, down LoRA), of the head's fc2 logits and of
+ * the next layer's gate/up LoRA partials.  Each kernel copies its weights into
+ * shared memory before it waits for the one before (the step's routes are
+ * known when it starts).  The heads' top-K (the routes of t+1) run in one
+ * launch at the end of the step.  No kernel waits on another's CTAs: the only
+ * device-side wait is a CTA's on its own copies (bounded; MOE_ETIMEOUT in the
+ * status word on expiry).
  * ws: moe_decode_step_chain_workspace_bytes() bytes, 256-byte aligned (no
  * clearing needed); its status reads with moe_decode_step_status.  The step
- * enqueues 2 * depth (+ 2 for layer 0's own router, + 1 for the last head's
- * top-K) launches; under stream capture they form one graph. */
+ * enqueues 2 * depth launches, + 2 for layer 0's own router and its top-K
+ * (+ 1 for its router alone when only the shared expert's gate/up adapters
+ * need layer 0's partials), + 1 for the heads' top-K; under stream capture
+ * they form one graph. */
 size_t moe_decode_step_chain_workspace_bytes(const moe_stack_desc *sd);
 int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, float *out,
                           int32_t *route_idx, float *route_w, float *route_margin,
