@@ -34,7 +34,6 @@ namespace chain {
 
 using step::chunk_dot_fix;
 using step::Fix;
-using step::stage_chunk;
 using step::fix_place;
 
 constexpr int kThreads = 512;
@@ -210,10 +209,8 @@ __device__ __forceinline__ float stage_vec(const float *src, int n, int vals, fl
 
 __host__ __device__ inline size_t padded(int n, int vals) { return (size_t)(n / vals) * (vals + 1); }
 
-// stage_vec in two halves, so that several vectors' loads are in flight
-// together: load_vec issues this thread's float4 loads (at most MAXP passes of
-// the block), store_vec stores them padded with the per-chunk sums (as
-// stage_vec, without the sum of squares).
+// Issues this thread's float4 loads of an n-float vector (at most MAXP passes
+// of the block) so that several vectors' loads are in flight together.
 template <int MAXP>
 __device__ __forceinline__ void load_vec(const float *src, int n, float4 (&v)[MAXP]) {
 #pragma unroll
@@ -223,49 +220,13 @@ __device__ __forceinline__ void load_vec(const float *src, int n, float4 (&v)[MA
     }
 }
 
-template <int MAXP>
-__device__ __forceinline__ void store_vec(const float4 (&v)[MAXP], int n, int vals, float *dst,
-                                          float *sums) {
-    const int per = vals / 4;
-#pragma unroll
-    for (int k = 0; k < MAXP; k++) {
-        const int i = k * blockDim.x + threadIdx.x;
-        if (k * (int)blockDim.x >= n / 4) break;                 // whole block: uniform
-        const int c = (4 * i) / vals, j = 4 * i - c * vals;
-        if (i < n / 4) {
-            float *d = dst + c * (vals + 1) + j;
-            d[0] = v[k].x;
-            d[1] = v[k].y;
-            d[2] = v[k].z;
-            d[3] = v[k].w;
-        }
-        float a = (v[k].x + v[k].y) + (v[k].z + v[k].w);
-        for (int o = 1; o < per; o <<= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-        if (i < n / 4 && (i & (per - 1)) == 0) sums[c] = a;
-    }
-}
-
-// The vector staged padded by stage_vec (chunks of 128 / BITS values), again
-// as 16-bit fixed point per chunk for the dp4a dot (one chunk per warp pass;
-// layout and scales as the persistent decode kernel's): xf bytes, the chunk
-// scale 2^(e-15) and xhat = sum of the fixed-point values times the scale.
-template <int BITS>
-__device__ __forceinline__ void stage_fix(const float *xp, int n, uint8_t *xf, float *xsc,
-                                          float *xhat) {
-    constexpr int VALS = 128 / BITS, PER = VALS / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nch = n / VALS;
-    for (int c = warp; c < nch; c += kWarps) {
-        float v[PER];
-#pragma unroll
-        for (int m = 0; m < PER; m++) v[m] = xp[c * (VALS + 1) + lane + 32 * m];
-        stage_chunk<BITS>(v, lane, xf, c, nch, xsc, xhat);
-    }
-}
-
-// One pass of stage_fix straight from registers: thread i holds positions
-// 4i .. 4i+3 of the vector (v), the 128 / BITS / 4 consecutive lanes of a
-// chunk find its max |x| and sum with shuffles, and each lane writes its four
-// fixed-point values (same scale, rounding and layout as stage_chunk).  Every
+// Stages a vector as 16-bit fixed point per chunk of 128 / BITS values for
+// the dp4a dot, straight from registers: thread i holds positions 4i .. 4i+3
+// (v), the 128 / BITS / 4 consecutive lanes of a chunk find its max |x| and
+// its sum with shuffles, and each lane writes its four fixed-point values --
+// xf bytes in the layout chunk_dot_fix reads, the chunk scale 2^(e-15) and
+// xhat = sum of the fixed-point values times the scale (scale, rounding and
+// layout as the persistent decode kernel's stage_chunk).  Every
 // lane of the warp calls it (in: whether position 4i exists).
 template <int BITS>
 __device__ __forceinline__ void quant4(const float4 &v, int i, bool in, uint8_t *xf, int nch,
@@ -323,7 +284,7 @@ __host__ __device__ inline size_t fix_bytes(int n, int bits) {
 }
 
 // Dots of R consecutive records (rec0, rec0 + stride, ...; cols columns) with
-// a vector staged by stage_fix, over this lane's chunks (exact integer chunk
+// a vector staged by quant4, over this lane's chunks (exact integer chunk
 // dots, then fma(scale, dot * 2^(e-15), bias * xhat)).
 template <int BITS, int R>
 __device__ __forceinline__ void fix_dot(const uint8_t *rec0, uint32_t stride, int cols,
