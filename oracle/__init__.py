@@ -30,12 +30,13 @@ AFFINE, F16 = 0, 1
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so (gcc -O2, no fast-math)."""
+    """Compile oracle.c into liboracle.so (gcc -O2, no fast-math, no FMA
+    contraction: the binary32 merge relies on each operation rounding)."""
     newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= newest:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-std=c11", "-O2", "-fPIC", "-shared", "-Wall",
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall",
                     "-o", tmp, _SRC, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -116,6 +117,7 @@ def lib():
             L.orc_combine.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P, P, P]
             L.orc_stack_step.argtypes = [C.POINTER(Stack), C.POINTER(StackState),
                                          P, P, C.c_double, P, P, P, P, P]
+            L.orc_merge_lora.argtypes = [C.POINTER(Mat), C.POINTER(Lora), P, P, P]
             _lib = L
     return _lib
 
@@ -222,6 +224,19 @@ def gemv(m: dict, x) -> np.ndarray:
     y = np.zeros(st.rows, np.float64)
     lib().orc_gemv(C.byref(st), _p(x), _p(y))
     return y
+
+
+def merge_lora(m: dict, l: dict | None) -> dict:
+    """W' = requantise(W + scale B A) group by group, in binary32 (oracle.h:
+    orc_merge_lora); returns a matrix dict of m's shape.  l None: W requantised."""
+    keep = _Keep()
+    st, sl = mat(keep, m), lora(keep, l)
+    q = np.zeros((st.rows, st.cols * st.bits // 32), np.uint32)
+    s = np.zeros((st.rows, st.cols // st.group), np.uint16)
+    b = np.zeros_like(s)
+    lib().orc_merge_lora(C.byref(st), C.byref(sl), _p(q), _p(s), _p(b))
+    return {"q": q, "s": s, "b": b, "rows": st.rows, "cols": st.cols, "bits": st.bits,
+            "group": st.group}
 
 
 def lora_apply(l: dict, x, y) -> np.ndarray:

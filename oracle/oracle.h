@@ -202,6 +202,26 @@ void orc_stack_step(const orc_stack *st, orc_stack_state *state,
                     double *used_margin /* [L] or NULL                    */,
                     uint8_t *forced     /* [L] or NULL                    */);
 
+/* ---- merging a LoRA delta into the quantised weights ---------------------
+ * The alternative to the unfused adapter: W' = requantise(W + (alpha/r) B A),
+ * group by group, in the same affine form (the pages run the adapter unfused
+ * because merging and requantising keeps only a small part of its delta:
+ * "Ejecucion del adaptador no fusionado", xyznot.com/es/paper/2609.18063).
+ * The codes are integers decided by floating point, so this function works
+ * in binary32, step by step, the way the GPU merge does (and nothing else
+ * here does): for row o, group g, column k of the group
+ *     d_k = sum_{j<r} B[o][j] * A[j][k]    (fmaf chain, j ascending, from 0)
+ *     w_k = fmaf(scale, d_k, fmaf(q_k, s, b))
+ *     lo = min w_k, hi = max w_k
+ *     s' = f16((hi - lo) / (2^bits - 1)),  b' = f16(lo)      (RNE)
+ *     q'_k = s' == 0 ? 0 : clamp(rint((w_k - b') / s'), 0, 2^bits - 1)
+ * with every operation rounded to binary32 (nearest even).  m: ORC_AFFINE;
+ * l->scale is used as a binary32 value; r == 0 requantises W itself.
+ * Outputs in m's layout: q_out [rows][cols*bits/32], s_out, b_out
+ * [rows][cols/group] fp16 bit patterns.                                      */
+void orc_merge_lora(const orc_mat *m, const orc_lora *l, uint32_t *q_out,
+                    uint16_t *s_out, uint16_t *b_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -461,3 +461,74 @@ def test_stack_teacher_forcing_only_at_near_ties(orc):
     r = run3.step(x0, ext_idx=other, tie_margin=1e9)
     assert r["idx"].tolist() == other.tolist() and r["forced"].all()
     assert abs(r["w"].sum() - 1) < 1e-12
+
+
+# --------------------------------------------------------------- LoRA merge
+def _codes(m):
+    return synth.unpack(np.asarray(m["q"]), m["bits"])
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_merge_without_adapter_is_idempotent(orc, bits):
+    """Requantising weights that came out of the min/max quantiser returns
+    them unchanged wherever a group holds both extreme codes (then lo = b and
+    hi = b + (2^bits - 1) s exactly, so s' = s, b' = b and q' = q)."""
+    m = synth.affine(21, 3, 48, 256, bits, 0.02)
+    got = orc.merge_lora(m, None)
+    qmax = (1 << bits) - 1
+    q, q2 = _codes(m).reshape(48, 4, 64), _codes(got).reshape(48, 4, 64)
+    full = (q.min(2) == 0) & (q.max(2) == qmax)
+    assert full.mean() > 0.9
+    assert np.array_equal(q2[full], q[full])
+    assert np.array_equal(got["s"][full], np.asarray(m["s"])[full])
+    assert np.array_equal(got["b"][full], np.asarray(m["b"])[full])
+
+
+def test_merge_exact_steps_and_sub_step_delta(orc):
+    """Deltas that are whole quantisation steps move the bias and keep every
+    code; a sub-step delta on one interior weight is lost entirely.  Row 0
+    gains one step (B[0][0] A[0] = s_0), row 2 two steps (B[2][1] A[1] =
+    2 s_2), row 1 gets 0.3 s_1 on one interior weight (B[1][2] A[2]).  A
+    transposed operand or a swapped index moves the wrong row."""
+    m = synth.affine(22, 4, 3, 128, 4, 0.02)
+    s = np.asarray(m["s"]).view(np.float16).astype(np.float64)
+    b = np.asarray(m["b"]).view(np.float16).astype(np.float64)
+    q = _codes(m)
+    k1 = next(k for k in range(128) if 2 <= q[1, k] <= 13)
+    A = np.zeros((3, 128), np.float64)
+    A[0] = np.repeat(s[0], 64)
+    A[1] = np.repeat(2 * s[2], 64)
+    A[2, k1] = 0.3 * s[1, k1 // 64]
+    B = np.zeros((3, 3), np.float64)
+    B[0, 0] = B[2, 1] = B[1, 2] = 1.0
+    l = dict(A=A.astype(np.float16).view(np.uint16), B=B.astype(np.float16).view(np.uint16),
+             scale=1.0)
+    assert np.array_equal(l["A"].view(np.float16).astype(np.float64)[:2], A[:2])   # exact in fp16
+    got = orc.merge_lora(m, l)
+    assert np.array_equal(_codes(got), q)
+    assert np.array_equal(got["s"], np.asarray(m["s"]))
+    f16 = lambda v: np.float16(v).view(np.uint16)
+    for g in range(2):
+        assert got["b"][0, g] == f16(b[0, g] + s[0, g])
+        assert got["b"][1, g] == m["b"][1, g]
+        assert got["b"][2, g] == f16(b[2, g] + 2 * s[2, g])
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_merge_error_bound(orc, bits):
+    """Every merged weight lies within half a new quantisation step (plus the
+    fp16 rounding of the new scale and bias and the binary32 arithmetic) of
+    the exact W + scale B A, computed densely in fp64 with a library matmul."""
+    m = synth.affine(23, 5, 32, 256, bits, 0.02)
+    l = _lora(16, 256, 32, 7, scale=2.0)
+    got = orc.merge_lora(m, l)
+    A = l["A"].view(np.float16).astype(np.float64)
+    B = l["B"].view(np.float16).astype(np.float64)
+    exact = (orc.dequant(m) + l["scale"] * (B @ A)).reshape(32, 4, 64)
+    wd = orc.dequant(got).reshape(32, 4, 64)
+    qmax = (1 << bits) - 1
+    s2 = got["s"].view(np.float16).astype(np.float64)
+    b2 = got["b"].view(np.float16).astype(np.float64)
+    span = (exact.max(2) - exact.min(2)) / qmax
+    bound = 0.5 * s2 + np.abs(b2 - exact.min(2)) + qmax * np.abs(s2 - span) + 1e-6
+    assert (np.abs(wd - exact).max(2) <= bound).all()
