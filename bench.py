@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--cpu-layers", type=int, default=40,
                     help="layer samples the oracle baseline times (native arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--lora-merge", action="store_true",
+                    help="time merging the shared-expert adapters into the int4 weights "
+                         "(moe_merge_lora) and report the retained delta")
     ap.add_argument("--path", default="chain", choices=["chain", "fused", "per-call"],
                     help="chain: two kernels per layer chained by programmatic dependent "
                          "launch; fused: one persistent kernel per step; per-call: the "
@@ -547,13 +550,97 @@ def run_batched(args, cfg):
         print(json.dumps(line), flush=True)
 
 
+def run_merge(args, cfg):
+    """One step = merging every layer's shared-expert adapters (gate, up,
+    down) into its int4 weights and requantising them (moe_merge_lora, one
+    launch per projection) into a second set of blobs; L2 is flushed before
+    every timed step, each step timed by its own events.  Also reports the
+    retention of layer 0's adapter delta through the merge."""
+    import torch
+
+    from int4_expert_gemv_gb300 import moe
+    from int4_expert_gemv_gb300.model import DeviceModel, expert_sections, lora_merge_retention
+    import __graft_entry__
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    if not (cfg.shared and cfg.lora_r and cfg.lora_on == "shared_all"):
+        raise SystemExit(f"--lora-merge needs a config with shared-expert adapters, not {cfg.name}")
+    dm = DeviceModel(cfg, heads=False)
+    secs = expert_sections(cfg)
+    jobs = []          # (src, dst, row stride, rows, cols, LoraDesc)
+    outs = [torch.empty_like(ly["shared"]) for ly in dm.layers]
+    for ly, out in zip(dm.layers, outs):
+        ed = ly["experts_desc"]
+        for (off, stride, rows, cols), i in zip(secs, range(3)):
+            l = ed.shared_lora[i]
+            jobs.append((ly["shared"].data_ptr() + off, out.data_ptr() + off, stride, rows, cols, l))
+
+    def step():
+        for src, dst, stride, rows, cols, l in jobs:
+            moe.moe_merge_lora(src, stride, rows, cols, cfg.bits, l.A, l.B, l.r, l.scale, dst, stride)
+
+    # algorithmic bytes: every record read and written once, A and B read once
+    nbytes = sum(2 * rows * moe.moe_record_bytes(cols, cfg.bits) + 2 * l.r * (cols + rows)
+                 for _, _, _, rows, cols, l in jobs)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda")
+    step()                                   # eager once, then one graph per step
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for a, b in pairs:
+            flush.fill_(1)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in pairs)
+    ms_step = ms / args.steps
+    gbs = nbytes / (ms_step / 1000.0) / 1e9
+    ret = lora_merge_retention(dm, 0, 16)
+    if rank == 0:
+        hbm, hbm_kind = peaks()
+        line = {
+            "metric": "LoRA merge into the int4 weights (requantised per 64-group): GB/s",
+            "value": gbs, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{cfg.name}: shared-expert adapters of {len(dm.layers)} layers "
+                                   f"(r{cfg.lora_r}, gate/up/down)",
+                       "l2": "flushed before every timed step",
+                       "bytes_per_step": nbytes},
+            "roofline": {"bound": "hbm", "kernel": "merge_lora_kernel", "achieved": gbs,
+                         "peak": hbm, "peak_kind": hbm_kind, "unit": "GB/s", "frac": gbs / hbm,
+                         "traffic": None, "bytes_per_launch": nbytes / len(jobs),
+                         "timing": "CUDA events around each step (one graph of all launches "
+                                   "of the step)"},
+            "retention": {k: v for k, v in ret.items() if k != "merged_blob"},
+            "gpu_launches": len(jobs) * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     from int4_expert_gemv_gb300.configs import ALL
     cfg = ALL[args.config]
     if args.steps is None:
-        args.steps = 16 if args.impl == "reference" else (256 if cfg.T > 1 else 2400)
-    if args.impl == "reference":
+        args.steps = (16 if args.impl == "reference" or args.lora_merge
+                      else (256 if cfg.T > 1 else 2400))
+    if args.lora_merge:
+        run_merge(args, cfg)
+    elif args.impl == "reference":
         import oracle
         oracle.build()
         run_reference(args, cfg)

@@ -263,6 +263,28 @@ int moe_combine_residual(const float *y_slots, const float *w, int T, int K,
                          int has_shared, int d, const float *residual,
                          float *out, float *x_next, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- merge */
+/* Merges a LoRA delta into packed records: W' = requantise(W + scale B A),
+ * group by group (64 columns) in the same affine form -- the merged
+ * alternative to the unfused adapter (xyznot.com/es/paper/2609.18063,
+ * "Ejecucion del adaptador no fusionado": the adapter stays unfused because
+ * requantising keeps little of its delta; this call measures how little).
+ * src: `rows` records of moe_record_bytes(cols, bits) bytes, src_stride
+ * bytes apart (e.g. 2 * record for the gate or up rows of an expert blob);
+ * A fp16 [r][cols], B fp16 [rows][r] (r == 0: W is only requantised);
+ * dst: the merged records, dst_stride apart -- dst == src with equal
+ * strides merges in place (any other overlap is undefined).  Arithmetic,
+ * binary32 with every operation rounded to nearest even: per row o, group,
+ * column k: d_k = sum_j B[o][j] A[j][k] (fma chain, j ascending),
+ * w_k = fma(scale, d_k, fma(code_k, s, b)); s' = f16((max w - min w) /
+ * (2^bits - 1)), b' = f16(min w); code'_k = s' == 0 ? 0 :
+ * clamp(rint((w_k - b') / s'), 0, 2^bits - 1).  Records and strides 16-byte
+ * aligned, A 4-byte aligned; all device memory; enqueued on `stream`.
+ * rows == 0 is a no-op. */
+int moe_merge_lora(const void *src, size_t src_stride, int rows, int cols, int bits,
+                   const uint16_t *A, const uint16_t *B, int r, float scale,
+                   void *dst, size_t dst_stride, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- stack */
 /* A decode stack: depth layers per step, layer N using resident layer
  * N % n_layers (all of one shape).  Layer 0 routes with its own router every

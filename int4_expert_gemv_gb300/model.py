@@ -366,3 +366,64 @@ class BatchedLayer:
             ffn_events[1].record()
         moe.moe_combine_residual(self.y, self.cur_w, T, c.K, c.shared, c.d, self.res, self.out,
                                  self.x_next)
+
+
+# ---------------------------------------------------------------- LoRA merge
+def expert_sections(cfg: MoEConfig):
+    """(byte offset, row stride, rows, cols) of the gate, up and down rows of
+    one expert blob (gate row f = record 2f, up row f = record 2f + 1 of the
+    gate/up section; the down section starts on the next 256-byte boundary)."""
+    rec_d = moe.moe_record_bytes(cfg.d, cfg.bits)
+    rec_f = moe.moe_record_bytes(cfg.F, cfg.bits)
+    down = _align(2 * cfg.F * rec_d)
+    return [(0, 2 * rec_d, cfg.F, cfg.d), (rec_d, 2 * rec_d, cfg.F, cfg.d),
+            (down, rec_f, cfg.d, cfg.F)]
+
+
+def merged_expert_blob(blob: torch.Tensor, cfg: MoEConfig, adapters) -> torch.Tensor:
+    """A copy of one expert blob with its gate / up / down adapters (three
+    LoraDesc, r == 0 for none) merged into the weights and requantised, on
+    the GPU (moe_merge_lora)."""
+    out = blob.clone()
+    for (off, stride, rows, cols), l in zip(expert_sections(cfg), adapters):
+        if l.r:
+            moe.moe_merge_lora(blob.data_ptr() + off, stride, rows, cols, cfg.bits, l.A, l.B,
+                               l.r, l.scale, out.data_ptr() + off, stride)
+    return out
+
+
+def lora_merge_retention(model: DeviceModel, layer: int = 0, T: int = 16, tag: int = 977) -> dict:
+    """How much of the shared expert's LoRA delta survives merging it into
+    the int4 weights: the shared slot's output y over T seeded tokens with
+    the base weights (no adapter), the unfused adapter and the merged,
+    requantised weights; retention = <y_m - y_b, y_l - y_b> / |y_l - y_b|^2
+    and the merged result's error |y_m - y_l| / |y_l - y_b|."""
+    c = model.cfg
+    ly = model.layers[layer]
+    ed = ly["experts_desc"]
+    merged = merged_expert_blob(ly["shared"], c, [ed.shared_lora[i] for i in range(3)])
+
+    def desc(shared: torch.Tensor, adapters: bool):
+        e = moe.ExpertsDesc.from_buffer_copy(ed)
+        e.shared = shared.data_ptr()
+        if not adapters:
+            for i in range(3):
+                e.shared_lora[i] = moe.LoraDesc()
+        return e
+
+    x = torch.from_numpy(synth.gauss(c.seed, tag, (T, c.d), 1.0)).to(model.device)
+    idx = torch.from_numpy(synth.routes(c.seed, tag + 1, T, c.E, c.K)).to(model.device)
+    ys = []
+    for e in (desc(ly["shared"], False), desc(ly["shared"], True), desc(merged, False)):
+        y = torch.empty((T, c.K + 1, c.d), device=model.device)
+        ws = torch.empty(moe.moe_expert_ffn_workspace_bytes(e, T, c.K), dtype=torch.uint8,
+                         device=model.device)
+        moe.moe_expert_ffn_int4(e, x, idx, T, c.K, y, ws)
+        ys.append(y[:, c.K].double())
+    yb, yl, ym = ys
+    dl, dm = yl - yb, ym - yb
+    n2 = float((dl * dl).sum())
+    return {"retention": float((dm * dl).sum()) / n2,
+            "merged_error": float(((ym - yl) ** 2).sum() / n2) ** 0.5,
+            "delta_rms_over_y_rms": float((n2 / float((yl * yl).sum())) ** 0.5),
+            "tokens": T, "layer": layer, "merged_blob": merged}

@@ -74,6 +74,7 @@ def lib():
                 "moe_packed_matrix_bytes": (S, [I, I, I]),
                 "moe_pool_expert_bytes": (S, [I, I, I, I]),
                 "moe_pack_matrix": (I, [P, P, P, I, I, I, P, P]),
+                "moe_merge_lora": (I, [P, S, I, I, I, P, P, I, C.c_float, P, S, P]),
                 "moe_pack_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "moe_debug_dequant": (I, [P, I, I, I, I, P, P]),
                 "moe_prerouter_head_workspace_bytes": (S, [C.POINTER(HeadDesc), I]),
@@ -165,6 +166,14 @@ def moe_expert_ffn_workspace_bytes(ed: ExpertsDesc, T: int, K: int) -> int:
 def moe_pack_matrix(q, s, b, rows: int, cols: int, bits: int, out, stream=None):
     _check(lib().moe_pack_matrix(_ptr(q), _ptr(s), _ptr(b), rows, cols, bits, _ptr(out),
                                  _stream(stream)), "moe_pack_matrix")
+
+
+def moe_merge_lora(src, src_stride: int, rows: int, cols: int, bits: int, A, B, r: int,
+                   scale: float, dst, dst_stride: int, stream=None):
+    """W' = requantise(W + scale B A) on packed records (see include/moe.h).
+    src / dst: tensors or device addresses (ints) of the first record."""
+    _check(lib().moe_merge_lora(_ptr(src), src_stride, rows, cols, bits, _ptr(A), _ptr(B), r,
+                                scale, _ptr(dst), dst_stride, _stream(stream)), "moe_merge_lora")
 
 
 def moe_pack_experts(d, F, E, bits, gate_q, gate_s, gate_b, up_q, up_s, up_b, down_q, down_s,

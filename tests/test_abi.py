@@ -204,3 +204,21 @@ def test_decode_step_rejects_wide_shared_gate_up_lora(m, entry):
         rc = getattr(m.lib(), entry)(C.byref(sd), p, None, p, p, p, 1, p, 1 << 30, None)
         assert rc == want, (ranks, m.last_error())
     assert "NULL" in m.last_error()
+
+
+def test_merge_lora_rejects_bad_arguments(m):
+    L = m.lib()
+    p = 1 << 20
+    rb = m.moe_record_bytes(512, 4)
+    ok = dict(src=p, ss=rb, rows=4, cols=512, bits=4, A=p, B=p, r=8, scale=2.0, dst=p, ds=rb)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.moe_merge_lora(a["src"], a["ss"], a["rows"], a["cols"], a["bits"], a["A"], a["B"],
+                                a["r"], a["scale"], a["dst"], a["ds"], None)
+    for bad in (dict(bits=3), dict(cols=500), dict(rows=-1), dict(r=-1), dict(A=None),
+                dict(B=None), dict(src=None), dict(dst=None), dict(ss=rb - 16), dict(ds=rb + 4),
+                dict(src=p + 4)):
+        assert call(**bad) == m.MOE_EINVAL, bad
+        assert m.last_error() != ""
+    assert call(rows=0, src=None, dst=None) == m.MOE_OK      # nothing to do, nothing touched
