@@ -93,6 +93,25 @@ def measured_traffic(layers: int, path: str):
     return int(per_layer.group(1)) * layers + (int(fixed.group(1)) if fixed else 0)
 
 
+# ---------------------------------------------------------------- ranks
+def max_over_ranks(v: float, world: int, device: str = "cuda") -> float:
+    """The largest of every rank's v: the job takes as long as its slowest
+    rank (a collective; every rank calls it)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank decodes `steps` tokens (independent
+    replicas, weak scaling) in the slowest rank's `ms`."""
+    return world * steps / (ms / 1000.0)
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -287,12 +306,8 @@ def run_native(args, cfg):
         stop.record(stream)
         torch.cuda.nvtx.range_pop()
         barrier()
-    ms = start.elapsed_time(stop)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    tok_s = world * args.steps / (ms / 1000.0)
+    ms = max_over_ranks(start.elapsed_time(stop), world)
+    tok_s = job_tokens_per_s(args.steps, world, ms)
     ms_step = ms / args.steps
 
     # ---- per-launch durations of the dominant kernel (instrumented replay of
@@ -345,11 +360,7 @@ def run_native(args, cfg):
         pin_out[i].copy_(st.stream, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
 
     if rank == 0:
         hbm, hbm_kind = peaks()
@@ -394,7 +405,7 @@ def run_native(args, cfg):
                                     if st.fused else
                                     f"CUDA events around each layer's call in {n_inst} ")
                               + "instrumented graph replays after the timed region"},
-            "e2e": {"value": world * args.steps / (e2e_ms / 1000.0), "unit": "tokens/s",
+            "e2e": {"value": job_tokens_per_s(args.steps, world, e2e_ms), "unit": "tokens/s",
                     "h2d_bytes_per_step": cfg.d * 4, "d2h_bytes_per_step": cfg.d * 4},
             "gpu_launches": kernels_per_step(cfg, st) * args.steps,
             "clocks": clk.summary(),
