@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--cpu-layers", type=int, default=40,
                     help="layer samples the oracle baseline times (native arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--route-agreement", action="store_true",
+                    help="measure how often the predicted routes agree with the layers' own "
+                         "routers (seeded decode steps)")
     ap.add_argument("--lora-merge", action="store_true",
                     help="time merging the shared-expert adapters into the int4 weights "
                          "(moe_merge_lora) and report the retained delta")
@@ -642,15 +645,38 @@ def run_merge(args, cfg):
         print(json.dumps(line), flush=True)
 
 
+def run_agreement(args, cfg):
+    """Predicted routes against the layers' own routers over seeded decode
+    steps (per-call path): one JSON line with the agreement statistics."""
+    import torch
+
+    from int4_expert_gemv_gb300.model import DeviceModel, prediction_agreement
+    import __graft_entry__
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    __graft_entry__.build()
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    res = prediction_agreement(DeviceModel(cfg, heads=True), steps=args.steps)
+    print(json.dumps({"metric": "predicted route vs the layer's own router: mean K-set overlap",
+                      "value": res["mean_overlap"], "unit": "fraction", "n_gpus": 1,
+                      "steps": args.steps, "higher_is_better": True, "data": "synthetic",
+                      "config": {"workload": cfg.name, "note": "random synthetic heads: "
+                                 "a consistency measurement, no quality claim"},
+                      "agreement": res}), flush=True)
+
+
 def main():
     args = parse()
     from int4_expert_gemv_gb300.configs import ALL
     cfg = ALL[args.config]
     if args.steps is None:
-        args.steps = (16 if args.impl == "reference" or args.lora_merge
+        args.steps = (16 if args.impl == "reference" or args.lora_merge or args.route_agreement
                       else (256 if cfg.T > 1 else 2400))
     if args.lora_merge:
         run_merge(args, cfg)
+    elif args.route_agreement:
+        run_agreement(args, cfg)
     elif args.impl == "reference":
         import oracle
         oracle.build()

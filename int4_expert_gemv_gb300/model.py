@@ -297,6 +297,23 @@ class DecodeStack:
                     self.enqueue_step(t)
             self.graphs[rot] = g
 
+    def own_routes(self, t: int):
+        """Right after step t (t >= 1, per-call path): the top-K of every
+        layer's own router on the input x_N it had at t, with the logits'
+        margins -- what the layer would have used without the prediction."""
+        c = self.cfg
+        assert not self.fused and t >= 1 and self.t == t + 1
+        dev = self.m.device
+        own = torch.empty((c.depth, c.K), dtype=torch.int32, device=dev)
+        w = torch.empty((c.depth, c.K), dtype=torch.float32, device=dev)
+        mg = torch.empty(c.depth, dtype=torch.float32, device=dev)
+        z = torch.empty(c.E, dtype=torch.float32, device=dev)
+        for N in range(c.depth):
+            moe.moe_prerouter_head(self._layer(N)["router_desc"], self.xs[N], None, None, c.K, 1,
+                                   z, self.head_ws)
+            moe.moe_topk_route(z, 1, c.E, c.K, own[N], w[N], mg[N])
+        return own, mg
+
     def used_routes(self, t: int):
         """(idx [depth][K], w, margin) the layers used at step t (valid right
         after step t, before step t+2 overwrites the rotation)."""
@@ -427,3 +444,32 @@ def lora_merge_retention(model: DeviceModel, layer: int = 0, T: int = 16, tag: i
             "merged_error": float(((ym - yl) ** 2).sum() / n2) ** 0.5,
             "delta_rms_over_y_rms": float((n2 / float((yl * yl).sum())) ** 0.5),
             "tokens": T, "layer": layer, "merged_blob": merged}
+
+
+# ---------------------------------------------------------------- prediction agreement
+def prediction_agreement(model: DeviceModel, steps: int = 16) -> dict:
+    """How often the predicted route (head N-1 at t-1) agrees with the route
+    layer N's own router would take on its input at t, over `steps` seeded
+    decode steps (t = 1 .. steps, per-call path).  Layers that route
+    themselves (layer 0 without self-prediction) are left out.  Returns the
+    fraction of layer-steps whose K-sets are equal, the mean overlap
+    |predicted & own| / K, and K / E, the overlap two independent uniform
+    K-subsets have on average (random synthetic heads sit near it)."""
+    c = model.cfg
+    st = DecodeStack(model)
+    first = 0 if c.self_predict else 1
+    equal = overlap = n = 0
+    for t in range(steps + 1):
+        st.step(torch.from_numpy(synth.step_input(c, t)[0]).to(model.device))
+        if t == 0:
+            continue
+        own, _ = st.own_routes(t)
+        used, _, _ = st.used_routes(t)
+        own, used = own.cpu().numpy(), used.cpu().numpy()
+        for N in range(first, c.depth):
+            a, b = set(own[N].tolist()), set(used[N].tolist())
+            equal += int(a == b)
+            overlap += len(a & b) / c.K
+            n += 1
+    return {"layer_steps": n, "equal_sets": equal / n, "mean_overlap": overlap / n,
+            "chance_overlap": c.K / c.E, "steps": steps}
