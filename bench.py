@@ -389,8 +389,9 @@ def run_native(args, cfg):
                 "shared_expert": cfg.shared, "weight_bits": cfg.bits, "group": cfg.group,
                 "head_hidden": cfg.H, "head_prec": cfg.head_prec,
                 "lora": f"r{cfg.lora_r} alpha{cfg.lora_alpha:g} {cfg.lora_on}" if cfg.lora_r else "none",
-                "l2": f"no flush: each step reads {cfg.depth * (ffn_bytes + head_bytes) / 1e6:.0f} MB "
-                      f"of weights (> {L2_BYTES / 1e6:.0f} MB L2); routed experts change every step",
+                "l2": (f"no flush: each step reads {cfg.depth * (ffn_bytes + head_bytes) / 1e6:.0f} MB "
+                       f"of weights ({'>' if cfg.depth * (ffn_bytes + head_bytes) > L2_BYTES else '<'}"
+                       f" {L2_BYTES / 1e6:.0f} MB L2); routed experts change every step"),
                 "graphs": "steady-state steps replayed from captured CUDA graphs",
                 "path": args.path,
             },
