@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--cpu-layers", type=int, default=40,
                     help="layer samples the oracle baseline times (native arm)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-tier", action="store_true",
+                    help="decode with the routed experts in pinned host memory, gathered into "
+                         "HBM a token ahead, against the HBM-resident stack")
     ap.add_argument("--route-agreement", action="store_true",
                     help="measure how often the predicted routes agree with the layers' own "
                          "routers (seeded decode steps)")
@@ -646,6 +649,69 @@ def run_merge(args, cfg):
         print(json.dumps(line), flush=True)
 
 
+def run_host_tier(args, cfg):
+    """Per-call decode steps (captured graphs) with the routed experts
+    resident in HBM and with them in pinned host memory, gathered into HBM
+    slots a token ahead from the predicted routes (HostTierStack); plus the
+    gather alone (host -> HBM over NVLink-C2C)."""
+    import torch
+
+    from int4_expert_gemv_gb300 import moe, synth
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel, HostTierStack
+    import __graft_entry__
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    dm = DeviceModel(cfg)
+    stacks = {"hbm": DecodeStack(dm), "host": HostTierStack(dm)}
+    total = args.warmup + args.steps
+    xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
+                                       (total + 1, cfg.d), 1.0)).cuda()
+    stream = torch.cuda.current_stream()
+    res = {}
+    with ClockSampler(local) as clk:
+        for name, st in stacks.items():
+            st.step(xin[0])
+            st.capture()
+            for t in range(1, args.warmup + 1):
+                st.step(xin[t])
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for t in range(args.warmup + 1, total + 1):
+                st.step(xin[t])
+            b.record(stream)
+            torch.cuda.synchronize()
+            res[name] = a.elapsed_time(b) / args.steps
+        # the gathers of one step alone (every layer's K experts), repeated
+        tier = stacks["host"]
+        reps = 8
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            for N in range(cfg.depth):
+                tier.gather(N, tier.t - 1, stream)
+        b.record(stream)
+        torch.cuda.synchronize()
+    g_ms = a.elapsed_time(b) / reps
+    g_bytes = cfg.depth * cfg.K * tier.blob
+    print(json.dumps({
+        "metric": "decode tokens/s with the routed experts in host memory, gathered a token ahead",
+        "value": 1000.0 / res["host"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["host"], "higher_is_better": True,
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "path": "per-call kernels, captured graphs",
+                   "host_pool_bytes": sum(h.numel() for h in tier.host_pools),
+                   "gather_bytes_per_step": g_bytes},
+        "hbm_resident": {"ms_per_step": res["hbm"], "tokens_per_s": 1000.0 / res["hbm"]},
+        "gather_alone": {"ms_per_step": g_ms, "gbs": g_bytes / (g_ms / 1000.0) / 1e9,
+                         "note": "host pinned memory -> HBM slots, read by the GPU over C2C"},
+        "clocks": clk.summary()}), flush=True)
+
+
 def run_agreement(args, cfg):
     """Predicted routes against the layers' own routers over seeded decode
     steps (per-call path): one JSON line with the agreement statistics."""
@@ -673,11 +739,13 @@ def main():
     cfg = ALL[args.config]
     if args.steps is None:
         args.steps = (16 if args.impl == "reference" or args.lora_merge or args.route_agreement
-                      else (256 if cfg.T > 1 else 2400))
+                      else 200 if args.host_tier else (256 if cfg.T > 1 else 2400))
     if args.lora_merge:
         run_merge(args, cfg)
     elif args.route_agreement:
         run_agreement(args, cfg)
+    elif args.host_tier:
+        run_host_tier(args, cfg)
     elif args.impl == "reference":
         import oracle
         oracle.build()

@@ -285,6 +285,22 @@ int moe_merge_lora(const void *src, size_t src_stride, int rows, int cols, int b
                    const uint16_t *A, const uint16_t *B, int r, float scale,
                    void *dst, size_t dst_stride, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- tiers */
+/* Copies the blobs of experts idx[0..n-1] (a device array: a route) of a
+ * pool of E experts, expert_stride bytes apart, into n slots slot_stride
+ * bytes apart, and writes slot_idx[i] = i -- or n where idx[i] is outside
+ * [0, E): that blob is not copied and an expert call reading slot_idx gives
+ * NaN for it, as it would for idx.  The pool may live outside HBM: pinned
+ * host memory is read directly by the GPU (over NVLink-C2C on a Grace
+ * machine), so the routed experts of a layer can be brought into HBM a token
+ * ahead from the predicted route without a host round trip (the predicted
+ * route is the routing: xyznot.com/es/paper/2609.18063, "Ideas clave").
+ * blob_bytes, strides: multiples of 16 (blob_bytes <= both strides); pool and
+ * slots 16-byte aligned; n <= 17; enqueued on `stream`. */
+int moe_gather_experts(const void *pool, size_t expert_stride, int E, const int32_t *idx,
+                       int n, size_t blob_bytes, void *slots, size_t slot_stride,
+                       int32_t *slot_idx, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- stack */
 /* A decode stack: depth layers per step, layer N using resident layer
  * N % n_layers (all of one shape).  Layer 0 routes with its own router every

@@ -24,7 +24,7 @@ FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxe
 
 LIBS = {
     "libmoe.so": ["abi.cu", "pack.cu", "ffn.cu", "grouped.cu", "head_route.cu", "noalloc.cu",
-                  "step.cu", "chain.cu", "lora_merge.cu"],
+                  "step.cu", "chain.cu", "lora_merge.cu", "gather.cu"],
     "libmoe_synth.so": ["synth.cu"],
 }
 

@@ -253,8 +253,7 @@ class DecodeStack:
         self.stream.copy_(self.xin)
         for N in range(D):
             ly = self._layer(N)
-            own = (N == 0 and not c.self_predict) or t == 0
-            if own:
+            if self._own(N, t):
                 self._route_own(N, use)
             if ffn_events is not None:
                 ffn_events[N][0].record()
@@ -262,15 +261,29 @@ class DecodeStack:
                                     self.y, self.ffn_ws)
             if ffn_events is not None:
                 ffn_events[N][1].record()
-            moe.moe_combine_residual(self.y, self.r_w[use, N], 1, c.K, c.shared, c.d,
-                                     self.stream, self.stream, self.xs[N + 1])
-            tgt = N + 1 if N + 1 < D else (0 if c.self_predict else -1)
-            if tgt >= 0:
-                prev = self.r_idx[prv, N] if t > 0 else None
-                moe.moe_prerouter_head(ly["head_desc"], self.xs[N], self.r_idx[use, N], prev,
-                                       c.K, 1, self.logits[N], self.head_ws)
-                moe.moe_topk_route(self.logits[N], 1, c.E, c.K, self.r_idx[nxt, tgt],
-                                   self.r_w[nxt, tgt], self.r_margin[nxt, tgt])
+            self._layer_tail(N, t)
+
+    def _own(self, N: int, t: int) -> bool:
+        """Layer N routes with its own router at step t (layer 0 without
+        self-prediction; every layer at t = 0)."""
+        return (N == 0 and not self.cfg.self_predict) or t == 0
+
+    def _layer_tail(self, N: int, t: int):
+        """Combine + residual of layer N, then its head's prediction of the
+        next route of layer N + 1 (or of itself when self-predicting)."""
+        c = self.cfg
+        D = c.depth
+        use, nxt, prv = t % 3, (t + 1) % 3, (t - 1) % 3
+        ly = self._layer(N)
+        moe.moe_combine_residual(self.y, self.r_w[use, N], 1, c.K, c.shared, c.d,
+                                 self.stream, self.stream, self.xs[N + 1])
+        tgt = N + 1 if N + 1 < D else (0 if c.self_predict else -1)
+        if tgt >= 0:
+            prev = self.r_idx[prv, N] if t > 0 else None
+            moe.moe_prerouter_head(ly["head_desc"], self.xs[N], self.r_idx[use, N], prev,
+                                   c.K, 1, self.logits[N], self.head_ws)
+            moe.moe_topk_route(self.logits[N], 1, c.E, c.K, self.r_idx[nxt, tgt],
+                               self.r_w[nxt, tgt], self.r_margin[nxt, tgt])
 
     def step(self, x0: torch.Tensor):
         """Run step self.t eagerly (or through its captured graph)."""
@@ -319,6 +332,76 @@ class DecodeStack:
         after step t, before step t+2 overwrites the rotation)."""
         u = t % 3
         return self.r_idx[u].clone(), self.r_w[u].clone(), self.r_margin[u].clone()
+
+
+class HostTierStack(DecodeStack):
+    """Per-call decode with the routed experts in pinned host memory.
+
+    Every resident layer's routed pool is moved to pinned host memory (the
+    shared expert stays in HBM).  At the start of step t the routes of every
+    predicted layer are already known (made during step t - 1), so a side
+    stream gathers each layer's K experts into that layer's HBM slots
+    (moe_gather_experts, reading host memory over NVLink-C2C) while the main
+    stream computes; layer N's expert call waits only for its own gather.  A
+    layer that routes itself in the step gathers right after its router.
+    Results are those of DecodeStack bit for bit (same kernels, same bytes)."""
+
+    def __init__(self, model: DeviceModel):
+        super().__init__(model)
+        c = self.cfg
+        if c.lora_r and c.lora_on == "routed_down":
+            raise ValueError("routed-expert adapters are not gathered with the blobs")
+        dev = model.device
+        self.host_pools = []
+        for ly in model.layers:
+            h = torch.empty(ly["pool"].numel(), dtype=torch.uint8, pin_memory=True)
+            h.copy_(ly["pool"])
+            self.host_pools.append(h)
+        self.blob = moe.moe_pool_expert_bytes(c.d, c.F, c.bits, 64)
+        self.slots = torch.empty((c.depth, c.K * model.stride), dtype=torch.uint8, device=dev)
+        self.slot_idx = torch.empty((c.depth, c.K), dtype=torch.int32, device=dev)
+        self.eds = []
+        for N in range(c.depth):
+            e = moe.ExpertsDesc.from_buffer_copy(self._layer(N)["experts_desc"])
+            e.pool = self.slots[N].data_ptr()
+            e.E = c.K
+            self.eds.append(e)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ready = [torch.cuda.Event() for _ in range(c.depth)]
+
+    def gather(self, N: int, t: int, stream=None):
+        """Layer N's routed experts of step t, host pool -> its HBM slots."""
+        c = self.cfg
+        moe.moe_gather_experts(self.host_pools[N % c.L].data_ptr(), self.m.stride, c.E,
+                               self.r_idx[t % 3, N], c.K, self.blob, self.slots[N],
+                               self.m.stride, self.slot_idx[N], stream)
+
+    def enqueue_step(self, t: int, ffn_events=None):
+        c = self.cfg
+        use = t % 3
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            for N in range(c.depth):
+                if not self._own(N, t):
+                    self.gather(N, t, self.side)
+                    self.ready[N].record(self.side)
+        self.xs[0].copy_(self.xin)
+        self.stream.copy_(self.xin)
+        for N in range(c.depth):
+            if self._own(N, t):
+                self._route_own(N, use)
+                self.gather(N, t, main)
+            else:
+                main.wait_event(self.ready[N])
+            if ffn_events is not None:
+                ffn_events[N][0].record()
+            moe.moe_expert_ffn_int4(self.eds[N], self.xs[N], self.slot_idx[N], 1, c.K, self.y,
+                                    self.ffn_ws)
+            if ffn_events is not None:
+                ffn_events[N][1].record()
+            self._layer_tail(N, t)
+        main.wait_stream(self.side)
 
 
 class BatchedLayer:

@@ -75,6 +75,7 @@ def lib():
                 "moe_pool_expert_bytes": (S, [I, I, I, I]),
                 "moe_pack_matrix": (I, [P, P, P, I, I, I, P, P]),
                 "moe_merge_lora": (I, [P, S, I, I, I, P, P, I, C.c_float, P, S, P]),
+                "moe_gather_experts": (I, [P, S, I, P, I, S, P, S, P, P]),
                 "moe_pack_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "moe_debug_dequant": (I, [P, I, I, I, I, P, P]),
                 "moe_prerouter_head_workspace_bytes": (S, [C.POINTER(HeadDesc), I]),
@@ -174,6 +175,15 @@ def moe_merge_lora(src, src_stride: int, rows: int, cols: int, bits: int, A, B, 
     src / dst: tensors or device addresses (ints) of the first record."""
     _check(lib().moe_merge_lora(_ptr(src), src_stride, rows, cols, bits, _ptr(A), _ptr(B), r,
                                 scale, _ptr(dst), dst_stride, _stream(stream)), "moe_merge_lora")
+
+
+def moe_gather_experts(pool, expert_stride: int, E: int, idx, n: int, blob_bytes: int, slots,
+                       slot_stride: int, slot_idx, stream=None):
+    """Routed experts' blobs from a pool (HBM or pinned host memory) into HBM
+    slots, route rewritten to the slots (see include/moe.h)."""
+    _check(lib().moe_gather_experts(_ptr(pool), expert_stride, E, _ptr(idx), n, blob_bytes,
+                                    _ptr(slots), slot_stride, _ptr(slot_idx), _stream(stream)),
+           "moe_gather_experts")
 
 
 def moe_pack_experts(d, F, E, bits, gate_q, gate_s, gate_b, up_q, up_s, up_b, down_q, down_s,

@@ -222,3 +222,19 @@ def test_merge_lora_rejects_bad_arguments(m):
         assert call(**bad) == m.MOE_EINVAL, bad
         assert m.last_error() != ""
     assert call(rows=0, src=None, dst=None) == m.MOE_OK      # nothing to do, nothing touched
+
+
+def test_gather_experts_rejects_bad_arguments(m):
+    L = m.lib()
+    p = 1 << 20
+    ok = dict(pool=p, st=4096, E=8, idx=p, n=4, blob=4096, slots=p, ss=4096, sidx=p)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.moe_gather_experts(a["pool"], a["st"], a["E"], a["idx"], a["n"], a["blob"],
+                                    a["slots"], a["ss"], a["sidx"], None)
+    for bad in (dict(n=-1), dict(n=18), dict(E=0), dict(pool=None), dict(idx=None),
+                dict(slots=None), dict(sidx=None), dict(blob=0), dict(blob=4008),
+                dict(st=2048), dict(ss=4100), dict(pool=p + 8)):
+        assert call(**bad) == m.MOE_EINVAL, bad
+    assert call(n=0, pool=None) == m.MOE_OK
