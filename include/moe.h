@@ -34,6 +34,15 @@
  *                         page, "Arquitectura del Sistema": fused expert
  *                         combine + residual, RMS normalisation).
  *
+ * Whole decode steps over a stack of layers (every layer's calls above, with
+ * all routes known at the start of the step): moe_decode_step (one persistent
+ * kernel) and moe_decode_step_chain (two kernels per layer chained by
+ * programmatic dependent launch; the faster of the two).  Around them:
+ * moe_merge_lora (the adapter merged into the int4 weights and requantised,
+ * the alternative the xyznot page argues against), moe_gather_experts (a
+ * route's experts from a host-memory pool into HBM slots, for an expert tier
+ * outside HBM), packing, sizes and test hooks.
+ *
  * Conventions shared by every call
  *  - Memory: every pointer argument is a DEVICE pointer unless stated
  *    otherwise; the caller owns all memory.  The library never allocates,

@@ -238,3 +238,19 @@ def test_gather_experts_rejects_bad_arguments(m):
                 dict(st=2048), dict(ss=4100), dict(pool=p + 8)):
         assert call(**bad) == m.MOE_EINVAL, bad
     assert call(n=0, pool=None) == m.MOE_OK
+
+
+def test_expert_sections_match_the_blob_layout(m):
+    """Gate row f = record 2f, up row f = record 2f + 1 of the gate/up
+    section; the down section on the next 256-byte boundary; the blob size
+    covers both (the layout the header states)."""
+    from int4_expert_gemv_gb300.model import expert_sections
+    for cfg in (MOE35B, TINY, ALL["wide-int2"]):
+        (g_off, g_st, g_rows, g_cols), (u_off, u_st, u_rows, u_cols), (d_off, d_st, d_rows, d_cols) = \
+            expert_sections(cfg)
+        rec_d, rec_f = m.moe_record_bytes(cfg.d, cfg.bits), m.moe_record_bytes(cfg.F, cfg.bits)
+        assert (g_off, g_st, g_rows, g_cols) == (0, 2 * rec_d, cfg.F, cfg.d)
+        assert (u_off, u_st, u_rows, u_cols) == (rec_d, 2 * rec_d, cfg.F, cfg.d)
+        assert d_off % 256 == 0 and 2 * cfg.F * rec_d <= d_off < 2 * cfg.F * rec_d + 256
+        assert (d_st, d_rows, d_cols) == (rec_f, cfg.d, cfg.F)
+        assert d_off + cfg.d * rec_f <= m.moe_pool_expert_bytes(cfg.d, cfg.F, cfg.bits, 64)
