@@ -164,7 +164,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait of a whole warp for the phase of `bar` with `parity`: lane 0
-// polls, the verdict is shared, then every lane observes the completed phase
+// polls, the outcome is shared, then every lane observes the completed phase
 // itself (its acquire of the stage's data).  Returns false on expiry.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok = 0;
