@@ -4,7 +4,12 @@ DeviceModel draws every weight of a configuration on the GPU with the seeded
 generator (synth.py / csrc/synth.cu), packs experts into per-expert blobs and
 head matrices into records through the C ABI, and keeps descriptors for the
 four calls.  DecodeStack runs decode steps of the layer stack through those
-four calls only, and can capture one step as a CUDA graph.
+four calls (or, from step 1, through one of the two whole-step entries) and
+can capture one step as a CUDA graph.  Around it: BatchedLayer (one layer
+over T tokens), HostTierStack (routed experts in pinned host memory, gathered
+into HBM a token ahead), merged_expert_blob / lora_merge_retention (the
+adapter merged into the int4 weights, and how much of it survives) and
+prediction_agreement (predicted routes against the layers' own routers).
 
 Stack semantics (one decode step at token t; x_0 is the step's input):
   layer 0 routes with its own router (a head with H = 0) on x_0;
