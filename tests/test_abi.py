@@ -254,3 +254,31 @@ def test_expert_sections_match_the_blob_layout(m):
         assert d_off % 256 == 0 and 2 * cfg.F * rec_d <= d_off < 2 * cfg.F * rec_d + 256
         assert (d_st, d_rows, d_cols) == (rec_f, cfg.d, cfg.F)
         assert d_off + cfg.d * rec_f <= m.moe_pool_expert_bytes(cfg.d, cfg.F, cfg.bits, 64)
+
+
+def test_decode_step_chain_validation(m):
+    """The chained entry checks its arguments before touching the device:
+    step 0 (every layer routes itself) is refused, NULL buffers and a short
+    or unaligned workspace are refused, and a 2-bit stack whose d is not a
+    multiple of 256 is unsupported."""
+    L = m.lib()
+    p = 1 << 20
+    sd, keep = _stack(m, (16, 16, 16))
+    need = L.moe_decode_step_chain_workspace_bytes(C.byref(sd))
+    assert need > 0
+    call = lambda **kw: L.moe_decode_step_chain(
+        C.byref(kw.get("sd", sd)), kw.get("x0", p), kw.get("out", p), p, p, p, kw.get("t", 1),
+        kw.get("ws", p), kw.get("nb", need), None)
+    assert call(t=0) == m.MOE_EINVAL
+    assert call(x0=None) == m.MOE_EINVAL and call(out=None) == m.MOE_EINVAL
+    assert call(nb=need - 1) == m.MOE_ENOSPACE
+    assert call(ws=p + 16) == m.MOE_ENOSPACE
+    sd2, keep2 = _stack(m, (0, 0, 0))
+    e = C.cast(sd2.experts, C.POINTER(m.ExpertsDesc))[0]
+    e.d, e.bits = 320, 2
+    e.expert_stride = m.moe_pool_expert_bytes(320, 512, 2, 64)
+    r = C.cast(sd2.routers, C.POINTER(m.HeadDesc))[0]
+    r.d = 320
+    need2 = L.moe_decode_step_chain_workspace_bytes(C.byref(sd2))
+    assert need2 > 0
+    assert L.moe_decode_step_chain(C.byref(sd2), p, p, p, p, p, 1, p, need2, None) == m.MOE_EUNSUPPORTED
