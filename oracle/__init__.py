@@ -31,7 +31,7 @@ AFFINE, F16 = 0, 1
 
 def build(force: bool = False) -> str:
     """Compile oracle.c into liboracle.so (gcc -O2, no fast-math, no FMA
-    contraction: the binary32 merge relies on each operation rounding)."""
+    contraction: every operation rounds as written)."""
     newest = max(os.path.getmtime(_SRC), os.path.getmtime(_HDR))
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= newest:
         return _LIB_PATH
@@ -117,7 +117,10 @@ def lib():
             L.orc_combine.argtypes = [P, P, C.c_int, C.c_int, C.c_int, P, P, P]
             L.orc_stack_step.argtypes = [C.POINTER(Stack), C.POINTER(StackState),
                                          P, P, C.c_double, P, P, P, P, P]
-            L.orc_merge_lora.argtypes = [C.POINTER(Mat), C.POINTER(Lora), P, P, P]
+            L.orc_merge_weights.argtypes = [C.POINTER(Mat), C.POINTER(Lora), P]
+            L.orc_quant_codes.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P, P]
+            L.orc_requantise.argtypes = [P, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P, P, P, P]
+            L.orc_merge_lora.argtypes = [C.POINTER(Mat), C.POINTER(Lora), P, P, P, P, P, P]
             _lib = L
     return _lib
 
@@ -227,16 +230,38 @@ def gemv(m: dict, x) -> np.ndarray:
 
 
 def merge_lora(m: dict, l: dict | None) -> dict:
-    """W' = requantise(W + scale B A) group by group, in binary32 (oracle.h:
-    orc_merge_lora); returns a matrix dict of m's shape.  l None: W requantised."""
+    """W' = requantise(W + scale B A) group by group, in fp64 (oracle.h:
+    orc_merge_lora); returns a matrix dict of m's shape plus the merged
+    weights "w" [rows][cols] and the values before each rounding: "s_pre",
+    "b_pre" [rows][cols/group], "t_pre" [rows][cols].  l None: W requantised."""
     keep = _Keep()
     st, sl = mat(keep, m), lora(keep, l)
     q = np.zeros((st.rows, st.cols * st.bits // 32), np.uint32)
     s = np.zeros((st.rows, st.cols // st.group), np.uint16)
     b = np.zeros_like(s)
-    lib().orc_merge_lora(C.byref(st), C.byref(sl), _p(q), _p(s), _p(b))
+    s_pre = np.zeros(s.shape, np.float64)
+    b_pre = np.zeros(s.shape, np.float64)
+    t_pre = np.zeros((st.rows, st.cols), np.float64)
+    w = np.zeros((st.rows, st.cols), np.float64)
+    lib().orc_merge_weights(C.byref(st), C.byref(sl), _p(w))
+    lib().orc_requantise(_p(w), st.rows, st.cols, st.bits, st.group, _p(q), _p(s), _p(b),
+                         _p(s_pre), _p(b_pre), _p(t_pre))
     return {"q": q, "s": s, "b": b, "rows": st.rows, "cols": st.cols, "bits": st.bits,
-            "group": st.group}
+            "group": st.group, "w": w, "s_pre": s_pre, "b_pre": b_pre, "t_pre": t_pre}
+
+
+def quant_codes(w, bits: int, group: int, s, b):
+    """Codes of fp64 weights w [rows][cols] under given fp16 scales / biases
+    (bit patterns [rows][cols/group]), and the values before rint (oracle.h:
+    orc_quant_codes)."""
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    rows, cols = w.shape
+    s = np.ascontiguousarray(s, dtype=np.uint16)
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    q = np.zeros((rows, cols * bits // 32), np.uint32)
+    t = np.zeros((rows, cols), np.float64)
+    lib().orc_quant_codes(_p(w), rows, cols, bits, group, _p(s), _p(b), _p(q), _p(t))
+    return q, t
 
 
 def lora_apply(l: dict, x, y) -> np.ndarray:

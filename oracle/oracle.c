@@ -478,58 +478,80 @@ void orc_stack_step(const orc_stack *st, orc_stack_state *state,
 }
 
 /* ======================================================================== */
-/* Merging a LoRA delta into the quantised weights (binary32, see oracle.h)  */
+/* Merging a LoRA delta into the quantised weights (fp64, see oracle.h)      */
 /* ======================================================================== */
 
-static uint32_t code_of(const orc_mat *m, int o, int k)
+void orc_merge_weights(const orc_mat *m, const orc_lora *l, double *w)
 {
-    const int per = 32 / m->bits;                     /* codes per word */
-    const uint32_t word = m->q[(size_t)o * (m->cols / per) + k / per];
-    return (word >> (m->bits * (k % per))) & ((1u << m->bits) - 1u);
+    orc_dequant(m, w);
+    if (!l || l->r == 0)
+        return;
+    for (int o = 0; o < m->rows; o++)
+        for (int k = 0; k < m->cols; k++) {
+            double d = 0.0;
+            for (int j = 0; j < l->r; j++)
+                d += orc_f16_to_f64(l->B[(size_t)o * l->r + j]) *
+                     orc_f16_to_f64(l->A[(size_t)j * m->cols + k]);
+            w[(size_t)o * m->cols + k] += l->scale * d;
+        }
 }
 
-/* binary32 -> binary16 bits, nearest even (the float widens exactly). */
-static uint16_t f32_to_f16(float v) { return orc_f64_to_f16((double)v); }
-static float f16_to_f32(uint16_t h) { return (float)orc_f16_to_f64(h); }
+void orc_quant_codes(const double *w, int rows, int cols, int bits, int group,
+                     const uint16_t *s, const uint16_t *b, uint32_t *q_out,
+                     double *t_pre)
+{
+    const int per = 32 / bits, ng = cols / group;
+    const double qmax = (double)((1 << bits) - 1);
+    memset(q_out, 0, sizeof(uint32_t) * (size_t)rows * (cols / per));
+    for (int o = 0; o < rows; o++)
+        for (int k = 0; k < cols; k++) {
+            const double sv = orc_f16_to_f64(s[(size_t)o * ng + k / group]);
+            const double bv = orc_f16_to_f64(b[(size_t)o * ng + k / group]);
+            double t = 0.0, q = 0.0;
+            if (sv != 0.0) {
+                t = (w[(size_t)o * cols + k] - bv) / sv;
+                q = nearbyint(t);                     /* nearest, ties even */
+                q = q < 0.0 ? 0.0 : (q > qmax ? qmax : q);
+            }
+            if (t_pre)
+                t_pre[(size_t)o * cols + k] = t;
+            q_out[(size_t)o * (cols / per) + k / per] |=
+                (uint32_t)q << (bits * (k % per));
+        }
+}
+
+void orc_requantise(const double *w, int rows, int cols, int bits, int group,
+                    uint32_t *q_out, uint16_t *s_out, uint16_t *b_out,
+                    double *s_pre, double *b_pre, double *t_pre)
+{
+    const int ng = cols / group;
+    const double qmax = (double)((1 << bits) - 1);
+    for (int o = 0; o < rows; o++)
+        for (int g = 0; g < ng; g++) {
+            const double *wg = w + (size_t)o * cols + (size_t)g * group;
+            double lo = wg[0], hi = wg[0];
+            for (int i = 1; i < group; i++) {
+                if (wg[i] < lo) lo = wg[i];
+                if (wg[i] > hi) hi = wg[i];
+            }
+            const double span = (hi - lo) / qmax;
+            s_out[(size_t)o * ng + g] = orc_f64_to_f16(span);
+            b_out[(size_t)o * ng + g] = orc_f64_to_f16(lo);
+            if (s_pre)
+                s_pre[(size_t)o * ng + g] = span;
+            if (b_pre)
+                b_pre[(size_t)o * ng + g] = lo;
+        }
+    orc_quant_codes(w, rows, cols, bits, group, s_out, b_out, q_out, t_pre);
+}
 
 void orc_merge_lora(const orc_mat *m, const orc_lora *l, uint32_t *q_out,
-                    uint16_t *s_out, uint16_t *b_out)
+                    uint16_t *s_out, uint16_t *b_out, double *s_pre,
+                    double *b_pre, double *t_pre)
 {
-    const int G = m->group, per = 32 / m->bits, ng = m->cols / G;
-    const uint32_t qmax = (1u << m->bits) - 1u;
-    const float scale = (float)l->scale;
-    float *w = malloc(sizeof(float) * (size_t)G);
-    memset(q_out, 0, sizeof(uint32_t) * (size_t)m->rows * (m->cols / per));
-    for (int o = 0; o < m->rows; o++) {
-        for (int g = 0; g < ng; g++) {
-            const float s = f16_to_f32(m->s[(size_t)o * ng + g]);
-            const float b = f16_to_f32(m->b[(size_t)o * ng + g]);
-            float lo = 0.0f, hi = 0.0f;
-            for (int i = 0; i < G; i++) {
-                const int k = g * G + i;
-                float d = 0.0f;
-                for (int j = 0; j < l->r; j++)
-                    d = fmaf(f16_to_f32(l->B[(size_t)o * l->r + j]),
-                             f16_to_f32(l->A[(size_t)j * m->cols + k]), d);
-                w[i] = fmaf(scale, d, fmaf((float)code_of(m, o, k), s, b));
-                if (i == 0 || w[i] < lo) lo = w[i];
-                if (i == 0 || w[i] > hi) hi = w[i];
-            }
-            const uint16_t s2 = f32_to_f16((hi - lo) / (float)qmax);
-            const uint16_t b2 = f32_to_f16(lo);
-            s_out[(size_t)o * ng + g] = s2;
-            b_out[(size_t)o * ng + g] = b2;
-            const float sf = f16_to_f32(s2), bf = f16_to_f32(b2);
-            for (int i = 0; i < G; i++) {
-                const int k = g * G + i;
-                uint32_t q = 0;
-                if (sf != 0.0f) {
-                    const float t = rintf((w[i] - bf) / sf);
-                    q = t <= 0.0f ? 0u : (t >= (float)qmax ? qmax : (uint32_t)t);
-                }
-                q_out[(size_t)o * (m->cols / per) + k / per] |= q << (m->bits * (k % per));
-            }
-        }
-    }
+    double *w = malloc(sizeof(double) * (size_t)m->rows * m->cols);
+    orc_merge_weights(m, l, w);
+    orc_requantise(w, m->rows, m->cols, m->bits, m->group, q_out, s_out,
+                   b_out, s_pre, b_pre, t_pre);
     free(w);
 }

@@ -207,20 +207,33 @@ void orc_stack_step(const orc_stack *st, orc_stack_state *state,
  * group by group, in the same affine form (the pages run the adapter unfused
  * because merging and requantising keeps only a small part of its delta:
  * "Ejecucion del adaptador no fusionado", xyznot.com/es/paper/2609.18063).
- * The codes are integers decided by floating point, so this function works
- * in binary32, step by step, the way the GPU merge does (and nothing else
- * here does): for row o, group g, column k of the group
- *     d_k = sum_{j<r} B[o][j] * A[j][k]    (fmaf chain, j ascending, from 0)
- *     w_k = fmaf(scale, d_k, fmaf(q_k, s, b))
- *     lo = min w_k, hi = max w_k
- *     s' = f16((hi - lo) / (2^bits - 1)),  b' = f16(lo)      (RNE)
- *     q'_k = s' == 0 ? 0 : clamp(rint((w_k - b') / s'), 0, 2^bits - 1)
- * with every operation rounded to binary32 (nearest even).  m: ORC_AFFINE;
- * l->scale is used as a binary32 value; r == 0 requantises W itself.
- * Outputs in m's layout: q_out [rows][cols*bits/32], s_out, b_out
- * [rows][cols/group] fp16 bit patterns.                                      */
+ *
+ * orc_merge_weights: the merged weights, from the definition, in fp64:
+ *     w[o][k] = W[o][k] + scale * sum_{j<r} B[o][j] * A[j][k]   (j ascending)
+ * orc_quant_codes: the codes of w under a given fp16 scale s and bias b per
+ *     (row, group) -- the affine quantiser's code rule:
+ *     q = s == 0 ? 0 : clamp(rint((w - b) / s), 0, 2^bits - 1)  (ties even)
+ *     t_pre (nullable) receives (w - b) / s before rounding (0 where s == 0).
+ * orc_requantise: the min/max affine quantiser applied to w, per (row, group):
+ *     lo = min w, hi = max w, s = f16((hi - lo) / (2^bits - 1)), b = f16(lo)
+ *     (RNE), then the codes as above.  s_pre / b_pre (nullable) receive
+ *     (hi - lo) / (2^bits - 1) and lo before the fp16 rounding, t_pre the
+ *     code values before rint -- so a caller can see which decisions lie
+ *     near a rounding boundary.
+ * orc_merge_lora = orc_merge_weights then orc_requantise.  m: ORC_AFFINE;
+ * r == 0 requantises W itself.  Outputs in m's layout: q [rows][cols*bits/32],
+ * s, b [rows][cols/group] fp16 bit patterns, s_pre/b_pre [rows][cols/group],
+ * t_pre [rows][cols].                                                         */
+void orc_merge_weights(const orc_mat *m, const orc_lora *l, double *w);
+void orc_quant_codes(const double *w, int rows, int cols, int bits, int group,
+                     const uint16_t *s, const uint16_t *b, uint32_t *q_out,
+                     double *t_pre);
+void orc_requantise(const double *w, int rows, int cols, int bits, int group,
+                    uint32_t *q_out, uint16_t *s_out, uint16_t *b_out,
+                    double *s_pre, double *b_pre, double *t_pre);
 void orc_merge_lora(const orc_mat *m, const orc_lora *l, uint32_t *q_out,
-                    uint16_t *s_out, uint16_t *b_out);
+                    uint16_t *s_out, uint16_t *b_out, double *s_pre,
+                    double *b_pre, double *t_pre);
 
 #ifdef __cplusplus
 }

@@ -108,3 +108,58 @@ def zero_expert(cfg) -> dict:
                     b=np.zeros((rows, cols // 64), np.uint16),
                     rows=rows, cols=cols, bits=bits, group=64)
     return dict(gate=z(F, d), up=z(F, d), down=z(d, F))
+
+
+MERGE_EPS = 0.01   # a rounding decision within this fraction of a grid step of a midpoint may go either way
+
+
+def _f16_pair(v):
+    """fp16 neighbours (bit patterns lo <= v <= hi, as values) of fp64 values,
+    and whether v lies within MERGE_EPS of a step of their midpoint."""
+    v = np.asarray(v, dtype=np.float64)
+    r = v.astype(np.float16)
+    rv = r.astype(np.float64)
+    lo = np.where(rv > v, np.nextafter(r, np.float16(-np.inf)), r)
+    hi = np.where(rv < v, np.nextafter(r, np.float16(np.inf)), r)
+    lv, hv = lo.astype(np.float64), hi.astype(np.float64)
+    near = (hv > lv) & (np.abs(v - 0.5 * (lv + hv)) <= MERGE_EPS * (hv - lv))
+    return lo.view(np.uint16), hi.view(np.uint16), near
+
+
+def _codes_ok(q_got, t, bits):
+    """Codes decided from the pre-rounding values t: equal to clamp(rint(t))
+    except within MERGE_EPS of a midpoint, where either neighbour is taken."""
+    qmax = (1 << bits) - 1
+    fl = np.floor(t)
+    near = np.abs(t - (fl + 0.5)) <= MERGE_EPS
+    exact = np.clip(np.rint(t), 0, qmax)
+    alt = np.clip(np.where(t - fl < 0.5, fl + 1, fl), 0, qmax)
+    return (q_got == exact) | (near & (q_got == alt))
+
+
+def assert_merge_matches(orc, ref: dict, q_got, s_got, b_got, what: str):
+    """GPU merge output (logical q words, s, b bit patterns) against the
+    oracle's fp64 merge (oracle.merge_lora).  The new scale and bias of a
+    group are compared bit for bit, except where the oracle's value before the
+    fp16 rounding lies within MERGE_EPS of a step of a midpoint (binary32
+    arithmetic may then land on the other neighbour).  The codes are compared
+    bit for bit against the oracle's rule applied, in fp64, under the scale
+    and bias the GPU chose, except where that value before rint lies within
+    MERGE_EPS of a midpoint.  Returns the number of near-boundary decisions
+    that went the other way."""
+    bits, group = ref["bits"], ref["group"]
+    s_lo, s_hi, s_near = _f16_pair(ref["s_pre"])
+    b_lo, b_hi, b_near = _f16_pair(ref["b_pre"])
+    s_ok = (s_got == ref["s"]) | (s_near & ((s_got == s_lo) | (s_got == s_hi)))
+    b_ok = (b_got == ref["b"]) | (b_near & ((b_got == b_lo) | (b_got == b_hi)))
+    assert s_ok.all(), f"{what}: {int((~s_ok).sum())} scales differ away from a rounding boundary"
+    assert b_ok.all(), f"{what}: {int((~b_ok).sum())} biases differ away from a rounding boundary"
+    _, t = orc.quant_codes(ref["w"], bits, group, s_got, b_got)
+    per = 32 // bits
+    codes = ((np.asarray(q_got, np.uint32)[:, :, None] >> (bits * np.arange(per, dtype=np.uint32)))
+             & np.uint32((1 << bits) - 1)).reshape(t.shape).astype(np.float64)
+    ok = _codes_ok(codes, t, bits)
+    assert ok.all(), f"{what}: {int((~ok).sum())} codes differ away from a rounding boundary"
+    ref_codes = ((np.asarray(ref["q"], np.uint32)[:, :, None] >> (bits * np.arange(per, dtype=np.uint32)))
+                 & np.uint32((1 << bits) - 1)).reshape(t.shape)
+    return int((s_got != ref["s"]).sum() + (b_got != ref["b"]).sum() + (codes != ref_codes).sum())

@@ -1,7 +1,9 @@
-"""LoRA merge on the GPU (moe_merge_lora) against the oracle's binary32
-merge: codes, scales and biases bit for bit, in place and strided; then the
-retention measurement (how much of the shared expert's adapter delta the
-merged int4 weights keep) against the same measurement on the oracle."""
+"""LoRA merge on the GPU (moe_merge_lora) against the oracle's fp64 merge:
+codes, scales and biases bit for bit except at decisions that lie within a
+small fraction of a grid step of a rounding midpoint (tests/_util.py:
+assert_merge_matches), in place and strided; then the retention measurement
+(how much of the shared expert's adapter delta the merged int4 weights keep)
+against the same measurement on the oracle."""
 from dataclasses import replace
 
 import numpy as np
@@ -11,7 +13,7 @@ import torch
 import oracle as orc
 from int4_expert_gemv_gb300 import synth
 from int4_expert_gemv_gb300.configs import ALL
-from _util import host_expert_from_gpu
+from _util import assert_merge_matches, host_expert_from_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -73,9 +75,7 @@ def test_merge_matches_oracle(m, bits, r):
     _merge(m, src, dst, rows, cols, bits, l)
     ref = orc.merge_lora(mat, l)
     q, s, b = _unpacked(m, dst, rows, cols, bits)
-    assert np.array_equal(q, ref["q"])
-    assert np.array_equal(s, ref["s"])
-    assert np.array_equal(b, ref["b"])
+    assert_merge_matches(orc, ref, q, s, b, f"int{bits} r{r}")
     # the copy is whole records (zero padding included); in place gives the same bytes
     _merge(m, src, src, rows, cols, bits, l)
     assert torch.equal(src, dst)
@@ -94,7 +94,7 @@ def test_merge_strided_rows_leave_the_others(m):
     odd = dict(mat, q=mat["q"][1::2], s=mat["s"][1::2], b=mat["b"][1::2], rows=rows)
     ref = orc.merge_lora(odd, l)
     q, s, b = _unpacked(m, src, rows, cols, bits, first=1, step=2)
-    assert np.array_equal(q, ref["q"]) and np.array_equal(s, ref["s"]) and np.array_equal(b, ref["b"])
+    assert_merge_matches(orc, ref, q, s, b, "odd rows")
     even = src.view(2 * rows, rb)[0::2]
     assert torch.equal(even, before.view(2 * rows, rb)[0::2])
 
@@ -121,11 +121,10 @@ def test_retention_matches_oracle(m):
     ret = float((dmg * dl).sum() / (dl * dl).sum())
     assert 0.0 < ret < 1.0
     assert abs(got["retention"] - ret) < 0.02, (got["retention"], ret)
-    # the merged blob itself: every section bit-exact against the oracle's merge
+    # the merged blob itself: every section against the oracle's merge
     blob = got["merged_blob"]
     from int4_expert_gemv_gb300.model import expert_sections
     for (off, stride, rows, cols), name in zip(expert_sections(cfg), ("gate", "up", "down")):
         rb = m.moe_record_bytes(cols, cfg.bits)
         q, s, b = _unpacked(m, blob[off:], rows, cols, cfg.bits, step=stride // rb)
-        assert np.array_equal(q, merged[name]["q"]), name
-        assert np.array_equal(s, merged[name]["s"]) and np.array_equal(b, merged[name]["b"]), name
+        assert_merge_matches(orc, merged[name], q, s, b, name)

@@ -5,6 +5,7 @@ on the pages, a library routine, brute force, or an invariant the definition
 implies.  None of these tests needs a GPU.
 """
 import itertools
+from dataclasses import replace
 import math
 import os
 
@@ -532,3 +533,91 @@ def test_merge_error_bound(orc, bits):
     span = (exact.max(2) - exact.min(2)) / qmax
     bound = 0.5 * s2 + np.abs(b2 - exact.min(2)) + qmax * np.abs(s2 - span) + 1e-6
     assert (np.abs(wd - exact).max(2) <= bound).all()
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_merge_comparison_tolerates_only_boundary_decisions(orc, bits):
+    """The GPU-merge comparison (tests/_util.py) accepts the oracle's own
+    output and a binary32 evaluation of the same merge (numpy float32, no
+    fused operations), and rejects a code, a scale or a bias moved away from
+    a rounding boundary."""
+    from _util import assert_merge_matches
+    m = synth.affine(24, 6, 40, 256, bits, 0.02)
+    l = _lora(17, 256, 40, 16, scale=2.0)
+    ref = orc.merge_lora(m, l)
+    assert assert_merge_matches(orc, ref, ref["q"], ref["s"], ref["b"], "self") == 0
+    # binary32: w = q s + b + scale (B A), min/max, fp16 rounding, codes
+    f32 = np.float32
+    A = l["A"].view(np.float16).astype(f32)
+    B = l["B"].view(np.float16).astype(f32)
+    qn = _codes(m).astype(f32)
+    s = np.repeat(np.asarray(m["s"]).view(np.float16).astype(f32), 64, axis=1)
+    b = np.repeat(np.asarray(m["b"]).view(np.float16).astype(f32), 64, axis=1)
+    w = (qn * s + b) + f32(2.0) * (B @ A)
+    wg = w.reshape(40, 4, 64)
+    qmax = f32((1 << bits) - 1)
+    s2 = ((wg.max(2) - wg.min(2)) / qmax).astype(np.float16)
+    b2 = wg.min(2).astype(np.float16)
+    s2f = np.repeat(s2.astype(f32), 64, axis=1)
+    b2f = np.repeat(b2.astype(f32), 64, axis=1)
+    codes = np.clip(np.rint((w - b2f) / s2f), 0, qmax).astype(np.uint32)
+    per = 32 // bits
+    q32 = (codes.reshape(40, -1, per) << (bits * np.arange(per, dtype=np.uint32))).sum(2).astype(np.uint32)
+    assert_merge_matches(orc, ref, q32, s2.view(np.uint16), b2.view(np.uint16), "binary32")
+    # planted mistakes (in copies of the oracle's output): each is caught
+    t = ref["t_pre"]
+    k = int(np.argmin(np.abs(np.abs(t - np.floor(t) - 0.5) - 0.25)))     # far from a midpoint
+    o, c = divmod(k, 256)
+    q_bad = ref["q"].copy()
+    q_bad[o, c // per] ^= np.uint32(1 << (bits * (c % per)))
+    with pytest.raises(AssertionError):
+        assert_merge_matches(orc, ref, q_bad, ref["s"], ref["b"], "code")
+    s_bad = ref["s"].copy()
+    s_bad[3, 1] += 1
+    with pytest.raises(AssertionError):
+        assert_merge_matches(orc, ref, ref["q"], s_bad, ref["b"], "scale")
+    b_bad = ref["b"].copy()
+    b_bad[5, 2] += 2
+    with pytest.raises(AssertionError):
+        assert_merge_matches(orc, ref, ref["q"], ref["s"], b_bad, "bias")
+
+
+def test_multi_layer_stack_routes_from_the_previous_layers_head(orc):
+    """A 3-layer stack (tiny shapes, shared expert) over 4 steps, rebuilt from
+    the separately pinned functions: layer 0 routes with its own router every
+    step; layer N >= 1 routes with its own router at t = 0 and afterwards with
+    the top-K head N-1 computed at t-1; head N runs on x_N with cur = layer
+    N's route at t and prev = layer N's route at t-1, and x_{N+1} is the RMS of
+    out_N.  Applying head N's prediction to layer N instead of N+1, or taking
+    prev from another layer, changes the routes and fails this test."""
+    cfg = replace(TINY, L=3, depth=3, self_predict=False)
+    L = cfg.L
+    layers = [dict(experts=[synth.expert_host(cfg, n, e) for e in range(cfg.E)],
+                   shared=synth.expert_host(cfg, n, synth.SHARED_EXPERT),
+                   router=synth.router_host(cfg, n), head=synth.head_host(cfg, n))
+              for n in range(L)]
+    run = orc.StackRunner(layers, cfg.d, cfg.E, cfg.K)
+    pred_z = [None] * L          # logits head N-1 gave for layer N at the last step
+    prev = [None] * L            # route layer N used at the last step
+    seen = set()
+    for t in range(4):
+        x0 = synth.step_input(cfg, t)[0].astype(np.float64)
+        r = run.step(x0)
+        stream, x = x0, x0
+        cur, nxt = [None] * L, [None] * L
+        for N in range(L):
+            ly = layers[N]
+            z = orc.head_logits(ly["router"], x) if (N == 0 or t == 0) else pred_z[N]
+            idx, w, _ = orc.topk(z, cfg.K)
+            assert r["idx"][N].tolist() == idx.tolist(), (t, N)
+            assert np.array_equal(r["w"][N], w), (t, N)
+            y = orc.expert_ffn(ly["experts"], ly["shared"], x[None], idx[None])[0]
+            out, xn = orc.combine(y, w, True, stream)
+            if N + 1 < L:
+                nxt[N + 1] = orc.head_logits(ly["head"], x, idx, prev[N], cfg.K)
+            cur[N] = idx
+            seen.add(tuple(idx.tolist()))
+            stream, x = out, xn
+        assert np.array_equal(r["out"], stream), t
+        prev, pred_z = cur, nxt
+    assert len(seen) > 6          # the routes do change from layer to layer and step to step
