@@ -138,7 +138,19 @@ class ClockSampler:
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        # nvidia-smi takes a moment to start: the work to be sampled waits
+        # for its first line (at most 5 s)
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 5.0 and self.samples() == 0:
+            time.sleep(0.05)
         return self
+
+    def samples(self) -> int:
+        try:
+            with open(self.path) as f:
+                return sum(1 for line in f if line.count(",") >= 8)
+        except OSError:
+            return 0
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -200,40 +212,89 @@ def oracle_layer_sampler(cfg, n_layers: int):
     return run_layer
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def host_threads() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle_layers(run_layer, layer_samples: int, threads: int) -> float:
+    """Seconds for layer_samples oracle layer passes at `threads` threads."""
+    import oracle as orc
+    orc.set_threads(threads)
+    try:
+        run_layer(0)
+        t0 = time.perf_counter()
+        for i in range(layer_samples):
+            run_layer(i)
+        return time.perf_counter() - t0
+    finally:
+        orc.set_threads(1)
+
+
 def cpu_baseline(cfg, layer_samples: int):
+    """The oracle on the host cores: layer passes timed at every core (the
+    reported value) and on one thread; results are the same bits at both."""
+    import oracle as orc
     run_layer = oracle_layer_sampler(cfg, 4)
-    run_layer(0)
-    t0 = time.perf_counter()
-    for i in range(layer_samples):
-        run_layer(i)
-    dt = time.perf_counter() - t0
-    per_layer = dt / layer_samples
-    return {"value": 1.0 / (per_layer * cfg.depth), "unit": "tokens/s", "cores": 1,
-            "kind": "oracle",
+    n = host_threads() if orc.openmp() else 1
+    dt_n = time_oracle_layers(run_layer, layer_samples, n)
+    dt_1 = time_oracle_layers(run_layer, layer_samples, 1) if n > 1 else dt_n
+    tok = lambda dt: layer_samples / (dt * cfg.depth)
+    return {"value": tok(dt_n), "unit": "tokens/s", "cores": n, "kind": "oracle",
+            "cpu_model": cpu_model(), "host_cpus": os.cpu_count(),
+            "single_thread": {"value": tok(dt_1), "unit": "tokens/s", "cores": 1},
             "sample": f"{layer_samples} layer passes (head, top-K, {cfg.slots} experts, combine) "
-                      f"on 4 distinct layers, {dt:.1f} s, extrapolated to a {cfg.depth}-layer token"}
+                      f"on 4 distinct layers: {dt_n:.1f} s on {n} threads (OpenMP over output "
+                      f"rows), {dt_1:.1f} s on 1; extrapolated to a {cfg.depth}-layer token"}
 
 
 def run_reference(args, cfg):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    import oracle as orc
     run_layer = oracle_layer_sampler(cfg, 4)
+    n = host_threads() if orc.openmp() else 1
+    orc.set_threads(n)
     for i in range(args.warmup):
         run_layer(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
         run_layer(i)
     dt = time.perf_counter() - t0
+    orc.set_threads(1)
     v = args.steps / (dt * cfg.depth)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "batch": 1, "layers": cfg.depth},
-            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": n, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"each step = one layer pass of the plain C oracle "
-                                       f"(head, top-K, {cfg.slots} experts, combine); "
+                                       f"(head, top-K, {cfg.slots} experts, combine) on {n} "
+                                       f"threads (OpenMP over output rows); "
                                        f"tokens/s = steps / (time * {cfg.depth} layers)"},
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -241,6 +302,15 @@ def run_reference(args, cfg):
 
 
 # ---------------------------------------------------------------- native
+def path_dtype(cfg, path: str) -> str:
+    """What the timed decode path computes in."""
+    w = f"int{cfg.bits}-g{cfg.group} weights (fp16 scale, bias)"
+    if path in ("chain", "fused"):
+        return (f"{w} x 16-bit fixed-point activations (power-of-two scale per 16-byte code "
+                f"chunk, exact integer chunk dots), fp32 accumulate")
+    return f"{w} x f32 activations, fp32 accumulate"
+
+
 def kernels_per_step(cfg, stack) -> int:
     """Kernel launches of one steady-state step (counted from the calls the
     driver makes; the kernels per call are fixed by the library)."""
@@ -289,6 +359,14 @@ def run_native(args, cfg):
     xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
                                        (total + 64, cfg.d), 1.0)).cuda()
 
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream()
+    # the clock sampler runs from the warm-up to the end of the last timed leg
+    clk = ClockSampler(local).__enter__()
     # step 0 (routers everywhere) eagerly, then capture the steady state
     st.step(xin[0])
     st.capture()
@@ -296,22 +374,15 @@ def run_native(args, cfg):
         st.step(xin[t])
     torch.cuda.synchronize()
 
-    def barrier():
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    stream = torch.cuda.current_stream()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
-    with ClockSampler(local) as clk:
-        torch.cuda.nvtx.range_push("timed")
-        start.record(stream)
-        for t in range(args.warmup, total):
-            st.step(xin[t])
-        stop.record(stream)
-        torch.cuda.nvtx.range_pop()
-        barrier()
+    torch.cuda.nvtx.range_push("timed")
+    start.record(stream)
+    for t in range(args.warmup, total):
+        st.step(xin[t])
+    stop.record(stream)
+    torch.cuda.nvtx.range_pop()
+    barrier()
     ms = max_over_ranks(start.elapsed_time(stop), world)
     tok_s = job_tokens_per_s(args.steps, world, ms)
     ms_step = ms / args.steps
@@ -351,22 +422,43 @@ def run_native(args, cfg):
     if st.chain:
         launch_bytes += dm.head_bytes_per_token() * cfg.depth
 
-    # ---- end to end: host input -> device, step, result -> host, per step
+    # ---- end to end through the library: per step, the token's input from
+    # pinned host memory (cudaMemcpyAsync), the decode call through the C ABI
+    # (moe_decode_step_chain / moe_decode_step, or the per-layer calls),
+    # the step's output back to pinned host memory
     pin_in = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 1),
                                           (args.steps, cfg.d), 1.0)).pin_memory()
     pin_out = torch.empty((args.steps, cfg.d), dtype=torch.float32).pin_memory()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        st.xin.copy_(pin_in[i], non_blocking=True)
-        g = st.graphs[st.t % 3]
-        g.replay()
-        st.t += 1
-        pin_out[i].copy_(st.stream, non_blocking=True)
-    e1.record(stream)
-    barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+
+    def e2e_leg(use_graphs: bool) -> float:
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            st.xin.copy_(pin_in[i], non_blocking=True)
+            if use_graphs:
+                st.graphs[st.t % 3].replay()
+            elif st.fused:
+                st.enqueue_fused_step(st.t)
+            else:
+                st.enqueue_step(st.t)
+            st.t += 1
+            pin_out[i].copy_(st.stream, non_blocking=True)
+        e1.record(stream)
+        barrier()
+        return max_over_ranks(e0.elapsed_time(e1), world)
+
+    e2e_ms = e2e_leg(False)
+    e2e_graph_ms = e2e_leg(True)
+    # short runs: keep the GPU under the same load until the sampler has seen
+    # at least ten samples (untimed)
+    t_end = time.time() + 3.0
+    while clk.samples() < 10 and time.time() < t_end:
+        for _ in range(64):
+            st.graphs[st.t % 3].replay()
+            st.t += 1
+        torch.cuda.synchronize()
+    clk.__exit__(None, None, None)
 
     if rank == 0:
         hbm, hbm_kind = peaks()
@@ -385,7 +477,7 @@ def run_native(args, cfg):
             "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f32", "data": "synthetic",
+            "dtype": path_dtype(cfg, args.path), "data": "synthetic",
             "config": {
                 "workload": cfg.name, "batch": 1, "layers": cfg.depth, "d_model": cfg.d,
                 "experts": cfg.E, "top_k": cfg.K, "expert_ffn": cfg.F,
@@ -413,7 +505,16 @@ def run_native(args, cfg):
                                     f"CUDA events around each layer's call in {n_inst} ")
                               + "instrumented graph replays after the timed region"},
             "e2e": {"value": job_tokens_per_s(args.steps, world, e2e_ms), "unit": "tokens/s",
-                    "h2d_bytes_per_step": cfg.d * 4, "d2h_bytes_per_step": cfg.d * 4},
+                    "h2d_bytes_per_step": cfg.d * 4, "d2h_bytes_per_step": cfg.d * 4,
+                    "how": "per step: cudaMemcpyAsync of x0 from pinned host memory, "
+                           + ("one moe_decode_step_chain call" if st.chain else
+                              "one moe_decode_step call" if st.fused else
+                              "the per-layer C-ABI calls")
+                           + " through the C ABI (no graph), out back to pinned host memory",
+                    "graph_replay": {"value": job_tokens_per_s(args.steps, world, e2e_graph_ms),
+                                     "unit": "tokens/s",
+                                     "how": "the same copies around a replay of the step's "
+                                            "captured CUDA graph"}},
             "gpu_launches": kernels_per_step(cfg, st) * args.steps,
             "clocks": clk.summary(),
         }
@@ -535,7 +636,8 @@ def run_batched(args, cfg):
             "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic",
+            "dtype": (f"int{cfg.bits}-g{cfg.group} weights (codes as exact bf16 on the tensor "
+                      f"cores) x bf16 activations, fp32 accumulate"), "data": "synthetic",
             "config": {
                 "workload": cfg.name, "batch": T, "layers": 1, "d_model": cfg.d,
                 "experts": cfg.E, "top_k": cfg.K, "expert_ffn": cfg.F,

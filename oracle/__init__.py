@@ -36,8 +36,11 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= newest:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall",
-                    "-o", tmp, _SRC, "-lm"], check=True)
+    base = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-Wall"]
+    # OpenMP (row loops, see orc_set_threads) where the compiler has it
+    r = subprocess.run(base + ["-fopenmp", "-o", tmp, _SRC, "-lm"], capture_output=True)
+    if r.returncode != 0:
+        subprocess.run(base + ["-Wno-unknown-pragmas", "-o", tmp, _SRC, "-lm"], check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -102,6 +105,10 @@ def lib():
             L.orc_weight.argtypes = [C.POINTER(Mat), C.c_int, C.c_int]
             L.orc_dequant.argtypes = [C.POINTER(Mat), P]
             L.orc_gemv.argtypes = [C.POINTER(Mat), P, P]
+            L.orc_set_threads.argtypes = [C.c_int]
+            L.orc_set_threads.restype = None
+            L.orc_openmp.argtypes = []
+            L.orc_openmp.restype = C.c_int
             L.orc_lora_apply.argtypes = [C.POINTER(Lora), C.c_int, C.c_int, P, P]
             L.orc_silu.restype = C.c_double
             L.orc_silu.argtypes = [C.c_double]
@@ -217,6 +224,17 @@ def dequant(m: dict) -> np.ndarray:
     w = np.zeros((st.rows, st.cols), np.float64)
     lib().orc_dequant(C.byref(st), _p(w))
     return w
+
+
+def set_threads(n: int) -> None:
+    """Threads for the oracle's row loops (results are identical at any
+    count; 1 when the library was built without OpenMP)."""
+    lib().orc_set_threads(int(n))
+
+
+def openmp() -> bool:
+    """Whether liboracle.so was built with OpenMP."""
+    return bool(lib().orc_openmp())
 
 
 def gemv(m: dict, x) -> np.ndarray:

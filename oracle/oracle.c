@@ -134,8 +134,26 @@ void orc_dequant(const orc_mat *m, double *w)
             w[(size_t)o * m->cols + k] = orc_weight(m, o, k);
 }
 
+/* Threads the row loops of orc_gemv and orc_head_logits may use (1 unless
+ * orc_set_threads raised it; only when built with OpenMP).  A row is always
+ * summed by one thread in ascending index order, so results are the same
+ * bits at any count. */
+static int orc_threads = 1;
+
+void orc_set_threads(int n) { orc_threads = n > 0 ? n : 1; }
+
+int orc_openmp(void)
+{
+#ifdef _OPENMP
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 void orc_gemv(const orc_mat *m, const double *x, double *y)
 {
+#pragma omp parallel for num_threads(orc_threads) schedule(static) if (orc_threads > 1)
     for (int o = 0; o < m->rows; o++) {
         double acc = 0.0;
         for (int k = 0; k < m->cols; k++)
@@ -263,12 +281,14 @@ void orc_head_logits(const orc_head *hd, const double *x, const int32_t *cur,
     orc_head_features(d, E, x, cur, prev, K, f);
 
     double *g = (double *)calloc((size_t)(H > 0 ? H : 1), sizeof(double));
+#pragma omp parallel for num_threads(orc_threads) schedule(static) if (orc_threads > 1)
     for (int o = 0; o < H; o++) {                     /* a = fc1 f + b1 */
         double acc = 0.0;
         for (int c = 0; c < width; c++)
             acc += split_weight(&hd->fc1x, hd->fc1_tab, H, d, o, c) * f[c];
         g[o] = orc_gelu_erf(acc + bias_or_zero(hd->b1, o));
     }
+#pragma omp parallel for num_threads(orc_threads) schedule(static) if (orc_threads > 1)
     for (int e = 0; e < E; e++) {
         double acc = 0.0;
         for (int o = 0; o < H; o++)                   /* fc2 gelu(a) */

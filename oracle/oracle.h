@@ -71,6 +71,12 @@ void   orc_dequant(const orc_mat *m, double *w);
 /* y[o] = sum_k W[o][k] * x[k]. */
 void   orc_gemv(const orc_mat *m, const double *x, double *y);
 
+/* Threads for the row loops of orc_gemv and orc_head_logits (default 1; the
+ * library is built with OpenMP where the compiler has it).  Each row is one
+ * thread's ascending-order sum: the results do not depend on n. */
+void   orc_set_threads(int n);
+int    orc_openmp(void);                /* 1 when built with OpenMP */
+
 /* ---- recovery LoRA:  y += (alpha/r) * B (A x)  ---------------------------
  * A fp16 [r][in], B fp16 [out][r]; r == 0 means no adapter.                 */
 typedef struct {

@@ -95,6 +95,24 @@ def test_expert_ffn_rejects_bad_arguments(m, kw, call):
     assert m.last_error() != ""
 
 
+@pytest.mark.parametrize("kw,call", [
+    (dict(d=2000), {}), (dict(E=0), {}), (dict(E=-5), {}),
+    (dict(pool=None), {}), ({}, dict(K=0)), ({}, dict(K=17)), ({}, dict(K=40)),
+    ({}, dict(T=-1)), ({}, dict(x=None)), ({}, dict(x=(1 << 20) + 4)), ({}, dict(x_dtype=7)),
+    ({}, dict(T=100000, x=(1 << 20) + 4)),
+])
+def test_noalloc_rejects_bad_arguments_like_the_workspace_entry(m, kw, call):
+    """The allocation-free entry validates before it sizes its scratch: bad
+    arguments get MOE_EINVAL (as from moe_expert_ffn_int4), never
+    MOE_ENOSPACE, and touch no device."""
+    ed = _experts_desc(m, **kw)
+    a = dict(T=1, K=4, x=1 << 20, idx=1 << 20, y=1 << 20, x_dtype=0)
+    a.update(call)
+    rc = m.lib().moe_expert_ffn_int4_noalloc(C.byref(ed), a["x"], a["x_dtype"], a["idx"],
+                                              a["T"], a["K"], a["y"], None)
+    assert rc == m.MOE_EINVAL, m.last_error()
+
+
 def test_expert_ffn_rejects_small_workspace(m):
     ed = _experts_desc(m)
     need = m.moe_expert_ffn_workspace_bytes(ed, 1, 4)

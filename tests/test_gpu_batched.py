@@ -204,3 +204,29 @@ def test_batched_layer_step(m):
                         for k in range(cfg.K)) + bf16_h_allowance(sh, xb[t])
             assert (err <= bound + allow).all(), f"layer output token {t}"
     assert checked >= 6
+
+
+def test_batched_bounded_wait_times_out_and_recovers(m):
+    """The batched engine's waits take the set limit: with the test hook on,
+    one consumer warp waits for bytes no copy sends; after 50 ms MOE_ETIMEOUT
+    lands in ws word 0 and the launches return (the context stays usable).
+    With the hook off the next call's outputs match the oracle again."""
+    import time
+    cfg = ALL["batched-T64"]
+    T = 64
+    routes = synth.routes(cfg.seed, 907, T, cfg.E, cfg.K)
+    x = _x(cfg, T, 908)
+    ed = _model(cfg).layers[0]["experts_desc"]
+    y = torch.full((T, cfg.slots, cfg.d), 7.0, device="cuda")
+    ws = torch.empty(m.moe_expert_ffn_workspace_bytes(ed, T, cfg.K), dtype=torch.uint8, device="cuda")
+    m.moe_debug_batched_waits(50_000_000, True)
+    try:
+        t0 = time.time()
+        m.moe_expert_ffn_int4(ed, x, torch.from_numpy(routes).cuda(), T, cfg.K, y, ws)
+        torch.cuda.synchronize()                                    # context alive
+        assert ws[:4].view(torch.int32).item() == m.MOE_ETIMEOUT
+        assert time.time() - t0 < 10.0               # the 50 ms limit, not 1 s per wait
+    finally:
+        m.moe_debug_batched_waits(0, False)
+    got = _run(m, cfg, routes, x)                    # asserts MOE_OK in ws word 0
+    _check(cfg, got, x, routes, np.arange(0, T, 4), "batched after a timed-out call")

@@ -137,3 +137,56 @@ def test_fused_bounded_wait_times_out_and_recovers():
     st.step(torch.from_numpy(synth.step_input(cfg, 1)[0]).cuda())
     assert st.status() == moe.MOE_OK
     assert torch.isfinite(st.stream).all()
+
+
+def test_chain_bounded_wait_times_out_and_recovers():
+    """The chained step's mbarrier waits take the caller's limit: with the
+    test hook on, CTA 0 of layer 0's first kernel waits for bytes no copy
+    sends; after the 50 ms limit MOE_ETIMEOUT lands in the status word and
+    the kernel returns (the context stays usable).  Step 1 run again with the
+    hook off, then steps 2 and 3, give the same bits as a stack that never
+    stalled (whose path the stack tests compare with the oracle)."""
+    import time
+    from int4_expert_gemv_gb300 import moe
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    cfg = ALL["35b-L4"]
+    dm = DeviceModel(cfg)
+    st, ref = DecodeStack(dm, fused="chain"), DecodeStack(dm, fused="chain")
+    xs = [torch.from_numpy(synth.step_input(cfg, t)[0]).cuda() for t in range(4)]
+    st.step(xs[0])                                                         # step 0: per-call
+    ref.step(xs[0])
+    st.sd.timeout_ns = 50_000_000
+    st.sd.debug_unset_wait = 1
+    t0 = time.time()
+    st.step(xs[1])
+    assert st.status() == moe.MOE_ETIMEOUT
+    assert time.time() - t0 < 10.0                   # the 50 ms limit, not 1 s per wait
+    torch.cuda.synchronize()                                               # context alive
+    st.sd.debug_unset_wait = 0
+    st.sd.timeout_ns = 0
+    st.t = 1
+    for t in (1, 2, 3):
+        st.step(xs[t])
+        ref.step(xs[t])
+        assert st.status() == moe.MOE_OK
+        assert torch.equal(st.stream, ref.stream)
+        assert torch.equal(st.r_idx, ref.r_idx)
+    assert torch.isfinite(st.stream).all()
+
+
+@pytest.mark.parametrize("name", ["35b", "35b-K2", "35b-K8", "8b", "tiny"])
+def test_chain_kernels_are_coresident(name):
+    """The chained step relies on a CTA of kernel A(N+1) sitting on an SM
+    beside one of B(N), so that A(N+1) copies its weights while B(N) runs: a
+    register spill or a shared-memory change that broke this would only show
+    as a slower step.  The library's residency query checks it on the
+    device (occupancy API, shared memory incl. reservations, registers)."""
+    from int4_expert_gemv_gb300 import moe
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    cfg = ALL[name] if name == "tiny" else replace(ALL[name], L=1)
+    st = DecodeStack(DeviceModel(cfg), fused="chain")
+    info = moe.moe_decode_step_chain_info(st.sd)
+    assert info["local_bytes_a"] == 0 and info["local_bytes_b"] == 0, info
+    assert info["regs_a"] <= 64 and info["regs_b"] <= 64, info
+    assert info["ctas_a"] >= 1 and info["ctas_b"] >= 1, info
+    assert info["coresident"] == 1, info

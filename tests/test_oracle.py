@@ -621,3 +621,23 @@ def test_multi_layer_stack_routes_from_the_previous_layers_head(orc):
         assert np.array_equal(r["out"], stream), t
         prev, pred_z = cur, nxt
     assert len(seen) > 6          # the routes do change from layer to layer and step to step
+
+
+# --------------------------------------------------------------- threads
+def test_threaded_rows_give_the_same_bits(orc):
+    """The CPU baseline times the oracle at several thread counts: a row is
+    still one thread's ascending-order sum, so GEMV and head logits are the
+    same bits at 1 and 4 threads."""
+    m = _rand_affine(96, 512, 4, 31)
+    x = np.random.default_rng(32).normal(size=512)
+    cfg, hd = _head(E=32, d=128, H=64, seed=33)
+    xh = np.random.default_rng(34).normal(size=cfg.d)
+    cur, prev = np.array([3, 7]), np.array([1, 30])
+    try:
+        orc.set_threads(1)
+        y1, z1 = orc.gemv(m, x), orc.head_logits(hd, xh, cur, prev, 2)
+        orc.set_threads(4)
+        y4, z4 = orc.gemv(m, x), orc.head_logits(hd, xh, cur, prev, 2)
+    finally:
+        orc.set_threads(1)
+    assert np.array_equal(y1, y4) and np.array_equal(z1, z4)
