@@ -46,8 +46,12 @@
  * Conventions shared by every call
  *  - Memory: every pointer argument is a DEVICE pointer unless stated
  *    otherwise; the caller owns all memory.  The library never allocates,
- *    frees or synchronises.  Scratch memory comes from a caller-provided
- *    workspace whose size the matching *_workspace_bytes() call returns.
+ *    frees or synchronises (the *_status readers synchronise the stream
+ *    they are given).  Scratch memory comes from a caller-provided workspace
+ *    whose size the matching *_workspace_bytes() call returns -- except for
+ *    moe_expert_ffn_int4_noalloc, whose scratch is one static 4 MiB device
+ *    array that every GPU loading the library holds until exit, shared by
+ *    all calls on that device.
  *  - Alignment: device pointers must be 16-byte aligned; expert pools and
  *    packed matrices 256-byte aligned.
  *  - Streams: every call only enqueues work on `stream` (asynchronous).
@@ -147,6 +151,15 @@ int moe_pack_experts(int d, int F, int E, int bits,
  * fmaf(code, scale, bias), the same decode the GEMV kernels use. */
 int moe_debug_dequant(const void *blob, int d, int F, int bits, int which,
                       float *out, cudaStream_t stream);
+
+/* Test hook, process-wide: the bound of every device-side wait of the
+ * batched tensor-core engine (moe_expert_ffn_int4 and moe_prerouter_head with
+ * T > 1 bf16 tokens), timeout_ns (0 = 1 second), read at each launch.
+ * stall != 0 adds to every later launch one wait for bytes that no copy
+ * sends: it runs out after timeout_ns, MOE_ETIMEOUT lands in the call's
+ * status word (ws word 0) and the launch returns with invalid outputs.
+ * moe_debug_batched_waits(0, 0) restores the defaults. */
+int moe_debug_batched_waits(unsigned long long timeout_ns, int stall);
 
 /* ---------------------------------------------------------------- head */
 typedef struct {
@@ -257,11 +270,22 @@ int moe_expert_ffn_int4(const moe_experts_desc *ed, const void *x, int x_dtype,
  * before any stream capture on the device.  All calls on a device share the
  * one array, which keeps the last call's contents: calls that may overlap on
  * the GPU (e.g. issued on different streams without ordering) race with each
- * other and must be serialised by the caller.  No scratch needs clearing
- * between calls. */
+ * other and must be serialised by the caller.  Each call clears the array's
+ * status word (word 0) on `stream`; the rest needs no clearing between
+ * calls.  Bad arguments get the same status as from moe_expert_ffn_int4.
+ *
+ * The batched path's bounded device-side waits record MOE_ETIMEOUT in that
+ * status word (the outputs are then invalid); the caller has no workspace to
+ * read it from, so it reads it with moe_expert_ffn_noalloc_status. */
 int moe_expert_ffn_int4_noalloc(const moe_experts_desc *ed, const void *x,
                                 int x_dtype, const int32_t *idx, int T, int K,
                                 float *y_slots, cudaStream_t stream);
+
+/* Waits for `stream` and stores in *status (host) the status word of the last
+ * moe_expert_ffn_int4_noalloc call on the current device that `stream` has
+ * finished: MOE_OK, or MOE_ETIMEOUT if one of its batched-path waits expired.
+ * Synchronises `stream`. */
+int moe_expert_ffn_noalloc_status(int *status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------- combine */
 /* out[t] = residual[t] + sum_k w[t][k] * y_slots[t][k] (+ y_slots[t][K] if
@@ -382,8 +406,11 @@ int moe_decode_step_status(const void *ws, int *status, cudaStream_t stream);
  * shared memory before it waits for the one before (the step's routes are
  * known when it starts).  The heads' top-K (the routes of t+1) run in one
  * launch at the end of the step.  No kernel waits on another's CTAs: the only
- * device-side wait is a CTA's on its own copies (bounded; MOE_ETIMEOUT in the
- * status word on expiry).
+ * device-side wait is a CTA's on its own copies (bounded by sd->timeout_ns,
+ * 0 = 1 second; on expiry MOE_ETIMEOUT lands in the status word and the CTA
+ * returns: the step's outputs are then invalid).  sd->debug_unset_wait = 1
+ * makes CTA 0 of layer 0's first kernel wait, once its own copies have
+ * landed, for bytes no copy sends: a test of that path.
  * ws: moe_decode_step_chain_workspace_bytes() bytes, 256-byte aligned (no
  * clearing needed); its status reads with moe_decode_step_status.  The step
  * enqueues 2 * depth launches, + 2 for layer 0's own router and its top-K
@@ -391,6 +418,27 @@ int moe_decode_step_status(const void *ws, int *status, cudaStream_t stream);
  * need layer 0's partials), + 1 for the heads' top-K; under stream capture
  * they form one graph. */
 size_t moe_decode_step_chain_workspace_bytes(const moe_stack_desc *sd);
+
+/* How the two per-layer kernels of moe_decode_step_chain sit on an SM of the
+ * current device for the stack sd (host struct, filled by the call below). */
+typedef struct {
+    size_t smem_a, smem_b;       /* dynamic shared memory per CTA of A and B  */
+    int threads;                 /* threads per CTA                           */
+    int regs_a, regs_b;          /* registers per thread                      */
+    int local_bytes_a, local_bytes_b; /* local memory per thread (spills)     */
+    int ctas_a, ctas_b;          /* CTAs of A (of B) an SM holds on its own   */
+    int coresident;              /* 1: an SM holds a CTA of A beside one of B
+                                    (shared memory incl. the per-CTA
+                                    reservation, and registers) -- so that
+                                    A(N+1) copies its weights while B(N) runs */
+} moe_chain_info;
+
+/* Fills *info for sd on the current device (the occupancy API and the
+ * kernels' attributes); MOE_EUNSUPPORTED when a kernel does not fit an SM at
+ * all (moe_decode_step_chain then fails the same way).  The step runs when
+ * coresident is 0, with each kernel's copies starting only when the previous
+ * one's CTAs have left. */
+int moe_decode_step_chain_info(const moe_stack_desc *sd, moe_chain_info *info);
 int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, float *out,
                           int32_t *route_idx, float *route_w, float *route_margin,
                           int t, void *ws, size_t ws_bytes, cudaStream_t stream);

@@ -40,7 +40,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxR = 32;                 // LoRA rank bound
 constexpr int kMaxK = 16;
-constexpr uint64_t kCopyWaitNs = 1000000000ull;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // a wait's bound when the caller sets none
 constexpr int kMaxHPass = 8;              // h of all slots: at most 8 * 512 float4 (16 Ki floats)
 
 struct CLayer {
@@ -80,6 +80,8 @@ struct CP {
     const float *topk_z;      // logits the router top-K ranks
     int topk_set, topk_tgt;   // where the route goes
     int32_t *err;
+    uint64_t timeout_ns;      // bound of every mbarrier wait
+    int debug_unset_wait;     // test hook: CTA 0 of this launch waits on bytes nobody sends
     unsigned long long *trace;   // debug: per launch 8 stamps of CTA 0 (start, waited, end, ...)
     int launch_id;
 };
@@ -110,8 +112,9 @@ __device__ __forceinline__ void bar_expect(uint64_t *bar, uint32_t bytes) {
                  "r"(bytes) : "memory");
 }
 
-// Bounded wait for phase 0 of bar (this kernel's one use of it).
-__device__ __forceinline__ bool bar_wait(uint64_t *bar, int32_t *err) {
+// Bounded wait for phase 0 of bar (this kernel's one use of it): false, with
+// MOE_ETIMEOUT in *err, once timeout_ns have passed.
+__device__ __forceinline__ bool bar_wait(uint64_t *bar, int32_t *err, uint64_t timeout_ns) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; it++) {
         uint32_t ok;
@@ -123,7 +126,7 @@ __device__ __forceinline__ bool bar_wait(uint64_t *bar, int32_t *err) {
         uint64_t now;
         asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
         if (it == 0) t0 = now;
-        else if (now - t0 > kCopyWaitNs) {
+        else if (now - t0 > timeout_ns) {
             atomicExch(err, MOE_ETIMEOUT);
             return false;
         }
@@ -645,7 +648,18 @@ __global__ void __launch_bounds__(kThreads, 2) chain_a_kernel(const __grid_const
         vx[lane] = a * inv;
     }
     __syncthreads();
-    if (!bar_wait(bar, p.err)) return;
+    if (!bar_wait(bar, p.err, p.timeout_ns)) return;
+    if (p.debug_unset_wait && c == 0) {
+        // test hook: a wait for 16 bytes no copy delivers, on a barrier of its
+        // own once this CTA's copies have landed: it runs out after
+        // timeout_ns, records MOE_ETIMEOUT and the CTA returns
+        if (threadIdx.x == 0) {
+            bar_init(bar + 1);
+            bar_expect(bar + 1, 16);
+        }
+        __syncthreads();
+        if (!bar_wait(bar + 1, p.err, p.timeout_ns)) return;
+    }
     // units v = w, w + kWarps, ... of the CTA's list (its pairs, then its head rows)
     stamp(p, 4);
     for (int v = warp; v < ng + nh; v += kWarps) {
@@ -844,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 2) chain_b_kernel(const __grid_const
     if (threadIdx.x >= 32 && threadIdx.x < 32 + ne) zls[threadIdx.x - 32] = zlv;
     __syncthreads();
     stamp(p, 3);
-    if (!bar_wait(bar, p.err)) return;
+    if (!bar_wait(bar, p.err, p.timeout_ns)) return;
     stamp(p, 4);
     // down LoRA: vd[s][k] = A_d[k] h_s (routed adapter slots, then the shared
     // one), one (slot, k) row per warp, A from shared memory
@@ -1077,7 +1091,7 @@ static void smem_need(const Shapes &s, int n_cta, size_t *sa, size_t *sb) {
                           (s.bits != 4 ? fix_bytes(s.d, 4) + (size_t)(s.d / 32) * 8 : 0) +
                           (nh + 1) * 4 + (nh * (2 * s.K + 1) + 1) * 4 +
                           2 * kMaxR * 4 + kWarps * 32 * 4 + ((wb / sp.P + 2) * 2 * kMaxR + 1) * 4 +
-                          32 * 4 + (kMaxK + 1) * 4 + 16;
+                          32 * 4 + (kMaxK + 1) * 4 + 24;      // two mbarriers (8-aligned)
             if (need > a) a = need;
         }
     }
@@ -1144,33 +1158,80 @@ static int launch(Kern k, const CP &p, int grid, int threads, size_t smem, bool 
     return MOE_OK;
 }
 
+// Once per (device, BITS) and host thread: every chain kernel may use the
+// device's largest dynamic shared memory and asks for the same (largest)
+// carveout -- an SM only holds CTAs of one carveout at a time, and a kernel
+// with a smaller one would wait for the SM to drain instead of starting
+// beside its predecessor.
 template <int BITS>
-static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float *out,
-               int32_t *ridx, float *rw, float *rmargin, int t, uint8_t *ws, cudaStream_t st) {
-    const int n_cta = sms_of_device();
-    const Ws W = ws_layout(s.d, s.F, s.E, s.H, s.S, s.depth, n_cta);
-    size_t sa, sb;
-    smem_need(s, n_cta, &sa, &sb);
-    int dev = 0, smem_max = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (sa > (size_t)smem_max || sb > (size_t)smem_max)
-        return fail(MOE_EUNSUPPORTED, "decode_step_chain: %zu / %zu bytes of shared memory (at most %d)",
-                    sa, sb, smem_max);
-    const size_t sr = padded(s.d, 32) * 4 + (size_t)(s.d / 32) * 4 + 32 * 4 + 16;
-    // every kernel of the chain asks for the same (largest) shared-memory
-    // carveout: an SM only holds CTAs of one carveout at a time, and a kernel
-    // with a smaller one would wait for the SM to drain instead of starting
-    // beside its predecessor
+static int configure(int dev, int smem_max) {
+    static thread_local int done_dev = -1;
+    if (done_dev == dev) return MOE_OK;
     const int co = cudaSharedmemCarveoutMaxShared;
-    if (cudaFuncSetAttribute(chain_a_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sa) != cudaSuccess ||
-        cudaFuncSetAttribute(chain_b_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sb) != cudaSuccess ||
+    if (cudaFuncSetAttribute(chain_a_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_b_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess ||
         cudaFuncSetAttribute(chain_a_kernel<BITS>, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
         cudaFuncSetAttribute(chain_b_kernel<BITS>, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
         cudaFuncSetAttribute(chain_r_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
         cudaFuncSetAttribute(chain_topk_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess ||
         cudaFuncSetAttribute(chain_rank_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, co) != cudaSuccess)
         return fail(MOE_ECUDA, "decode_step_chain: shared-memory attribute");
+    done_dev = dev;
+    return MOE_OK;
+}
+
+// Residency of the two per-layer kernels on the current device: CTAs of each
+// an SM holds alone (occupancy API), and whether an SM holds a CTA of A
+// beside one of B (shared memory incl. the per-CTA reservation, registers
+// in their allocation granules) -- what lets A(N+1) stream its weights
+// while B(N) runs.
+template <int BITS>
+static int residency(const Shapes &s, int n_cta, moe_chain_info *info) {
+    size_t sa, sb;
+    smem_need(s, n_cta, &sa, &sb);
+    int dev = 0, smem_max = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev);
+    *info = moe_chain_info{};
+    info->smem_a = sa;
+    info->smem_b = sb;
+    info->threads = kThreads;
+    if (sa > (size_t)smem_max || sb > (size_t)smem_max)
+        return fail(MOE_EUNSUPPORTED, "decode_step_chain: %zu / %zu bytes of shared memory (at most %d)",
+                    sa, sb, smem_max);
+    if (int rc = configure<BITS>(dev, smem_max)) return rc;
+    cudaFuncAttributes fa{}, fb{};
+    if (cudaFuncGetAttributes(&fa, chain_a_kernel<BITS>) != cudaSuccess ||
+        cudaFuncGetAttributes(&fb, chain_b_kernel<BITS>) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&info->ctas_a, chain_a_kernel<BITS>, kThreads, sa) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&info->ctas_b, chain_b_kernel<BITS>, kThreads, sb) != cudaSuccess)
+        return fail(MOE_ECUDA, "decode_step_chain: kernel attributes / occupancy");
+    info->regs_a = fa.numRegs;
+    info->regs_b = fb.numRegs;
+    info->local_bytes_a = (int)fa.localSizeBytes;
+    info->local_bytes_b = (int)fb.localSizeBytes;
+    const auto granule = [](int r) { return (r + 7) / 8 * 8; };
+    info->coresident = sa + sb + 2 * (size_t)reserved <= (size_t)smem_sm &&
+                       (granule(fa.numRegs) + granule(fb.numRegs)) * kThreads <= regs_sm &&
+                       info->ctas_a >= 1 && info->ctas_b >= 1;
+    if (info->ctas_a < 1 || info->ctas_b < 1)
+        return fail(MOE_EUNSUPPORTED, "decode_step_chain: a kernel does not fit an SM (%d / %d CTAs)",
+                    info->ctas_a, info->ctas_b);
+    return MOE_OK;
+}
+
+template <int BITS>
+static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float *out,
+               int32_t *ridx, float *rw, float *rmargin, int t, uint8_t *ws, cudaStream_t st) {
+    const int n_cta = sms_of_device();
+    const Ws W = ws_layout(s.d, s.F, s.E, s.H, s.S, s.depth, n_cta);
+    moe_chain_info info;
+    if (int rc = residency<BITS>(s, n_cta, &info)) return rc;
+    const size_t sa = info.smem_a, sb = info.smem_b;
+    const size_t sr = padded(s.d, 32) * 4 + (size_t)(s.d / 32) * 4 + 32 * 4 + 16;
     int32_t *err = reinterpret_cast<int32_t *>(ws);
     if (cudaMemsetAsync(err, 0, sizeof(int32_t), st) != cudaSuccess)
         return fail(MOE_ECUDA, "decode_step_chain: status reset");
@@ -1205,6 +1266,7 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
     b.rw = rw;
     b.rmargin = rmargin;
     b.err = err;
+    b.timeout_ns = sd->timeout_ns ? sd->timeout_ns : kDefaultWaitNs;
     b.trace = sd->debug_trace;
     int lid = 0;
     const moe_experts_desc &e0 = sd->experts[0];
@@ -1260,8 +1322,10 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
         p.vp = vp + (size_t)N * vps;
         next_lora(p, N + 1);
         p.launch_id = lid++;
+        p.debug_unset_wait = N == 0 ? sd->debug_unset_wait : 0;
         if (int rc = launch(chain_a_kernel<BITS>, p, n_cta, kThreads, sa, !first, st, "A")) return rc;
         first = false;
+        p.debug_unset_wait = 0;
         p.launch_id = lid++;
         if (int rc = launch(chain_b_kernel<BITS>, p, n_cta, kThreads, sb, true, st, "B")) return rc;
     }
@@ -1297,6 +1361,15 @@ extern "C" size_t moe_decode_step_chain_workspace_bytes(const moe_stack_desc *sd
     const chain::Shapes s = chain::shapes_of(sd);
     const int sms = chain::sms_of_device();
     return chain::ws_layout(s.d, s.F, s.E, s.H, s.S, s.depth, sms > 0 ? sms : 256).total;
+}
+
+extern "C" int moe_decode_step_chain_info(const moe_stack_desc *sd, moe_chain_info *info) {
+    if (info == nullptr) return fail(MOE_EINVAL, "decode_step_chain_info: NULL info");
+    if (int rc = check_decode_stack(sd)) return rc;
+    const chain::Shapes s = chain::shapes_of(sd);
+    const int n = chain::sms_of_device();
+    if (n <= 0) return fail(MOE_ECUDA, "decode_step_chain_info: no device");
+    return s.bits == 4 ? chain::residency<4>(s, n, info) : chain::residency<2>(s, n, info);
 }
 
 extern "C" int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, float *out,

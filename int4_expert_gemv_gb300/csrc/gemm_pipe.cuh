@@ -60,7 +60,20 @@ constexpr int kStageB = ((kEntOff + kTok * 4) + 1023) / 1024 * 1024;
 constexpr int kOutLd = kTok + 1;               // epilogue staging row (floats)
 static_assert(kRB * kOutLd * 4 <= kEntOff, "the epilogue staging would overwrite the entries");
 
-constexpr uint32_t kWaitLimit = 1u << 22;      // polls of a bounded wait (seconds)
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // a wait's bound unless set
+
+// Bounds of the engine's device-side waits, process-wide (host side):
+// timeout_ns (0 = kDefaultWaitNs) and a test hook -- stall != 0 makes
+// consumer warp 0 of CTA 0 wait for bytes no copy sends, so that wait runs
+// out and the launch takes its expiry path.
+struct WaitCfg {
+    unsigned long long timeout_ns;
+    int stall;
+};
+inline WaitCfg &wait_cfg() {
+    static WaitCfg w{0, 0};
+    return w;
+}
 
 // Offset c of the bf16 code values (c + q).
 template <int BITS> struct CodeOff;
@@ -163,13 +176,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 // Bounded wait of a whole warp for the phase of `bar` with `parity`: lane 0
-// polls, the outcome is shared, then every lane observes the completed phase
-// itself (its acquire of the stage's data).  Returns false on expiry.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity) {
+// polls (for at most timeout_ns), the outcome is shared, then every lane
+// observes the completed phase itself (its acquire of the stage's data).
+// Returns false on expiry.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, uint64_t timeout_ns) {
     uint32_t ok = 0;
     if ((threadIdx.x & 31) == 0) {
-        for (uint32_t i = 0; i < kWaitLimit && !ok; i++) ok = mbar_try_wait(bar, parity);
+        ok = mbar_try_wait(bar, parity);
+        const uint64_t t0 = ok ? 0 : globaltimer_ns();
+        for (uint32_t i = 1; !ok; i++) {
+            ok = mbar_try_wait(bar, parity);
+            if (!ok && (i & 15) == 0 && globaltimer_ns() - t0 > timeout_ns) break;
+        }
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) mbar_try_wait(bar, parity);
@@ -318,19 +343,22 @@ __device__ __forceinline__ void mma_chunk(const uint8_t *stage, int rw, int g0, 
 // Dynamic shared memory: alignment slack, kStages stages, 2 kStages
 // mbarriers, the scratch.
 template <int BITS, class Job>
-__global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constant__ Job job) {
+__global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constant__ Job job,
+                                                            const uint64_t timeout_ns, const int stall) {
     extern __shared__ __align__(1024) uint8_t smdyn[];
     // stages on a 1024-byte boundary (TMA destinations), whatever the base
     uint8_t *smraw = smdyn + ((1024u - (saddr(smdyn) & 1023u)) & 1023u);
     uint64_t *full = reinterpret_cast<uint64_t *>(smraw + kStages * kStageB);
     uint64_t *empty = full + kStages;
-    int32_t *sm = reinterpret_cast<int32_t *>(empty + kStages);
+    uint64_t *stall_bar = empty + kStages;          // the test hook's wait
+    int32_t *sm = reinterpret_cast<int32_t *>(stall_bar + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; s++) {
             mbar_init(full + s, 1);
             mbar_init(empty + s, kConsumers);
         }
+        mbar_init(stall_bar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     job.init(sm);
@@ -352,7 +380,7 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
         for (; q < nq; q++) {
             const int s = q % kStages;
             uint8_t *stage = smraw + s * kStageB;
-            if (q >= kStages && !warp_wait(empty + s, ((q / kStages) - 1) & 1)) {
+            if (q >= kStages && !warp_wait(empty + s, ((q / kStages) - 1) & 1, timeout_ns)) {
                 if (lane == 0) atomicExch(job.err, MOE_ETIMEOUT);
                 break;
             }
@@ -386,7 +414,7 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
         // the copies of the last fill of each stage land before the CTA exits
         for (int s = 0; s < kStages && s < q; s++) {
             const int last = q - 1 - ((q - 1 - s) % kStages);     // last chunk issued on s
-            if (!warp_wait(full + s, (last / kStages) & 1) && lane == 0)
+            if (!warp_wait(full + s, (last / kStages) & 1, timeout_ns) && lane == 0)
                 atomicExch(job.err, MOE_ETIMEOUT);
         }
         return;
@@ -396,6 +424,16 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
     // warp w: records (w % 8) * 16 .., column groups 2 (w / 8), 2 (w / 8) + 1
     const int tid = threadIdx.x, rw = warp % kRowWarps, kh = warp / kRowWarps;
     bool dead = false;
+    if (stall && blockIdx.x == 0 && warp == 0) {
+        // test hook: 16 bytes that no copy sends; the wait runs out and this
+        // warp goes on as a warp whose stage never arrived
+        if (lane == 0) mbar_expect_tx(stall_bar, 16);
+        __syncwarp();
+        if (!warp_wait(stall_bar, 0, timeout_ns)) {
+            dead = true;
+            if (lane == 0) atomicExch(job.err, MOE_ETIMEOUT);
+        }
+    }
     float total[8][4];
 #pragma unroll
     for (int u = 0; u < 8; u++)
@@ -407,7 +445,7 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
     for (int q = 0; q < nq; q++) {
         const int s = q % kStages;
         uint8_t *stage = smraw + s * kStageB;
-        if (!dead && !warp_wait(full + s, (q / kStages) & 1)) {
+        if (!dead && !warp_wait(full + s, (q / kStages) & 1, timeout_ns)) {
             dead = true;
             if (lane == 0) atomicExch(job.err, MOE_ETIMEOUT);
         }
@@ -451,10 +489,13 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
 template <int BITS, class Job>
 inline int launch_pipe_gemm(const Job &job, size_t scratch_bytes, int sms, cudaStream_t st,
                             const char *name) {
-    const size_t smem = 1024 + (size_t)kStages * kStageB + 2 * kStages * sizeof(uint64_t) + scratch_bytes;
+    const size_t smem = 1024 + (size_t)kStages * kStageB + (2 * kStages + 1) * sizeof(uint64_t) +
+                        scratch_bytes;
     cudaFuncSetAttribute(pipe_gemm_kernel<BITS, Job>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (int)smem);
-    pipe_gemm_kernel<BITS, Job><<<sms, kThr, smem, st>>>(job);
+    const WaitCfg w = wait_cfg();
+    pipe_gemm_kernel<BITS, Job><<<sms, kThr, smem, st>>>(job, w.timeout_ns ? w.timeout_ns : kDefaultWaitNs,
+                                                          w.stall);
     return check_launch(name);
 }
 

@@ -395,3 +395,8 @@ int launch_expert_ffn_grouped(const FfnParams &p, cudaStream_t st) {
 }
 
 }  // namespace moe
+
+extern "C" int moe_debug_batched_waits(unsigned long long timeout_ns, int stall) {
+    moe::pipe::wait_cfg() = moe::pipe::WaitCfg{timeout_ns, stall ? 1 : 0};
+    return MOE_OK;
+}

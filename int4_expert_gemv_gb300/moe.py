@@ -57,6 +57,13 @@ class StackDesc(C.Structure):
                 ("inflight_bytes", C.c_uint)]
 
 
+class ChainInfo(C.Structure):
+    _fields_ = [("smem_a", C.c_size_t), ("smem_b", C.c_size_t), ("threads", C.c_int),
+                ("regs_a", C.c_int), ("regs_b", C.c_int),
+                ("local_bytes_a", C.c_int), ("local_bytes_b", C.c_int),
+                ("ctas_a", C.c_int), ("ctas_b", C.c_int), ("coresident", C.c_int)]
+
+
 # ------------------------------------------------------------------ loading
 def lib():
     global _lib
@@ -78,6 +85,7 @@ def lib():
                 "moe_gather_experts": (I, [P, S, I, P, I, S, P, S, P, P]),
                 "moe_pack_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "moe_debug_dequant": (I, [P, I, I, I, I, P, P]),
+                "moe_debug_batched_waits": (I, [C.c_ulonglong, I]),
                 "moe_prerouter_head_workspace_bytes": (S, [C.POINTER(HeadDesc), I]),
                 "moe_prerouter_head": (I, [C.POINTER(HeadDesc), P, I, P, P, I, I, P, P, S, P]),
                 "moe_topk_route": (I, [P, I, I, I, P, P, P, P]),
@@ -85,11 +93,13 @@ def lib():
                 "moe_expert_ffn_int4": (I, [C.POINTER(ExpertsDesc), P, I, P, I, I, P, P, S, P]),
                 "moe_combine_residual": (I, [P, P, I, I, I, I, P, P, P, P]),
                 "moe_expert_ffn_int4_noalloc": (I, [C.POINTER(ExpertsDesc), P, I, P, I, I, P, P]),
+                "moe_expert_ffn_noalloc_status": (I, [C.POINTER(C.c_int), P]),
                 "moe_decode_step_workspace_bytes": (S, [C.POINTER(StackDesc)]),
                 "moe_decode_step": (I, [C.POINTER(StackDesc), P, P, P, P, P, I, P, S, P]),
                 "moe_decode_step_status": (I, [P, C.POINTER(C.c_int), P]),
                 "moe_decode_step_chain_workspace_bytes": (S, [C.POINTER(StackDesc)]),
                 "moe_decode_step_chain": (I, [C.POINTER(StackDesc), P, P, P, P, P, I, P, S, P]),
+                "moe_decode_step_chain_info": (I, [C.POINTER(StackDesc), C.POINTER(ChainInfo)]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -194,6 +204,13 @@ def moe_pack_experts(d, F, E, bits, gate_q, gate_s, gate_b, up_q, up_s, up_b, do
                                   _stream(stream)), "moe_pack_experts")
 
 
+def moe_debug_batched_waits(timeout_ns: int, stall: bool) -> None:
+    """Test hook: the batched engine's wait bound (0 = 1 s) and a wait that
+    nothing satisfies in every later launch (stall)."""
+    _check(lib().moe_debug_batched_waits(int(timeout_ns), int(bool(stall))),
+           "moe_debug_batched_waits")
+
+
 def moe_debug_dequant(blob, d: int, F: int, bits: int, which: int, out, stream=None):
     _check(lib().moe_debug_dequant(_ptr(blob), d, F, bits, which, _ptr(out), _stream(stream)),
            "moe_debug_dequant")
@@ -240,6 +257,15 @@ def moe_expert_ffn_int4_noalloc(ed: ExpertsDesc, x, idx, T: int, K: int, y_slots
            "moe_expert_ffn_int4_noalloc")
 
 
+def moe_expert_ffn_noalloc_status(stream=None) -> int:
+    """Status word of the last allocation-free expert call on the current
+    device (synchronises the stream): MOE_OK or MOE_ETIMEOUT."""
+    st = C.c_int(0)
+    _check(lib().moe_expert_ffn_noalloc_status(C.byref(st), _stream(stream)),
+           "moe_expert_ffn_noalloc_status")
+    return st.value
+
+
 # ------------------------------------------------------------------ stack
 def moe_decode_step_workspace_bytes(sd: StackDesc) -> int:
     return lib().moe_decode_step_workspace_bytes(C.byref(sd))
@@ -261,6 +287,15 @@ def moe_decode_step_chain(sd: StackDesc, x0, out, route_idx, route_w, route_marg
     _check(lib().moe_decode_step_chain(C.byref(sd), _ptr(x0), _ptr(out), _ptr(route_idx),
                                        _ptr(route_w), _ptr(route_margin), t, _ptr(ws), _nbytes(ws),
                                        _stream(stream)), "moe_decode_step_chain")
+
+
+def moe_decode_step_chain_info(sd: StackDesc) -> dict:
+    """How the chain's two per-layer kernels sit on an SM of the current
+    device (shared memory, registers, CTAs per SM, co-residency)."""
+    info = ChainInfo()
+    _check(lib().moe_decode_step_chain_info(C.byref(sd), C.byref(info)),
+           "moe_decode_step_chain_info")
+    return {k: getattr(info, k) for k, _ in ChainInfo._fields_}
 
 
 def moe_decode_step_status(ws, stream=None) -> int:
