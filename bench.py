@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--lora-merge", action="store_true",
                     help="time merging the shared-expert adapters into the int4 weights "
                          "(moe_merge_lora) and report the retained delta")
+    ap.add_argument("--engine", default="auto", choices=["auto", "mma_sync", "tcgen05"],
+                    help="batched configs: the grouped-GEMM engine (auto: the library's "
+                         "default, the register engine)")
     ap.add_argument("--path", default="chain", choices=["chain", "fused", "per-call"],
                     help="chain: two kernels per layer chained by programmatic dependent "
                          "launch; fused: one persistent kernel per step; per-call: the "
@@ -553,6 +556,8 @@ def run_batched(args, cfg):
     torch.cuda.set_device(local)
     __graft_entry__.build()
     T = cfg.T
+    from int4_expert_gemv_gb300 import moe
+    moe.moe_debug_batched_engine({"auto": 0, "mma_sync": 1, "tcgen05": 2}[args.engine])
     dm = DeviceModel(cfg)
     bl = BatchedLayer(dm, T)
     x0 = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0), (T, cfg.d), 1.0))
@@ -647,6 +652,7 @@ def run_batched(args, cfg):
                 "distinct_experts": distinct,
                 "l2": "flushed (2x L2 written) before every timed step",
                 "graphs": "each step replayed from a captured CUDA graph",
+                "engine": args.engine,
             },
             "expert_weight_gbs": ffn_bytes / (ms_step / 1000.0) / 1e9,
             "ffn_tflops": ffn_flops / (ffn_avg / 1000.0) / 1e12,

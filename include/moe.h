@@ -161,6 +161,25 @@ int moe_debug_dequant(const void *blob, int d, int F, int bits, int which,
  * moe_debug_batched_waits(0, 0) restores the defaults. */
 int moe_debug_batched_waits(unsigned long long timeout_ns, int stall);
 
+/* Test and measurement hook, process-wide: which engine runs the batched
+ * path's grouped GEMMs.  0 (default) or 1: the register engine (mma.sync,
+ * fp32 accumulators in registers); 2: the tensor-memory engine (tcgen05.mma,
+ * fp32 accumulators in TMEM) when its shared memory fits and the GEMM's
+ * columns are a multiple of 128, else the register engine.  Both give
+ * results within the same tolerance of the exact sums (the per-group affine
+ * terms are applied in fp32 to exact bf16 partial sums either way); the
+ * register engine is the faster of the two on GB300 at every batch size
+ * measured (8 to 4096 tokens), hence the default. */
+int moe_debug_batched_engine(int mode);
+
+/* Profiling hook, process-wide: a device buffer of 64 * 16 u64 that CTA 0 of
+ * the next tensor-memory engine launch fills with %globaltimer stamps of
+ * its first 64 chunks (per chunk: producer issue, converters see / release
+ * groups 0-3, MMA warp sees the stage / issues groups 0-3, epilogue sees
+ * accumulators 0-3, epilogue releases the stage); NULL turns it off.  The
+ * hook is cleared by that launch. */
+int moe_debug_batched_trace(unsigned long long *buf);
+
 /* ---------------------------------------------------------------- head */
 typedef struct {
     int d;                    /* d_model                                      */

@@ -90,6 +90,14 @@ struct Item {
 // activation rows; their per-group sums.
 struct Maps {
     CUtensorMap codes[2], sb[2], act, gsum;
+    // for the tcgen05 engine (gemm_umma.cuh): the codes of a chunk (4-bit:
+    // one 128-byte box per record, 128-byte swizzle; 2-bit: one 16-byte box
+    // per record and group), activations in 64-column boxes with the 128-byte
+    // swizzle of the tensor cores' K-major operand layout and their group
+    // sums, each in boxes of 8, 16, 32 or 64 rows
+    CUtensorMap gcodes[2], act128[4], gsum4[4];
+    // the register engine's activations in boxes of 8, 16, 32 or 64 rows
+    CUtensorMap act4[4];
 };
 
 // ---------------------------------------------------------------- host
@@ -107,12 +115,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 }
 
 inline int encode_map(CUtensorMap *m, CUtensorMapDataType dt, int rank, const void *base,
-                      const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box) {
+                      const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+                      CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_NONE) {
     const PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
     if (fn == nullptr) return MOE_ECUDA;
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     const CUresult r = fn(m, dt, (cuuint32_t)rank, const_cast<void *>(base), dims, strides, box, es,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? MOE_OK : MOE_ECUDA;
 }
@@ -128,6 +137,15 @@ inline int weight_maps(Maps &m, int which, const void *base, size_t rec, int nro
     const cuuint32_t bs[3] = {16, kRB, 1};
     if (int rc = encode_map(&m.codes[which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, bc))
         return rc;
+    if (bits == 4) {
+        if (int rc = encode_map(&m.gcodes[which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, bc,
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return rc;
+    } else {
+        const cuuint32_t bg[3] = {(cuuint32_t)(kGroup * bits / 8), kRB, 1};
+        if (int rc = encode_map(&m.gcodes[which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, bg))
+            return rc;
+    }
     return encode_map(&m.sb[which], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, bs);
 }
 
@@ -143,6 +161,17 @@ inline int act_maps(Maps &m, const void *act, const float *gsum, int rows, int c
     if (int rc = encode_map(&m.act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, act, da, sa, ba)) return rc;
     const cuuint64_t dg[2] = {(cuuint64_t)(cols / kGroup), (cuuint64_t)rows};
     const cuuint64_t sg[1] = {(cuuint64_t)gsum_ld(cols) * 4};
+    for (int i = 0; i < 4; i++) {                  // boxes of 8 << i rows
+        const cuuint32_t bai[2] = {kKc, (cuuint32_t)(kRowBox << i)};
+        if (int rc = encode_map(&m.act4[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, act, da, sa, bai)) return rc;
+        const cuuint32_t b128[2] = {kGroup, (cuuint32_t)(kRowBox << i)};
+        if (int rc = encode_map(&m.act128[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, act, da, sa, b128,
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return rc;
+        const cuuint32_t bgi[2] = {kGpc, (cuuint32_t)(kRowBox << i)};
+        if (int rc = encode_map(&m.gsum4[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, gsum, dg, sg, bgi))
+            return rc;
+    }
     const cuuint32_t bg[2] = {kGpc, kRowBox};
     return encode_map(&m.gsum, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, gsum, dg, sg, bg);
 }
@@ -338,8 +367,8 @@ __device__ __forceinline__ void mma_chunk(const uint8_t *stage, int rw, int g0, 
 //   weights(it, map, row, blob): the tensor-map coordinates of its records,
 //   row0(sm, it): its first activation row (the rest follow),
 //   meta(sm, it): nt words for the epilogue (or null),
-//   epilogue(sm, it, out, ent, tid): out[r * kOutLd + t] = record r's dot
-//     with token t; tid in [0, kConsumers * 32) of the consumer threads.
+//   epilogue(sm, it, out, ent, tid, nthr): out[r * kOutLd + t] = record r's
+//     dot with token t; tid in [0, nthr) of the threads that run it.
 // Dynamic shared memory: alignment slack, kStages stages, 2 kStages
 // mbarriers, the scratch.
 template <int BITS, class Job>
@@ -390,22 +419,24 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
                 if (m != nullptr)
                     for (int t = lane; t < it.nt; t += 32) ent[t] = m[t];
             }
+            // the chunk's four copies (codes, {s, b}, the activation rows in one
+            // box of 8, 16, 32 or 64 rows, their group sums), each from a lane
+            // of its own: one lane issues a copy only every ~200 ns
+            const int bk = it.nt <= 8 ? 0 : it.nt <= 16 ? 1 : it.nt <= 32 ? 2 : 3;
+            const int rows = kRowBox << bk;
+            if (lane == 0) mbar_expect_tx(full + s, kCodeBytes + kRB * 16 + rows * (kXRow + 16));
             __syncwarp();
-            if (lane == 0) {
-                const int nbox = (it.nt + kRowBox - 1) / kRowBox;
-                mbar_expect_tx(full + s, kCodeBytes + kRB * 16 + nbox * kRowBox * (kXRow + 16));
-                int map, row, blob;
-                job.weights(it, map, row, blob);
+            int map, row, blob;
+            job.weights(it, map, row, blob);
+            const int r0 = job.row0(sm, it);
+            if (lane == 0)
                 tma_3d(stage, &job.maps.codes[map], lc * kKc * BITS / 8, row, blob, full + s, policy);
+            else if (lane == 1)
                 tma_3d(stage + kSbOff, &job.maps.sb[map], cbytes + 16 * lc, row, blob, full + s, policy);
-                const int r0 = job.row0(sm, it);
-                for (int x = 0; x < nbox; x++) {
-                    tma_2d(stage + kXOff + x * kRowBox * kXRow, &job.maps.act, lc * kKc,
-                           r0 + x * kRowBox, full + s);
-                    tma_2d(stage + kXsOff + x * kRowBox * 16, &job.maps.gsum, lc * kGpc,
-                           r0 + x * kRowBox, full + s);
-                }
-            }
+            else if (lane == 2)
+                tma_2d(stage + kXOff, &job.maps.act4[bk], lc * kKc, r0, full + s);
+            else if (lane == 3)
+                tma_2d(stage + kXsOff, &job.maps.gsum4[bk], lc * kGpc, r0, full + s);
             if (++lc == nch) {
                 lc = 0;
                 if (++li < mine) it = job.item(sm, b + li * nb);
@@ -471,7 +502,8 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
                 }
             }
             consumers_sync();
-            job.epilogue(sm, it, out, reinterpret_cast<const int32_t *>(stage + kEntOff), tid);
+            job.epilogue(sm, it, out, reinterpret_cast<const int32_t *>(stage + kEntOff), tid,
+                         kConsumers * 32);
 #pragma unroll
             for (int u = 0; u < 8; u++)
 #pragma unroll

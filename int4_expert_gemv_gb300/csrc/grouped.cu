@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 
 #include "gemm_pipe.cuh"
+#include "gemm_umma.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -261,14 +262,14 @@ struct FfnJob {
     }
 
     __device__ void epilogue(const int32_t *sm, const Item &it, const float *out,
-                             const int32_t *ent, int tid) const {
+                             const int32_t *ent, int tid, int nthr) const {
         const int nr = min(kRB, nrows - it.rb * kRB);
         const int pos0 = row0(sm, it);
         const bool shared = it.g == p.E;
         if (!DOWN) {
             // gate/up: records 2 fl (gate) and 2 fl + 1 (up) give h[f], f = rb * 64 + fl
             constexpr int kF = kRB / 2;
-            for (int o = tid; o < it.nt * kF; o += kConsumers * 32) {
+            for (int o = tid; o < it.nt * kF; o += nthr) {
                 const int t = o / kF, fl = o - t * kF;
                 if (2 * fl >= nr) continue;
                 const int f = it.rb * kF + fl;
@@ -296,7 +297,7 @@ struct FfnJob {
             }
         } else {
             // down: record ol gives y[o], o = rb * 128 + ol
-            for (int o = tid; o < it.nt * kRB; o += kConsumers * 32) {
+            for (int o = tid; o < it.nt * kRB; o += nthr) {
                 const int t = o / kRB, ol = o - t * kRB;
                 if (ol >= nr) continue;
                 const int oo = it.rb * kRB + ol;
@@ -373,7 +374,9 @@ static int launch_bits(const FfnParams &p, cudaStream_t st) {
     const int sms = num_sms();
     FfnJob<false> gu;
     if (int rc = gu.make(p, p.item_off)) return rc;
-    if (int rc = launch_pipe_gemm<BITS>(gu, scratch, sms, st, "pipe_gemm_kernel (gate/up)"))
+    // mean tokens of a routed expert's group: the engine choice
+    const double mean_tok = (double)p.T * p.K / p.E;
+    if (int rc = umma::launch_batched_gemm<BITS>(gu, scratch, sms, st, "batched gemm (gate/up)", mean_tok))
         return rc;
     if (int rc = launch_group_sums(p.h16, npos, p.F, p.hsum, st)) return rc;
     if (p.lora[2].r || (p.shared && p.shared_lora[2].r)) {
@@ -385,7 +388,7 @@ static int launch_bits(const FfnParams &p, cudaStream_t st) {
     }
     FfnJob<true> dn;
     if (int rc = dn.make(p, p.item_off + G + 1)) return rc;
-    return launch_pipe_gemm<BITS>(dn, scratch, sms, st, "pipe_gemm_kernel (down)");
+    return umma::launch_batched_gemm<BITS>(dn, scratch, sms, st, "batched gemm (down)", mean_tok);
 }
 
 }  // namespace grouped
@@ -395,6 +398,17 @@ int launch_expert_ffn_grouped(const FfnParams &p, cudaStream_t st) {
 }
 
 }  // namespace moe
+
+extern "C" int moe_debug_batched_trace(unsigned long long *buf) {
+    moe::umma::trace_buf() = buf;
+    return MOE_OK;
+}
+
+extern "C" int moe_debug_batched_engine(int mode) {
+    if (mode < 0 || mode > 2) return moe::fail(MOE_EINVAL, "debug_batched_engine: mode %d", mode);
+    moe::umma::engine_mode() = mode;
+    return MOE_OK;
+}
 
 extern "C" int moe_debug_batched_waits(unsigned long long timeout_ns, int stall) {
     moe::pipe::wait_cfg() = moe::pipe::WaitCfg{timeout_ns, stall ? 1 : 0};

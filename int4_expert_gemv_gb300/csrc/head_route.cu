@@ -12,6 +12,7 @@
 #include <cfloat>
 
 #include "gemm_pipe.cuh"
+#include "gemm_umma.cuh"
 #include "internal.h"
 
 namespace moe {
@@ -229,11 +230,11 @@ struct HeadXJob {
     __device__ int row0(const int32_t *, const pipe::Item &it) const { return it.t0; }
     __device__ const int32_t *meta(const int32_t *, const pipe::Item &) const { return nullptr; }
     __device__ void epilogue(const int32_t *, const pipe::Item &it, const float *out,
-                             const int32_t *, int tid) const {
+                             const int32_t *, int tid, int nthr) const {
         const bool fc1 = it.rb < RB0;
         const int base = (fc1 ? it.rb : it.rb - RB0) * pipe::kRB;
         const int nr = min(pipe::kRB, (fc1 ? p.H : p.E) - base);
-        for (int o = tid; o < it.nt * pipe::kRB; o += pipe::kConsumers * 32) {
+        for (int o = tid; o < it.nt * pipe::kRB; o += nthr) {
             const int t = o / pipe::kRB, rl = o - t * pipe::kRB;
             if (rl >= nr) continue;
             const int tok = it.t0 + t, r = base + rl;
@@ -293,10 +294,10 @@ struct Fc2Job {
     __device__ int row0(const int32_t *, const pipe::Item &it) const { return it.t0; }
     __device__ const int32_t *meta(const int32_t *, const pipe::Item &) const { return nullptr; }
     __device__ void epilogue(const int32_t *, const pipe::Item &it, const float *out,
-                             const int32_t *, int tid) const {
+                             const int32_t *, int tid, int nthr) const {
         const int base = it.rb * pipe::kRB;
         const int nr = min(pipe::kRB, p.E - base);
-        for (int o = tid; o < (it.nt / 2) * pipe::kRB; o += pipe::kConsumers * 32) {
+        for (int o = tid; o < (it.nt / 2) * pipe::kRB; o += nthr) {
             const int tl = o / pipe::kRB, rl = o - tl * pipe::kRB;
             if (rl >= nr) continue;
             const int tok = (it.t0 >> 1) + tl, e = base + rl;
@@ -316,13 +317,13 @@ int launch_prerouter_head(const HeadParams &p, cudaStream_t st) {
         if (cudaMemsetAsync(p.err, 0, sizeof(int32_t), st) != cudaSuccess) return MOE_ECUDA;
         HeadXJob job;
         if (int rc = job.make(p)) return rc;
-        if (int rc = pipe::launch_pipe_gemm<4>(job, 0, num_sms(), st, "pipe_gemm_kernel (head fc1, l)"))
+        if (int rc = umma::launch_batched_gemm<4>(job, 0, num_sms(), st, "batched gemm (head fc1, l)", p.T))
             return rc;
         if (p.H > 0) {
             if (int rc = pipe::launch_group_sums(p.gg, 2 * p.T, p.H, p.ggsum, st)) return rc;
             Fc2Job f2;
             if (int rc = f2.make(p)) return rc;
-            return pipe::launch_pipe_gemm<4>(f2, 0, num_sms(), st, "pipe_gemm_kernel (head fc2)");
+            return umma::launch_batched_gemm<4>(f2, 0, num_sms(), st, "batched gemm (head fc2)", 2.0 * p.T);
         }
         return MOE_OK;
     } else {

@@ -86,6 +86,8 @@ def lib():
                 "moe_pack_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "moe_debug_dequant": (I, [P, I, I, I, I, P, P]),
                 "moe_debug_batched_waits": (I, [C.c_ulonglong, I]),
+                "moe_debug_batched_engine": (I, [I]),
+                "moe_debug_batched_trace": (I, [P]),
                 "moe_prerouter_head_workspace_bytes": (S, [C.POINTER(HeadDesc), I]),
                 "moe_prerouter_head": (I, [C.POINTER(HeadDesc), P, I, P, P, I, I, P, P, S, P]),
                 "moe_topk_route": (I, [P, I, I, I, P, P, P, P]),
@@ -209,6 +211,18 @@ def moe_debug_batched_waits(timeout_ns: int, stall: bool) -> None:
     nothing satisfies in every later launch (stall)."""
     _check(lib().moe_debug_batched_waits(int(timeout_ns), int(bool(stall))),
            "moe_debug_batched_waits")
+
+
+def moe_debug_batched_engine(mode: int) -> None:
+    """Which engine runs the batched GEMMs: 0 by size, 1 register
+    (mma.sync), 2 tensor memory (tcgen05)."""
+    _check(lib().moe_debug_batched_engine(int(mode)), "moe_debug_batched_engine")
+
+
+def moe_debug_batched_trace(buf) -> None:
+    """Profiling hook: stamps of CTA 0 of later tensor-memory engine launches
+    into buf (device u64 [64 * 16]), or off (None)."""
+    _check(lib().moe_debug_batched_trace(_ptr(buf)), "moe_debug_batched_trace")
 
 
 def moe_debug_dequant(blob, d: int, F: int, bits: int, which: int, out, stream=None):

@@ -36,6 +36,15 @@ def m():
 _MODELS = {}
 
 
+@pytest.fixture(params=[1, 2], ids=["mma_sync", "tcgen05"])
+def engine(request, m):
+    """Both engines of the grouped GEMMs: the register engine (mma.sync) and
+    the tensor-memory engine (tcgen05.mma, TMEM accumulators)."""
+    m.moe_debug_batched_engine(request.param)
+    yield request.param
+    m.moe_debug_batched_engine(0)
+
+
 def _model(cfg):
     from int4_expert_gemv_gb300.model import DeviceModel
     key = (cfg.d, cfg.F, cfg.E, cfg.bits, cfg.shared, cfg.seed, cfg.lora_on, cfg.lora_r)
@@ -82,7 +91,7 @@ def _check(cfg, got, x, routes, tokens, what):
 
 
 @pytest.mark.parametrize("T,sample", [(8, 0), (64, 0), (512, 48), (4096, 24)])
-def test_batched_parity(m, T, sample):
+def test_batched_parity(m, engine, T, sample):
     cfg = ALL[f"batched-T{T}"]
     routes = synth.routes(cfg.seed, 902, T, cfg.E, cfg.K)
     x = _x(cfg, T)
@@ -102,7 +111,7 @@ def test_batched_is_deterministic(m):
     assert np.array_equal(a.view(np.int64), b.view(np.int64))
 
 
-def test_batched_ragged_tiny_with_invalid_and_repeated(m):
+def test_batched_ragged_tiny_with_invalid_and_repeated(m, engine):
     """T not a multiple of the 64-token tile, F below the 256-column chunk,
     LoRA on the routed down projection, expert indices outside [0, E) (NaN
     slots) and an expert repeated within a token."""
@@ -119,7 +128,7 @@ def test_batched_ragged_tiny_with_invalid_and_repeated(m):
     assert np.array_equal(got[3, 0], got[3, 1])
 
 
-def test_batched_one_expert_beyond_the_tile_grid(m):
+def test_batched_one_expert_beyond_the_tile_grid(m, engine):
     """Every slot of every token on one expert: the expert has T*K entries,
     more than the grid's ceil(T/64) tiles cover in one pass."""
     cfg = TINY
@@ -132,7 +141,7 @@ def test_batched_one_expert_beyond_the_tile_grid(m):
 
 
 @pytest.mark.parametrize("bits", [2, 4])
-def test_batched_wide(m, bits):
+def test_batched_wide(m, engine, bits):
     cfg = replace(ALL[f"wide-int{bits}"], T=64)
     routes = synth.routes(cfg.seed, 906, 64, cfg.E, cfg.K)
     for t in range(8):                   # one expert with 8 tokens, indices still distinct

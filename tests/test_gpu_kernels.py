@@ -190,10 +190,15 @@ def test_prerouter_head_parity(m, cfg, prec):
 
 @pytest.mark.parametrize("cfg,T", [(TINY, 100), (MOE35B, 64), (ALL["wide-int4"], 70)],
                          ids=["tiny-T100", "35b-T64", "wide-T70"])
-def test_prerouter_head_batched_bf16(m, cfg, T):
+@pytest.mark.parametrize("engine", [1, 2], ids=["mma_sync", "tcgen05"])
+def test_prerouter_head_batched_bf16(m, cfg, T, engine):
     """Several bf16 tokens with an int4 head take the batched head (fc1 and l
-    as one tensor-core job over all tokens)."""
-    _head_case(m, cfg, "int4", T, x_dtype=torch.bfloat16)
+    as one tensor-core job over all tokens), on either engine."""
+    m.moe_debug_batched_engine(engine)
+    try:
+        _head_case(m, cfg, "int4", T, x_dtype=torch.bfloat16)
+    finally:
+        m.moe_debug_batched_engine(0)
 
 
 def test_prerouter_head_without_prev_route(m):
