@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--host-tier", action="store_true",
                     help="decode with the routed experts in pinned host memory, gathered into "
                          "HBM a token ahead, against the HBM-resident stack")
+    ap.add_argument("--cache-slots", type=int, default=64,
+                    help="--host-tier with --path chain: HBM cache slots per layer")
+    ap.add_argument("--free-sms", type=int, default=0,
+                    help="--host-tier with --path chain: SMs the chained step leaves to the copies")
     ap.add_argument("--route-agreement", action="store_true",
                     help="measure how often the predicted routes agree with the layers' own "
                          "routers (seeded decode steps)")
@@ -767,6 +771,90 @@ def run_merge(args, cfg):
         print(json.dumps(line), flush=True)
 
 
+def run_host_tier_chain(args, cfg):
+    """Chained decode steps (captured graphs) with the routed experts in
+    pinned host memory behind an LRU cache of --cache-slots experts per layer
+    in HBM (HostTierChain), against the HBM-resident chained step; plus, per
+    layer, when its cache update finishes against when the layer starts."""
+    import torch
+
+    from int4_expert_gemv_gb300 import synth
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel, HostTierChain
+    import __graft_entry__
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    __graft_entry__.build()
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    dm = DeviceModel(cfg)
+    stacks = {"hbm": DecodeStack(dm, fused="chain"),
+              "host": HostTierChain(dm, args.cache_slots, args.free_sms)}
+    total = args.warmup + args.steps
+    xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
+                                       (total + 1, cfg.d), 1.0)).cuda()
+    stream = torch.cuda.current_stream()
+    res = {}
+    tier = stacks["host"]
+    with ClockSampler(local) as clk:
+        for name, st in stacks.items():
+            st.step(xin[0])
+            st.capture()
+            for t in range(1, args.warmup + 1):
+                st.step(xin[t])
+            torch.cuda.synchronize()
+            if st is tier:
+                tier.stats.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for t in range(args.warmup + 1, total + 1):
+                st.step(xin[t])
+            b.record(stream)
+            torch.cuda.synchronize()
+            res[name] = a.elapsed_time(b) / args.steps
+        hits, misses = tier.stats.sum(0).tolist()
+        # when each layer's update finishes (instrumented replays), against
+        # the layer's start in the HBM-resident step (N x its per-layer time)
+        n_rep = 8
+        fin = [[] for _ in range(cfg.depth)]
+        for r in range(n_rep):
+            ev = (torch.cuda.Event(enable_timing=True, external=True),
+                  [torch.cuda.Event(enable_timing=True, external=True) for _ in range(cfg.depth)])
+            g = torch.cuda.CUDAGraph()
+            t = tier.t
+            with torch.cuda.graph(g):
+                tier.enqueue_fused_step(t, update_events=ev)
+            tier.xin.copy_(xin[r])
+            g.replay()
+            tier.t += 1
+            torch.cuda.synchronize()
+            for N in range(1, cfg.depth):
+                fin[N].append(ev[0].elapsed_time(ev[1][N]))
+    per_layer = res["hbm"] / cfg.depth
+    slack = [N * per_layer - statistics.mean(fin[N]) for N in range(1, cfg.depth)]
+    hidden = sum(1 for x in slack if x >= 0)
+    moved = misses * tier.blob
+    print(json.dumps({
+        "metric": "decode tokens/s with the routed experts in host memory behind an HBM cache",
+        "value": 1000.0 / res["host"], "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["host"], "higher_is_better": True,
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "path": "chained step, captured graphs",
+                   "cache_slots_per_layer": args.cache_slots, "free_sms": args.free_sms,
+                   "cache_bytes": tier.cache.numel(),
+                   "host_pool_bytes": sum(h.numel() for h in tier.host_pools)},
+        "hbm_resident": {"ms_per_step": res["hbm"], "tokens_per_s": 1000.0 / res["hbm"]},
+        "cache": {"hits": hits, "misses": misses, "hit_rate": hits / max(1, hits + misses),
+                  "c2c_bytes_per_step": moved / args.steps,
+                  "c2c_gbs": moved / (res["host"] * args.steps / 1000.0) / 1e9},
+        "prefetch": {"layers_hidden": hidden, "layers": cfg.depth - 1,
+                     "slack_ms_min": min(slack), "slack_ms_mean": statistics.mean(slack),
+                     "note": "slack = layer N's start in the HBM-resident step (N x its per-layer "
+                             "time) minus when layer N's cache update finished, from the step's "
+                             "start, mean of 8 instrumented replays; >= 0: the copies hide"},
+        "clocks": clk.summary()}), flush=True)
+
+
 def run_host_tier(args, cfg):
     """Per-call decode steps (captured graphs) with the routed experts
     resident in HBM and with them in pinned host memory, gathered into HBM
@@ -863,7 +951,7 @@ def main():
     elif args.route_agreement:
         run_agreement(args, cfg)
     elif args.host_tier:
-        run_host_tier(args, cfg)
+        (run_host_tier_chain if args.path == "chain" else run_host_tier)(args, cfg)
     elif args.impl == "reference":
         import oracle
         oracle.build()

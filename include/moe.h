@@ -353,6 +353,28 @@ int moe_gather_experts(const void *pool, size_t expert_stride, int E, const int3
                        int n, size_t blob_bytes, void *slots, size_t slot_stride,
                        int32_t *slot_idx, cudaStream_t stream);
 
+/* An HBM cache of C expert slots in front of a pool (host or device memory)
+ * of one layer -- the expert cache of the xyznot page's streaming design
+ * ("Ideas clave": the predicted route is known a token ahead), kept on the
+ * GPU.  cache: C slots, slot_stride bytes apart (device); tags [C] (device):
+ * the expert in each slot, -1 for none (the caller sets every tag to -1 once);
+ * ages [C] (device): the step each slot was last used at; clock (device, one
+ * int32): the cache's step counter, advanced by one by every call (on the
+ * device, so calls replayed from a captured graph age the slots too).  For
+ * the route idx[0..n-1] (device): an expert already in a slot is a hit;
+ * any other valid one takes the least recently used slot this route does not
+ * use (empty slots first, then the oldest step, then the lowest index) and its
+ * blob is copied there from pool.  slot_idx[i] (device) receives idx[i]'s
+ * slot, or C for an index outside [0, E) (not copied); this is the slot map
+ * moe_decode_step_chain reads (moe_stack_desc.slot_map).  plan [n] (device):
+ * scratch between the call's two launches (the decision, one warp; the
+ * copies).  stats (device int32 [2], or NULL): += distinct hits, += misses.
+ * 1 <= n <= 17, n <= C <= 1024; strides and blob 16-byte multiples. */
+int moe_cache_experts(const void *pool, size_t expert_stride, int E, const int32_t *idx,
+                      int n, size_t blob_bytes, void *cache, size_t slot_stride, int C,
+                      int32_t *tags, int32_t *ages, int32_t *clock, int32_t *slot_idx,
+                      int32_t *plan, int32_t *stats, cudaStream_t stream);
+
 /* ---------------------------------------------------------------- stack */
 /* A decode stack: depth layers per step, layer N using resident layer
  * N % n_layers (all of one shape).  Layer 0 routes with its own router every
@@ -384,6 +406,31 @@ typedef struct {
                                          (256 per launch)                     */
     unsigned inflight_bytes;          /* tuning: weight-copy bytes in flight
                                          per SM (0 = 32 KiB; at least 16 KiB) */
+    const int32_t *slot_map;          /* moe_decode_step_chain only (NULL for
+                                         moe_decode_step): NULL, or a device
+                                         array [depth][K] -- layer N's route
+                                         position k then reads the routed
+                                         expert blob at experts[N % n_layers]
+                                         .pool + slot_map[N * K + k] *
+                                         expert_stride instead of the one its
+                                         route index names (an expert cache or
+                                         staging area the caller filled, e.g.
+                                         with moe_gather_experts); the route
+                                         indices still feed the heads and the
+                                         routed adapters.  Not used for layer
+                                         0 when it routes itself in the step */
+    void *const *layer_ready;         /* moe_decode_step_chain only: NULL, or
+                                         [depth] cudaEvent_t (NULL entries
+                                         allowed); the step's stream waits on
+                                         layer_ready[N] before layer N's first
+                                         kernel (e.g. the copy of its experts
+                                         on another stream) */
+    int free_sms;                     /* moe_decode_step_chain only: SMs the
+                                         step leaves free (its kernels run one
+                                         CTA on each of the others; 0 = every
+                                         SM), e.g. for copy kernels running on
+                                         another stream beside it; the
+                                         workspace size depends on it */
 } moe_stack_desc;
 
 /* Workspace bytes of moe_decode_step; 0 if the descriptor is invalid. */

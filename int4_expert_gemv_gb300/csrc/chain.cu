@@ -23,6 +23,7 @@
 // before it.  The only wait inside a kernel is on its own bulk copies
 // (bounded: on expiry the status word records MOE_ETIMEOUT and the kernel
 // returns).  No CTA waits on another.
+#include <algorithm>
 #include <cfloat>
 #include <cstring>
 
@@ -66,6 +67,7 @@ struct CP {
     uint32_t gu_off, down_off, rec_d, rec_F, rec_dh, rec_H;
     int gu_lora;              // the shared expert has a gate or up adapter
     CLayer L;
+    const int32_t *smap;      // this layer's slot map [K] (route position -> pool blob), or null
     const uint16_t *nA[2];    // the next layer's shared gate / up A (for its LoRA partials)
     int nr[2];
     const float *x_in;        // out(N - 1), or x0
@@ -456,15 +458,18 @@ __host__ __device__ inline ASplit a_split(int S, int F, int H, int E, int head, 
     return s;
 }
 
+// The blob of route position s: the shared expert, the routed expert the
+// route names, or -- with a slot map -- the pool blob the map names for it.
 __device__ __forceinline__ const uint8_t *slot_blob(const CP &p, const int32_t *route, int s,
                                                     bool &bad) {
     if (s >= p.K) return p.L.shared;
     const int e = route[s];
-    if ((unsigned)e >= (unsigned)p.E) {
+    const int b = p.smap ? p.smap[s] : e;
+    if ((unsigned)e >= (unsigned)p.E || b < 0) {
         bad = true;
         return p.L.pool;
     }
-    return p.L.pool + (size_t)e * p.stride;
+    return p.L.pool + (size_t)b * p.stride;
 }
 
 // ---------------------------------------------------------------- kernel A
@@ -1223,10 +1228,18 @@ static int residency(const Shapes &s, int n_cta, moe_chain_info *info) {
     return MOE_OK;
 }
 
+// CTAs per kernel of the step: one per SM, less the SMs the caller leaves
+// free (at least one).
+static int chain_ctas(const moe_stack_desc *sd) {
+    const int sms = sms_of_device();
+    if (sms <= 0) return sms;
+    return std::max(1, sms - std::max(0, sd->free_sms));
+}
+
 template <int BITS>
 static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float *out,
                int32_t *ridx, float *rw, float *rmargin, int t, uint8_t *ws, cudaStream_t st) {
-    const int n_cta = sms_of_device();
+    const int n_cta = chain_ctas(sd);
     const Ws W = ws_layout(s.d, s.F, s.E, s.H, s.S, s.depth, n_cta);
     moe_chain_info info;
     if (int rc = residency<BITS>(s, n_cta, &info)) return rc;
@@ -1321,6 +1334,12 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
         p.z = z + (size_t)N * s.E;
         p.vp = vp + (size_t)N * vps;
         next_lora(p, N + 1);
+        p.smap = sd->slot_map && !p.route_late ? sd->slot_map + (size_t)N * s.K : nullptr;
+        if (sd->layer_ready && sd->layer_ready[N]) {
+            const cudaError_t e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(sd->layer_ready[N]), 0);
+            if (e != cudaSuccess)
+                return fail(MOE_ECUDA, "decode_step_chain: wait for layer %d: %s", N, cudaGetErrorString(e));
+        }
         p.launch_id = lid++;
         p.debug_unset_wait = N == 0 ? sd->debug_unset_wait : 0;
         if (int rc = launch(chain_a_kernel<BITS>, p, n_cta, kThreads, sa, !first, st, "A")) return rc;
@@ -1359,7 +1378,7 @@ using namespace moe;
 extern "C" size_t moe_decode_step_chain_workspace_bytes(const moe_stack_desc *sd) {
     if (check_decode_stack(sd) != MOE_OK) return 0;
     const chain::Shapes s = chain::shapes_of(sd);
-    const int sms = chain::sms_of_device();
+    const int sms = chain::chain_ctas(sd);
     return chain::ws_layout(s.d, s.F, s.E, s.H, s.S, s.depth, sms > 0 ? sms : 256).total;
 }
 
@@ -1367,7 +1386,7 @@ extern "C" int moe_decode_step_chain_info(const moe_stack_desc *sd, moe_chain_in
     if (info == nullptr) return fail(MOE_EINVAL, "decode_step_chain_info: NULL info");
     if (int rc = check_decode_stack(sd)) return rc;
     const chain::Shapes s = chain::shapes_of(sd);
-    const int n = chain::sms_of_device();
+    const int n = chain::chain_ctas(sd);
     if (n <= 0) return fail(MOE_ECUDA, "decode_step_chain_info: no device");
     return s.bits == 4 ? chain::residency<4>(s, n, info) : chain::residency<2>(s, n, info);
 }
@@ -1388,7 +1407,7 @@ extern "C" int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, 
     const chain::Shapes s = chain::shapes_of(sd);
     if (s.d % 256 && s.bits == 2)
         return fail(MOE_EUNSUPPORTED, "decode_step_chain: 2-bit needs d a multiple of 256");
-    const int n = chain::sms_of_device();
+    const int n = chain::chain_ctas(sd);
     if (n <= 0) return fail(MOE_ECUDA, "decode_step_chain: no device");
     if ((long long)s.S * s.F > (long long)chain::kMaxHPass * chain::kThreads * 4 ||
         (s.d + n - 1) / n > chain::kThreads || (s.E + n - 1) / n > chain::kThreads - 32)

@@ -23,6 +23,7 @@ namespace moe {
 constexpr int kGroup = 64;           // quantisation group along the input dim
 constexpr int kChunk = 16;           // bytes per vector load
 constexpr int kMaxSlots = 17;        // K <= 16 routed experts + 1 shared
+constexpr int kMaxCacheSlots = 1024; // slots of one layer's expert cache
 constexpr int kMaxLoraRank = 64;
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) {

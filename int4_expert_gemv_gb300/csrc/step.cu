@@ -1883,6 +1883,8 @@ extern "C" int moe_decode_step(const moe_stack_desc *sd, const float *x0, float 
                                int32_t *route_idx, float *route_w, float *route_margin, int t,
                                void *ws, size_t ws_bytes, cudaStream_t stream) {
     if (int rc = check_stack(sd)) return rc;
+    if (sd->slot_map || sd->layer_ready)
+        return fail(MOE_EUNSUPPORTED, "decode_step: slot_map / layer_ready are for moe_decode_step_chain");
     if (t < 1)
         return fail(MOE_EINVAL, "decode_step: t=%d (step 0 routes every layer with its own router; "
                                 "run it with the per-call functions)", t);

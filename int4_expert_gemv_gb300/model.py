@@ -409,6 +409,142 @@ class HostTierStack(DecodeStack):
         main.wait_stream(self.side)
 
 
+class HostTierChain(DecodeStack):
+    """Chained decode steps (moe_decode_step_chain) with the routed experts in
+    pinned host memory behind an HBM cache per layer.
+
+    Every resident layer's routed pool is moved to pinned host memory (the
+    shared expert stays in HBM).  Each layer of the stack gets its own cache
+    of `cache_slots` expert slots in HBM (least recently used out,
+    moe_cache_experts; its hit and miss counts in `stats`).  At the start of
+    step t the routes of layers 1 .. depth-1 are already known (predicted
+    during step t - 1), so a side stream runs every such layer's cache update
+    -- the decision and the copies of its misses over NVLink-C2C -- while the
+    main stream runs the chained step, whose layer N waits only for its own
+    update (moe_stack_desc.layer_ready) and reads its experts from the cache
+    slots (moe_stack_desc.slot_map); free_sms SMs can be left to the copies
+    (moe_stack_desc.free_sms).  Layer 0 routes with its own router inside
+    the step, so its experts stay resident in HBM.  Results are those of the
+    HBM-resident chained step bit for bit (same kernels, same bytes)."""
+
+    def __init__(self, model: DeviceModel, cache_slots: int, free_sms: int = 0):
+        super().__init__(model, fused="chain")
+        c = self.cfg
+        if c.self_predict:
+            raise ValueError("a self-predicting single layer has no layer routed a token ahead")
+        if c.lora_r and c.lora_on == "routed_down":
+            raise ValueError("routed-expert adapters are not cached with the blobs")
+        dev = model.device
+        D, K = c.depth, c.K
+        self.C = cache_slots
+        self.host_pools = []
+        for ly in model.layers:
+            h = torch.empty(ly["pool"].numel(), dtype=torch.uint8, pin_memory=True)
+            h.copy_(ly["pool"])
+            self.host_pools.append(h)
+        # (the model's HBM pools stay allocated, for stacks that share the model;
+        # this stack reads only layer 0's, the layer that routes itself)
+        self.blob = moe.moe_pool_expert_bytes(c.d, c.F, c.bits, 64)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.cache = torch.empty((D, cache_slots * model.stride), dtype=torch.uint8, device=dev)
+        self.tags = torch.full((D, cache_slots), -1, **i32)
+        self.ages = torch.zeros((D, cache_slots), **i32)
+        self.clock = torch.zeros(D, **i32)
+        self.slot_map = torch.zeros((D, K), **i32)
+        self.plan = torch.zeros((D, K), **i32)
+        self.stats = torch.zeros((D, 2), **i32)
+        # one descriptor per layer of the stack: layer 0 on its resident pool,
+        # every other on its cache
+        self._ed = (moe.ExpertsDesc * D)()
+        self._rd = (moe.HeadDesc * D)()
+        self._hd = (moe.HeadDesc * D)()
+        for N in range(D):
+            ly = self._layer(N)
+            e = moe.ExpertsDesc.from_buffer_copy(ly["experts_desc"])
+            if N > 0:
+                e.pool = self.cache[N].data_ptr()
+            self._ed[N] = e
+            self._rd[N] = ly["router_desc"]
+            self._hd[N] = ly["head_desc"]
+        self.sd = moe.StackDesc(C.cast(self._ed, C.c_void_p), C.cast(self._rd, C.c_void_p),
+                                C.cast(self._hd, C.c_void_p), D, D, K, 0, 0, 0, None)
+        self.sd.slot_map = self.slot_map.data_ptr()
+        self.sd.free_sms = free_sms             # SMs left to the cache copies
+        self.step_ws = torch.zeros(moe.moe_decode_step_chain_workspace_bytes(self.sd),
+                                   dtype=torch.uint8, device=dev)
+        self.side = torch.cuda.Stream(device=dev)
+        self.ready = [torch.cuda.Event() for _ in range(D)]
+        self._ready_ptrs = None
+
+    def hit_rate(self) -> float:
+        """Hits / (hits + misses) over every cache update so far."""
+        h, m = self.stats.sum(0).tolist()
+        return h / max(1, h + m)
+
+    def update(self, N: int, t: int, stream):
+        """Layer N's cache for the route of step t: hits kept, misses copied
+        from host memory; slot_map[N] names each route position's slot."""
+        c = self.cfg
+        moe.moe_cache_experts(self.host_pools[N % c.L].data_ptr(), self.m.stride, c.E,
+                              self.r_idx[t % 3, N], c.K, self.blob, self.cache[N], self.m.stride,
+                              self.C, self.tags[N], self.ages[N], self.clock[N:N + 1],
+                              self.slot_map[N], self.plan[N], self.stats[N], stream)
+
+    def enqueue_fused_step(self, t: int, events=None, update_events=None):
+        """Step t >= 1: the cache updates of layers 1 .. depth-1 on the side
+        stream, the chained step on the current one (layer N after its
+        update).  update_events: optional (start, [depth]) events -- start
+        recorded on the current stream when the step begins, [N] on the side
+        stream when layer N's update has finished."""
+        c = self.cfg
+        main = torch.cuda.current_stream()
+        if update_events is not None:
+            update_events[0].record(main)
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            for N in range(1, c.depth):
+                self.update(N, t, self.side)
+                self.ready[N].record(self.side)
+                if update_events is not None:
+                    update_events[1][N].record(self.side)
+        if self._ready_ptrs is None:         # event handles exist once recorded
+            self._ready_ptrs = (C.c_void_p * c.depth)(
+                *([None] + [C.c_void_p(e.cuda_event) for e in self.ready[1:]]))
+            self.sd.layer_ready = C.cast(self._ready_ptrs, C.c_void_p)
+        if events is not None:
+            events[0].record()
+        moe.moe_decode_step_chain(self.sd, self.xin, self.stream, self.r_idx, self.r_w,
+                                  self.r_margin, t, self.step_ws)
+        if events is not None:
+            events[1].record()
+        main.wait_stream(self.side)
+
+    def enqueue_step(self, t: int, ffn_events=None):
+        """Step 0 (every layer routes itself): the per-call path, each layer's
+        cache updated right after its router."""
+        c = self.cfg
+        use = t % 3
+        self.xs[0].copy_(self.xin)
+        self.stream.copy_(self.xin)
+        for N in range(c.depth):
+            ly = self._layer(N)
+            self._route_own(N, use)
+            ed = ly["experts_desc"] if N == 0 else self._slot_desc(N)
+            idx = self.r_idx[use, N]
+            if N > 0:
+                self.update(N, t, torch.cuda.current_stream())
+                idx = self.slot_map[N]
+            moe.moe_expert_ffn_int4(ed, self.xs[N], idx, 1, c.K, self.y, self.ffn_ws)
+            self._layer_tail(N, t)
+
+    def _slot_desc(self, N: int):
+        """Layer N's cache as an expert pool of C experts (for the per-call
+        expert FFN, which indexes it by slot)."""
+        e = moe.ExpertsDesc.from_buffer_copy(self._ed[N])
+        e.E = self.C
+        return e
+
+
 class BatchedLayer:
     """One MoE layer over T tokens at once (prefill, batched decode).
 

@@ -54,7 +54,8 @@ class StackDesc(C.Structure):
                 ("n_layers", C.c_int), ("depth", C.c_int), ("K", C.c_int),
                 ("self_predict", C.c_int), ("timeout_ns", C.c_ulonglong),
                 ("debug_unset_wait", C.c_int), ("debug_trace", C.c_void_p),
-                ("inflight_bytes", C.c_uint)]
+                ("inflight_bytes", C.c_uint), ("slot_map", C.c_void_p),
+                ("layer_ready", C.c_void_p), ("free_sms", C.c_int)]
 
 
 class ChainInfo(C.Structure):
@@ -83,6 +84,7 @@ def lib():
                 "moe_pack_matrix": (I, [P, P, P, I, I, I, P, P]),
                 "moe_merge_lora": (I, [P, S, I, I, I, P, P, I, C.c_float, P, S, P]),
                 "moe_gather_experts": (I, [P, S, I, P, I, S, P, S, P, P]),
+                "moe_cache_experts": (I, [P, S, I, P, I, S, P, S, I, P, P, P, P, P, P, P]),
                 "moe_pack_experts": (I, [I, I, I, I, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "moe_debug_dequant": (I, [P, I, I, I, I, P, P]),
                 "moe_debug_batched_waits": (I, [C.c_ulonglong, I]),
@@ -196,6 +198,17 @@ def moe_gather_experts(pool, expert_stride: int, E: int, idx, n: int, blob_bytes
     _check(lib().moe_gather_experts(_ptr(pool), expert_stride, E, _ptr(idx), n, blob_bytes,
                                     _ptr(slots), slot_stride, _ptr(slot_idx), _stream(stream)),
            "moe_gather_experts")
+
+
+def moe_cache_experts(pool, expert_stride: int, E: int, idx, n: int, blob_bytes: int, cache,
+                      slot_stride: int, C: int, tags, ages, clock, slot_idx, plan, stats=None,
+                      stream=None):
+    """Route idx's experts through an HBM cache of C slots (LRU); slot_idx
+    receives each entry's slot (the chain's slot map)."""
+    _check(lib().moe_cache_experts(_ptr(pool), expert_stride, E, _ptr(idx), n, blob_bytes,
+                                   _ptr(cache), slot_stride, C, _ptr(tags), _ptr(ages), _ptr(clock),
+                                   _ptr(slot_idx), _ptr(plan), _ptr(stats), _stream(stream)),
+           "moe_cache_experts")
 
 
 def moe_pack_experts(d, F, E, bits, gate_q, gate_s, gate_b, up_q, up_s, up_b, down_q, down_s,

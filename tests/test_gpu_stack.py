@@ -26,10 +26,13 @@ def built():
     build.build()
 
 
-def run_gpu(cfg, steps, fused=False):
+def run_gpu(cfg, steps, fused=False, make=None):
+    """Run `steps` decode steps (captured graphs from step 1 on) and record
+    each step's routes and output.  make(model): another stack driver to run
+    (default: DecodeStack on the path `fused` names)."""
     from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
     dm = DeviceModel(cfg)
-    st = DecodeStack(dm, fused=fused)
+    st = make(dm) if make is not None else DecodeStack(dm, fused=fused)
     rec = []
     for t in range(steps):
         x0 = torch.from_numpy(synth.step_input(cfg, t)[0]).cuda()
@@ -40,7 +43,7 @@ def run_gpu(cfg, steps, fused=False):
         torch.cuda.synchronize()
         rec.append(dict(idx=idx.cpu().numpy(), w=w.cpu().double().numpy(),
                         margin=mg.cpu().double().numpy(), out=st.stream.cpu().double().numpy()))
-    if fused:
+    if st.fused:
         assert st.status() == 0
     del st, dm
     torch.cuda.empty_cache()
@@ -62,8 +65,8 @@ def oracle_layers(cfg, rec):
     return [res[N % cfg.L] for N in range(cfg.depth)]
 
 
-def check_stack(cfg, steps, fused=False):
-    rec = run_gpu(cfg, steps, fused)
+def check_stack(cfg, steps, fused=False, make=None):
+    rec = run_gpu(cfg, steps, fused, make)
     run = orc.StackRunner(oracle_layers(cfg, rec), cfg.d, cfg.E, cfg.K,
                           single_layer_self_predict=cfg.self_predict)
     forced = 0
