@@ -79,12 +79,18 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def measured_traffic(layers: int, path: str):
-    """DRAM bytes (read + write) of one whole decode step over `layers`
-    layers on `path` ("fused" or "chain"), scaled from the ncu capture of the
-    4-layer stack summarised under profiles/ (per-layer bytes x layers + the
-    step's fixed launches); None when the kernel sources have changed since
-    that capture."""
+def measured_traffic(cfg, path: str):
+    """DRAM bytes (read + write) of one whole decode step of cfg on `path`
+    ("fused" or "chain"), scaled from the ncu capture of the 4-layer 35B-like
+    stack summarised under profiles/ (per-layer bytes x layers + the step's
+    fixed launches); None for other layer shapes, or when the kernel sources
+    have changed since that capture."""
+    from int4_expert_gemv_gb300.configs import MOE35B
+    if (cfg.d, cfg.E, cfg.K, cfg.F, cfg.shared, cfg.bits, cfg.H, cfg.lora_r) != (
+            MOE35B.d, MOE35B.E, MOE35B.K, MOE35B.F, MOE35B.shared, MOE35B.bits, MOE35B.H,
+            MOE35B.lora_r):
+        return None
+    layers = cfg.depth
     import hashlib
     import re
     name = {"fused": "decode_step_35b_L4.md", "chain": "decode_chain_35b_L4.md"}.get(path)
@@ -503,8 +509,7 @@ def run_native(args, cfg):
             "roofline": {"bound": "hbm", "kernel": kname,
                          "achieved": achieved, "peak": hbm, "peak_kind": hbm_kind,
                          "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": measured_traffic(cfg.depth, args.path)
-                         if st.fused else None,
+                         "traffic": measured_traffic(cfg, args.path) if st.fused else None,
                          "bytes_per_launch": launch_bytes,
                          "avg_launch_us": launch_avg_ms * 1000.0,
                          "timing": (f"CUDA events around each whole step in {n_inst} "
