@@ -59,6 +59,8 @@ constexpr int kEntOff = kXsOff + kTok * 16;    // group sums: kTok x 4 floats
 constexpr int kStageB = ((kEntOff + kTok * 4) + 1023) / 1024 * 1024;
 constexpr int kOutLd = kTok + 1;               // epilogue staging row (floats)
 static_assert(kRB * kOutLd * 4 <= kEntOff, "the epilogue staging would overwrite the entries");
+static_assert(kXOff % 1024 == 0 && kTok * kXRow == 4 * kTok * 128,
+              "activation slabs of 64 columns on 1 KB swizzle atoms");
 
 constexpr uint64_t kDefaultWaitNs = 1000000000ull;   // a wait's bound unless set
 
@@ -289,7 +291,10 @@ __device__ __forceinline__ void a_frags(const uint8_t *codes, int r0, int gi, in
     if (BITS == 4) {
 #pragma unroll
         for (int h = 0; h < 2; h++) {          // record r0 (h = 0), r0 + 8 (h = 1)
-            const uint2 w = *reinterpret_cast<const uint2 *>(codes + (r0 + 8 * h) * CB + gi * 32 + j * 8);
+            // records of 128 bytes with the 128-byte swizzle: 16-byte piece c
+            // of record r at 16 (c ^ r % 8)
+            const int r = r0 + 8 * h, o = gi * 32 + j * 8;
+            const uint2 w = *reinterpret_cast<const uint2 *>(codes + r * CB + ((((o >> 4) ^ (r & 7)) << 4) | (o & 15)));
 #pragma unroll
             for (int half = 0; half < 2; half++) {   // columns 16j + 0..7, 16j + 8..15
                 const uint32_t v = half ? w.y : w.x;
@@ -340,9 +345,13 @@ __device__ __forceinline__ void mma_chunk(const uint8_t *stage, int rw, int g0, 
 #pragma unroll
         for (int nti = 0; nti < 8; nti++) {
             if (nti < nnt) {
-                const __nv_bfloat16 *xr = x + (nti * 8 + gq) * kKc + gi * kGroup + j * 16;
-                const uint4 xa = *reinterpret_cast<const uint4 *>(xr);
-                const uint4 xb = *reinterpret_cast<const uint4 *>(xr + 8);
+                // group gi's activation rows: 128 bytes each, 128-byte swizzle
+                // (16-byte piece c of row t at 16 (c ^ t % 8)); this lane's 16
+                // values are pieces 2j and 2j + 1
+                const int t = nti * 8 + gq;
+                const uint8_t *xr = reinterpret_cast<const uint8_t *>(x) + gi * (kTok * 128) + t * 128;
+                const uint4 xa = *reinterpret_cast<const uint4 *>(xr + (((2 * j) ^ (t & 7)) << 4));
+                const uint4 xb = *reinterpret_cast<const uint4 *>(xr + (((2 * j + 1) ^ (t & 7)) << 4));
                 float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                 mma_bf16(acc, a[0], xa.x, xa.y);
                 mma_bf16(acc, a[1], xa.z, xa.w);
@@ -419,23 +428,28 @@ __global__ void __launch_bounds__(kThr, 1) pipe_gemm_kernel(const __grid_constan
                 if (m != nullptr)
                     for (int t = lane; t < it.nt; t += 32) ent[t] = m[t];
             }
-            // the chunk's four copies (codes, {s, b}, the activation rows in one
-            // box of 8, 16, 32 or 64 rows, their group sums), each from a lane
-            // of its own: one lane issues a copy only every ~200 ns
+            // the chunk's copies, each from a lane of its own (one lane issues a
+            // copy only every ~200 ns): the codes (4-bit: 128-byte records with
+            // the 128-byte swizzle), {s, b}, per group the activation rows (in
+            // one box of 8, 16, 32 or 64 rows, 128-byte swizzle), their group
+            // sums
+            const int ng = min(kKc, job.cols - lc * kKc) / kGroup;
             const int bk = it.nt <= 8 ? 0 : it.nt <= 16 ? 1 : it.nt <= 32 ? 2 : 3;
             const int rows = kRowBox << bk;
-            if (lane == 0) mbar_expect_tx(full + s, kCodeBytes + kRB * 16 + rows * (kXRow + 16));
+            if (lane == 0) mbar_expect_tx(full + s, kCodeBytes + kRB * 16 + ng * rows * 128 + rows * 16);
             __syncwarp();
             int map, row, blob;
             job.weights(it, map, row, blob);
             const int r0 = job.row0(sm, it);
             if (lane == 0)
-                tma_3d(stage, &job.maps.codes[map], lc * kKc * BITS / 8, row, blob, full + s, policy);
+                tma_3d(stage, BITS == 4 ? &job.maps.gcodes[map] : &job.maps.codes[map], lc * kKc * BITS / 8,
+                       row, blob, full + s, policy);
             else if (lane == 1)
                 tma_3d(stage + kSbOff, &job.maps.sb[map], cbytes + 16 * lc, row, blob, full + s, policy);
-            else if (lane == 2)
-                tma_2d(stage + kXOff, &job.maps.act4[bk], lc * kKc, r0, full + s);
-            else if (lane == 3)
+            else if (lane < 2 + ng)
+                tma_2d(stage + kXOff + (lane - 2) * (kTok * 128), &job.maps.act128[bk],
+                       lc * kKc + (lane - 2) * kGroup, r0, full + s);
+            else if (lane == 2 + ng)
                 tma_2d(stage + kXsOff, &job.maps.gsum4[bk], lc * kGpc, r0, full + s);
             if (++lc == nch) {
                 lc = 0;
