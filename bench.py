@@ -54,6 +54,8 @@ def parse():
                     help="--host-tier with --path chain: HBM cache slots per layer")
     ap.add_argument("--free-sms", type=int, default=0,
                     help="--host-tier with --path chain: SMs the chained step leaves to the copies")
+    ap.add_argument("--side-streams", type=int, default=1,
+                    help="--host-tier with --path chain: streams the layers' cache updates use")
     ap.add_argument("--route-agreement", action="store_true",
                     help="measure how often the predicted routes agree with the layers' own "
                          "routers (seeded decode steps)")
@@ -794,7 +796,7 @@ def run_host_tier_chain(args, cfg):
         return
     dm = DeviceModel(cfg)
     stacks = {"hbm": DecodeStack(dm, fused="chain"),
-              "host": HostTierChain(dm, args.cache_slots, args.free_sms)}
+              "host": HostTierChain(dm, args.cache_slots, args.free_sms, args.side_streams)}
     total = args.warmup + args.steps
     xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
                                        (total + 1, cfg.d), 1.0)).cuda()
@@ -846,6 +848,7 @@ def run_host_tier_chain(args, cfg):
         "data": "synthetic",
         "config": {"workload": cfg.name, "path": "chained step, captured graphs",
                    "cache_slots_per_layer": args.cache_slots, "free_sms": args.free_sms,
+                   "side_streams": args.side_streams,
                    "cache_bytes": tier.cache.numel(),
                    "host_pool_bytes": sum(h.numel() for h in tier.host_pools)},
         "hbm_resident": {"ms_per_step": res["hbm"], "tokens_per_s": 1000.0 / res["hbm"]},

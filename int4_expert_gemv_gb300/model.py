@@ -427,7 +427,7 @@ class HostTierChain(DecodeStack):
     the step, so its experts stay resident in HBM.  Results are those of the
     HBM-resident chained step bit for bit (same kernels, same bytes)."""
 
-    def __init__(self, model: DeviceModel, cache_slots: int, free_sms: int = 0):
+    def __init__(self, model: DeviceModel, cache_slots: int, free_sms: int = 0, side_streams: int = 1):
         super().__init__(model, fused="chain")
         c = self.cfg
         if c.self_predict:
@@ -472,7 +472,10 @@ class HostTierChain(DecodeStack):
         self.sd.free_sms = free_sms             # SMs left to the cache copies
         self.step_ws = torch.zeros(moe.moe_decode_step_chain_workspace_bytes(self.sd),
                                    dtype=torch.uint8, device=dev)
-        self.side = torch.cuda.Stream(device=dev)
+        # the layers' updates go round-robin over side_streams streams (more
+        # copies in flight over C2C at once)
+        self.sides = [torch.cuda.Stream(device=dev) for _ in range(max(1, side_streams))]
+        self.side = self.sides[0]
         self.ready = [torch.cuda.Event() for _ in range(D)]
         self._ready_ptrs = None
 
@@ -500,13 +503,15 @@ class HostTierChain(DecodeStack):
         main = torch.cuda.current_stream()
         if update_events is not None:
             update_events[0].record(main)
-        self.side.wait_stream(main)
-        with torch.cuda.stream(self.side):
-            for N in range(1, c.depth):
-                self.update(N, t, self.side)
-                self.ready[N].record(self.side)
+        for sd in self.sides:
+            sd.wait_stream(main)
+        for N in range(1, c.depth):
+            sd = self.sides[(N - 1) % len(self.sides)]
+            with torch.cuda.stream(sd):
+                self.update(N, t, sd)
+                self.ready[N].record(sd)
                 if update_events is not None:
-                    update_events[1][N].record(self.side)
+                    update_events[1][N].record(sd)
         if self._ready_ptrs is None:         # event handles exist once recorded
             self._ready_ptrs = (C.c_void_p * c.depth)(
                 *([None] + [C.c_void_p(e.cuda_event) for e in self.ready[1:]]))
@@ -517,7 +522,8 @@ class HostTierChain(DecodeStack):
                                   self.r_margin, t, self.step_ws)
         if events is not None:
             events[1].record()
-        main.wait_stream(self.side)
+        for sd in self.sides:
+            main.wait_stream(sd)
 
     def enqueue_step(self, t: int, ffn_events=None):
         """Step 0 (every layer routes itself): the per-call path, each layer's
