@@ -98,10 +98,14 @@ __device__ __forceinline__ void grid_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;");
 }
 
+// Weight copies stream each byte once per step: L2 evict-first, so that they
+// do not push the small exchanged vectors (x, h, g) out of L2.
 __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(saddr(dst)), "l"(src), "r"(bytes), "r"(saddr(bar)) : "memory");
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(saddr(dst)), "l"(src), "r"(bytes), "r"(saddr(bar)), "l"(pol) : "memory");
 }
 
 __device__ __forceinline__ void bar_init(uint64_t *bar) {
