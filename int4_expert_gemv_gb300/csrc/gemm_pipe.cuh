@@ -260,9 +260,11 @@ __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *m, int x, i
         : "memory");
 }
 
+// (not volatile: a pure function of its operands, so the compiler may
+// interleave the independent MMAs of different n-tiles)
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
