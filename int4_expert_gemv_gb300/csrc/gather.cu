@@ -127,12 +127,15 @@ __global__ void __launch_bounds__(256) cache_fill_kernel(const uint8_t *pool, si
     uint4 *dst = reinterpret_cast<uint4 *>(cache + (size_t)slot * slot_stride);
     const size_t words = blob_bytes / 16, step = (size_t)gridDim.y * blockDim.x;
     size_t w = (size_t)blockIdx.y * blockDim.x + threadIdx.x;
-    for (; w + 3 * step < words; w += 4 * step) {
-        const uint4 a = src[w], b = src[w + step], c = src[w + 2 * step], d = src[w + 3 * step];
-        dst[w] = a;
-        dst[w + step] = b;
-        dst[w + 2 * step] = c;
-        dst[w + 3 * step] = d;
+    // eight independent loads in flight per thread (a read of host memory
+    // over C2C waits microseconds)
+    constexpr int kU = 8;
+    for (; w + (kU - 1) * step < words; w += kU * step) {
+        uint4 v[kU];
+#pragma unroll
+        for (int u = 0; u < kU; u++) v[u] = src[w + u * step];
+#pragma unroll
+        for (int u = 0; u < kU; u++) dst[w + u * step] = v[u];
     }
     for (; w < words; w += step) dst[w] = src[w];
 }
@@ -162,7 +165,7 @@ extern "C" int moe_cache_experts(const void *pool, size_t expert_stride, int E, 
     cache_plan_kernel<<<1, 32, 0, stream>>>(idx, n, E, C, tags, ages, clock, slot_idx, plan, stats);
     if (int rc = check_launch("cache_plan_kernel")) return rc;
     const size_t words = blob_bytes / 16;
-    const unsigned parts = (unsigned)std::max<size_t>(1, std::min<size_t>(16, words / (256 * 4)));
+    const unsigned parts = (unsigned)std::max<size_t>(1, std::min<size_t>(16, words / (256 * 8)));
     cache_fill_kernel<<<dim3((unsigned)n, parts), 256, 0, stream>>>(
         static_cast<const uint8_t *>(pool), expert_stride, idx, plan, blob_bytes,
         static_cast<uint8_t *>(cache), slot_stride);
