@@ -65,10 +65,13 @@ def parse():
     ap.add_argument("--engine", default="auto", choices=["auto", "mma_sync", "tcgen05"],
                     help="batched configs: the grouped-GEMM engine (auto: the library's "
                          "default, the register engine)")
-    ap.add_argument("--path", default="chain", choices=["chain", "fused", "per-call"],
+    ap.add_argument("--path", default="chain", choices=["chain", "cluster", "fused", "per-call"],
                     help="chain: two kernels per layer chained by programmatic dependent "
-                         "launch; fused: one persistent kernel per step; per-call: the "
-                         "four calls per layer")
+                         "launch; cluster: the same step with one cluster kernel per layer "
+                         "(h exchanged in distributed shared memory); fused: one persistent "
+                         "kernel per step; per-call: the four calls per layer")
+    ap.add_argument("--no-l2-prefetch", action="store_true",
+                    help="cluster path: no L2 prefetch of the next layer's weights")
     return ap.parse_args()
 
 
@@ -320,22 +323,26 @@ def run_reference(args, cfg):
 def path_dtype(cfg, path: str) -> str:
     """What the timed decode path computes in."""
     w = f"int{cfg.bits}-g{cfg.group} weights (fp16 scale, bias)"
-    if path in ("chain", "fused"):
+    if path in ("chain", "cluster", "fused"):
         return (f"{w} x 16-bit fixed-point activations (power-of-two scale per 16-byte code "
                 f"chunk, exact integer chunk dots), fp32 accumulate")
     return f"{w} x f32 activations, fp32 accumulate"
 
 
-def kernels_per_step(cfg, stack) -> int:
+def kernels_per_step(cfg, stack, cluster=False) -> int:
     """Kernel launches of one steady-state step (counted from the calls the
     driver makes; the kernels per call are fixed by the library)."""
     ed = stack.m.layers[0]["experts_desc"]
+    heads = cfg.depth if cfg.self_predict else cfg.depth - 1
+    if stack.chain and cluster:
+        # layer-0 router and its top-K (unless layer 0 follows its own head),
+        # one cluster launch per layer, the output sum, one ranking launch
+        return (0 if cfg.self_predict else 2) + cfg.depth + 1 + (1 if heads > 0 else 0)
     if stack.chain:
         # layer-0 router (+ its top-K) when layer 0 routes itself or the shared
         # expert carries a gate/up adapter, A and B per layer, one ranking launch
         sh_gu = cfg.shared and any(ed.shared_lora[i].r for i in range(2))
         n = (1 if (not cfg.self_predict or sh_gu) else 0) + (0 if cfg.self_predict else 1)
-        heads = cfg.depth if cfg.self_predict else cfg.depth - 1
         return n + 2 * cfg.depth + (1 if heads > 0 else 0)
     if stack.fused:
         return 1
@@ -356,7 +363,7 @@ def run_native(args, cfg):
     import torch
     import torch.distributed as dist
 
-    from int4_expert_gemv_gb300 import synth
+    from int4_expert_gemv_gb300 import moe, synth
     from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
     import __graft_entry__
 
@@ -369,7 +376,9 @@ def run_native(args, cfg):
     __graft_entry__.build()
 
     dm = DeviceModel(cfg)
-    st = DecodeStack(dm, fused={"chain": "chain", "fused": True, "per-call": False}[args.path])
+    moe.moe_decode_step_chain_variant(2 if args.path == "cluster" else 0, not args.no_l2_prefetch)
+    st = DecodeStack(dm, fused={"chain": "chain", "cluster": "chain", "fused": True,
+                                "per-call": False}[args.path])
     total = args.warmup + args.steps
     xin = torch.from_numpy(synth.gauss(cfg.seed, synth.tag(synth.X_INPUT, 0),
                                        (total + 64, cfg.d), 1.0)).cuda()
@@ -481,7 +490,11 @@ def run_native(args, cfg):
         expert_gbs = ffn_bytes * cfg.depth / (ms_step / 1000.0) / 1e9
         achieved = launch_bytes / (launch_avg_ms / 1000.0) / 1e9
         head_bytes = dm.head_bytes_per_token()
-        if st.chain:
+        cluster = args.path == "cluster"
+        if st.chain and cluster:
+            kname = ("chain_c_kernel, one 16-CTA-cluster launch per layer (whole step: experts, "
+                     f"combine, heads; {kernels_per_step(cfg, st, True)} PDL-chained launches)")
+        elif st.chain:
             kname = ("chain_a_kernel + chain_b_kernel (whole step: experts, combine, heads; "
                      f"{kernels_per_step(cfg, st)} PDL-chained launches)")
         elif st.fused:
@@ -529,7 +542,7 @@ def run_native(args, cfg):
                                      "unit": "tokens/s",
                                      "how": "the same copies around a replay of the step's "
                                             "captured CUDA graph"}},
-            "gpu_launches": kernels_per_step(cfg, st) * args.steps,
+            "gpu_launches": kernels_per_step(cfg, st, args.path == "cluster") * args.steps,
             "clocks": clk.summary(),
         }
         if not args.no_cpu_baseline and world == 1:

@@ -505,6 +505,24 @@ typedef struct {
  * coresident is 0, with each kernel's copies starting only when the previous
  * one's CTAs have left. */
 int moe_decode_step_chain_info(const moe_stack_desc *sd, moe_chain_info *info);
+
+/* Which form moe_decode_step_chain takes (process-wide, read at each call):
+ * variant 0 the library's choice (two kernels per layer), 1 two kernels per
+ * layer, 2 one kernel per layer with a thread-block cluster of 16 CTAs per
+ * expert slot and one for the head: CTA j of a slot takes gate/up row pairs
+ * [F j/16, F (j+1)/16) and output rows [d j/16, d (j+1)/16), h is exchanged
+ * inside the cluster through distributed shared memory, and each slot's
+ * weighted output goes to a per-slot vector that the next layer sums onto
+ * the residual (one global exchange per layer).  Two CTAs per SM: gate/up
+ * rows are copied into shared memory, down rows read into registers.
+ * Variant 2 returns MOE_EUNSUPPORTED from the step when a CTA's share of a
+ * slot does not fit (shared memory, or F / (128 / bits) not dividing 32, or
+ * more than 4 passes of a warp over its down rows, or F > 1024, or an
+ * adapter rank above 16).  prefetch_l2: variant 2 prefetches its down rows
+ * into L2 in its prologue.  Same arguments, routes and results as variant 1;
+ * workspace from moe_decode_step_chain_workspace_bytes (sized for both).
+ * MOE_EINVAL for another variant. */
+int moe_decode_step_chain_variant(int variant, int prefetch_l2);
 int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, float *out,
                           int32_t *route_idx, float *route_w, float *route_margin,
                           int t, void *ws, size_t ws_bytes, cudaStream_t stream);

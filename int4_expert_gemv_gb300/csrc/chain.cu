@@ -1008,6 +1008,573 @@ __global__ void __launch_bounds__(32) chain_topk_kernel(const __grid_constant__ 
     stamp(p, 2);
 }
 
+// ---------------------------------------------------------------- kernel C
+// The cluster variant of a layer: one launch per layer, one thread-block
+// cluster of kCluster CTAs per expert slot and one for the head.  CTA j of
+// slot s takes gate/up row pairs [F j / C, F (j+1) / C) of that slot and
+// output rows [d j / C, d (j+1) / C) of its down projection; h of the slot
+// is all-gathered inside the cluster through distributed shared memory, so
+// the layer has one global exchange (its input x) instead of two.  Each slot
+// cluster writes its weighted output w_s y_s (down LoRA included) to a
+// per-slot vector; the next launch sums them onto the residual while it
+// stages its x (out(N) = out(N-1) + sum_s w_s y_s), and slot cluster 0
+// stores that sum as out(N).  The head cluster takes fc1 rows [H j / C, ...)
+// and logit rows [E j / C, ...) (l and fc2), with gelu(fc1 f) all-gathered
+// the same way.
+//
+// Residency: two CTAs per SM, so that the next layer's clusters sit beside
+// this layer's and copy their gate/up rows while it runs.  Only the gate/up
+// rows go to shared memory (bulk copies); the down rows are prefetched into
+// L2 in the prologue and loaded into registers while h is exchanged, and so
+// are the rows of the down adapter's A.
+//
+// Exchanges: a CTA writes its values into every peer's shared memory
+// (st.shared::cluster) and then arrives on that peer's mbarrier with release
+// semantics at cluster scope (each writing thread arrives itself, so each
+// arrive covers the writes before it); the reader waits on its own mbarrier
+// (acquire, bounded).  No CTA returns early: a wait that runs out records
+// MOE_ETIMEOUT and the CTA carries on (its results are then invalid), so
+// every CTA reaches the cluster barrier before exit, after which no peer
+// touches its shared memory.
+constexpr int kCThreads = 512;
+constexpr int kCWarps = kCThreads / 32;
+constexpr int kCluster = 16;
+constexpr int kDPass = 4;      // down: a warp's passes over its rows (32 / chunks-per-row rows each)
+constexpr int kAPass = 4;      // down adapter A: 16-byte pieces of a row per lane (F <= 1024)
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared-memory address of `p` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void peer_store(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void peer_arrive(uint32_t bar_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr) : "memory");
+}
+
+__device__ __forceinline__ void bar_init_n(uint64_t *bar, uint32_t n) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(n));
+}
+
+// Bounded wait for phase 0 of a barrier that peers arrive on (acquire at
+// cluster scope): false, with MOE_ETIMEOUT in *err, after timeout_ns.
+__device__ __forceinline__ bool cbar_wait(uint64_t *bar, int32_t *err, uint64_t timeout_ns) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; it++) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0; "
+            "selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok) : "r"(saddr(bar)) : "memory");
+        if (ok) return true;
+        uint64_t now;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(now));
+        if (it == 0) t0 = now;
+        else if (now - t0 > timeout_ns) {
+            atomicExch(err, MOE_ETIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Even split [n j / C, n (j+1) / C).
+__host__ __device__ inline void csplit(int n, int j, int C, int &a, int &b) {
+    a = (int)((long long)n * j / C);
+    b = (int)((long long)n * (j + 1) / C);
+}
+
+// Shared-memory layout of kernel C (byte offsets; the same for every CTA of
+// a launch, sized for the largest share of either role).
+struct CLay {
+    uint32_t wts, xr, xf, xsc, xhat, agu, bgu, bdn, hs, hf, hsc, hhat, vpart, vd, tterm, tsum, zls,
+        b2s, red, route, wk, bars, total;
+};
+
+__host__ __device__ inline CLay c_layout(int d, int F, int E, int H, int K, int bits, int C, int rmax) {
+    const int VALS = 128 / bits;
+    const uint32_t rec_d = (uint32_t)record_bytes(d, bits);
+    const uint32_t rec_dh = (uint32_t)record_bytes(d, 4), rec_H = H ? (uint32_t)record_bytes(H, 4) : 0u;
+    const int np = (F + C - 1) / C, no = (d + C - 1) / C, nh = (H + C - 1) / C, ne = (E + C - 1) / C;
+    const size_t slot_w = (size_t)np * 2 * rec_d;
+    const size_t head_w = (size_t)(nh + ne) * rec_dh + (size_t)ne * rec_H;
+    CLay L;
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = (off + align - 1) / align * align;
+        const uint32_t at = (uint32_t)off;
+        off += bytes;
+        return at;
+    };
+    L.wts = take(slot_w > head_w ? slot_w : head_w, 128);
+    L.xr = take((size_t)no * 4, 16);                         // this CTA's rows of x (raw)
+    L.xf = take(fix_bytes(d, 4) > fix_bytes(d, bits) ? fix_bytes(d, 4) : fix_bytes(d, bits), 16);
+    L.xsc = take((size_t)(d / 32) * 4, 16);
+    L.xhat = take((size_t)(d / 32) * 4, 16);
+    L.agu = take((size_t)32 * no * 2, 16);                   // [32][no] fp16 gate/up A columns
+    L.bgu = take((size_t)np * 32 * 4, 16);                   // [np][32] gate/up B rows
+    L.bdn = take((size_t)no * rmax * 4 + 4, 16);             // [no][rmax] down B rows
+    const size_t hpad = padded(F, VALS) > (size_t)H ? padded(F, VALS) : (size_t)H;
+    L.hs = take(hpad * 4, 16);                               // h padded per chunk / g
+    L.hf = take(fix_bytes(F, bits) > (H ? fix_bytes(H, 4) : 0) ? fix_bytes(F, bits) : fix_bytes(H, 4), 16);
+    const int nq = F / VALS > (H ? H / 32 : 0) ? F / VALS : H / 32;
+    L.hsc = take((size_t)nq * 4, 16);
+    L.hhat = take((size_t)nq * 4, 16);
+    L.vpart = take((size_t)C * 32 * 4, 16);                  // [C][32] gate/up LoRA partials
+    L.vd = take(kMaxR * 4, 16);
+    L.tterm = take((size_t)(nh + ne) * (2 * K + 1) * 4 + 4, 16);
+    L.tsum = take((size_t)(nh + ne) * 4 + 4, 16);
+    L.zls = take((size_t)ne * 4 + 4, 16);
+    L.b2s = take((size_t)ne * 4 + 4, 16);
+    L.red = take((size_t)kCWarps * 32 * 4, 16);
+    L.route = take((kMaxK + 1) * 4, 16);
+    L.wk = take((kMaxK + 1) * 4, 16);
+    L.bars = take(4 * 8, 8);
+    L.total = (uint32_t)off;
+    return L;
+}
+
+// Extra parameters of kernel C (beside the layer's CP).
+struct CX {
+    int C;                     // cluster size
+    int rmax;                  // largest down adapter rank of the stack
+    int prefetch;              // prefetch the down rows into L2 in the prologue
+    const float *base;         // out(N-2) (or x0): the residual the partials add onto
+    const float *part_in;      // [S][d] weighted slot outputs of layer N-1, or null (layer 0)
+    float *part;               // [S][d] this layer's
+    float *x_out;              // where out(N-1) is stored (slot cluster 0), or null
+};
+
+template <int BITS>
+__global__ void __launch_bounds__(kCThreads, 2) chain_c_kernel(const __grid_constant__ CP p,
+                                                                const __grid_constant__ CX q) {
+    constexpr int VALS = 128 / BITS;
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int C = q.C;
+    const int j = (int)cluster_rank(), cl = blockIdx.x / C;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool head = cl >= p.S;
+    const int s = cl;                                           // slot (slot clusters)
+    const CLay Lo = c_layout(p.d, p.F, p.E, p.H, p.K, BITS, C, q.rmax);
+    uint8_t *wts = sm + Lo.wts;
+    float *xr = reinterpret_cast<float *>(sm + Lo.xr);
+    uint8_t *xf = sm + Lo.xf;
+    float *xsc = reinterpret_cast<float *>(sm + Lo.xsc);
+    float *xhat = reinterpret_cast<float *>(sm + Lo.xhat);
+    uint16_t *agu = reinterpret_cast<uint16_t *>(sm + Lo.agu);
+    float *bgu = reinterpret_cast<float *>(sm + Lo.bgu);
+    float *bdn = reinterpret_cast<float *>(sm + Lo.bdn);
+    float *hs = reinterpret_cast<float *>(sm + Lo.hs);
+    uint8_t *hf = sm + Lo.hf;
+    float *hsc = reinterpret_cast<float *>(sm + Lo.hsc);
+    float *hhat = reinterpret_cast<float *>(sm + Lo.hhat);
+    float *vpart = reinterpret_cast<float *>(sm + Lo.vpart);
+    float *vd = reinterpret_cast<float *>(sm + Lo.vd);
+    float *tterm = reinterpret_cast<float *>(sm + Lo.tterm);
+    float *tsum = reinterpret_cast<float *>(sm + Lo.tsum);
+    float *zls = reinterpret_cast<float *>(sm + Lo.zls);
+    float *b2s = reinterpret_cast<float *>(sm + Lo.b2s);
+    float *red = reinterpret_cast<float *>(sm + Lo.red);
+    int32_t *route = reinterpret_cast<int32_t *>(sm + Lo.route);
+    float *wk = reinterpret_cast<float *>(sm + Lo.wk);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + Lo.bars);   // copies, LoRA v, h / g, test hook
+
+    // this CTA's shares
+    int f0, f1, o0, o1, h0, h1, e0, e1;
+    csplit(p.F, j, C, f0, f1);
+    csplit(p.d, j, C, o0, o1);
+    csplit(p.H, j, C, h0, h1);
+    csplit(p.E, j, C, e0, e1);
+    const int np = f1 - f0, no = o1 - o0, nh = h1 - h0, ne = e1 - e0;
+    const uint32_t P = 2 * p.rec_d;
+    const uint32_t gbytes = head ? 0u : (uint32_t)np * P;
+    const uint32_t dbytes = head ? 0u : (uint32_t)no * p.rec_F;
+    const bool shared = !head && s >= p.K;
+    // this slot's down adapter (routed: the route's; shared: its own)
+    const int rd = head ? 0 : shared ? p.L.sr[2] : p.L.r_d;
+    const int rg = shared ? p.L.sr[0] : 0, ru = shared ? p.L.sr[1] : 0;
+    const bool gul = rg + ru > 0;
+    const int32_t *rcur = p.ridx + ((size_t)p.cur * p.depth + p.N) * p.K;
+    const float *wcur = p.rw + ((size_t)p.cur * p.depth + p.N) * p.K;
+    const int32_t *rprv = p.ridx + ((size_t)p.prv * p.depth + p.N) * p.K;
+
+    stamp(p, 0);
+    if (threadIdx.x == 0) {
+        bar_init_n(bar, 1);
+        bar_init_n(bar + 1, (uint32_t)C);             // one lane of every CTA
+        bar_init_n(bar + 2, (uint32_t)kCWarps * C);   // every warp of every CTA
+        bar_init_n(bar + 3, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    auto load_route = [&]() {
+        if (threadIdx.x < p.K) {
+            route[threadIdx.x] = rcur[threadIdx.x];
+            wk[threadIdx.x] = wcur[threadIdx.x];
+        }
+    };
+    if (!p.route_late) load_route();
+    __syncthreads();
+    cluster_sync();             // every peer's barriers initialised before any remote arrive
+    bool bad = false;
+    const uint8_t *blob = p.L.pool;   // this slot's expert blob (slot CTAs)
+    auto issue = [&]() {
+        if (!head) blob = slot_blob(p, route, s, bad);        // every thread
+        if (threadIdx.x != 0) return;
+        if (!head) {
+            bar_expect(bar, gbytes);
+            if (gbytes) bulk_copy(wts, blob + p.gu_off + (size_t)f0 * P, gbytes, bar);
+            if (q.prefetch) prefetch_l2(blob + p.down_off + (size_t)o0 * p.rec_F, dbytes);
+        } else {
+            const uint32_t b1 = (uint32_t)nh * p.rec_dh, b2 = (uint32_t)ne * p.rec_dh, b3 = (uint32_t)ne * p.rec_H;
+            bar_expect(bar, b1 + b2 + b3);
+            if (b1) bulk_copy(wts, p.L.fc1x + (size_t)h0 * p.rec_dh, b1, bar);
+            if (b2) bulk_copy(wts + b1, p.L.lx + (size_t)e0 * p.rec_dh, b2, bar);
+            if (b3) bulk_copy(wts + b1 + b2, p.L.fc2 + (size_t)e0 * p.rec_H, b3, bar);
+        }
+        if (bad) atomicExch(p.err, MOE_EINVAL);
+    };
+    if (!p.route_late) issue();
+    // static side data: gate/up adapters' A columns of this CTA's rows and B
+    // rows of its pairs (shared slot)
+    if (!head && gul) {
+        for (int it = threadIdx.x; it < (rg + ru) * no; it += blockDim.x) {
+            const int k = it / no, i = it - k * no;
+            const uint16_t *A = k < rg ? p.L.sa[0] + (size_t)k * p.d : p.L.sa[1] + (size_t)(k - rg) * p.d;
+            agu[k * no + i] = A[o0 + i];
+        }
+        for (int it = threadIdx.x; it < np * 32; it += blockDim.x) {
+            const int i = it >> 5, k = it & 31, f = f0 + i;
+            float v = 0.0f;
+            if (k < rg) v = half_at(p.L.sb[0], (size_t)f * rg + k);
+            else if (k < rg + ru) v = half_at(p.L.sb[1], (size_t)f * ru + (k - rg));
+            bgu[i * 32 + k] = v;
+        }
+    }
+    // route-dependent side data: down B rows of this CTA's outputs; the head's
+    // table sums (routes of layer N now and at t - 1) and fc2 biases
+    auto side = [&]() {
+        if (!head && rd) {
+            const bool ok = shared || (unsigned)route[s] < (unsigned)p.E;
+            const uint16_t *B = shared ? p.L.sb[2] : p.L.lb_d + (size_t)(ok ? route[s] : 0) * p.L.lb_ds;
+            for (int it = threadIdx.x; it < no * rd; it += blockDim.x) {
+                const int i = it / rd, k = it - i * rd;
+                bdn[i * q.rmax + k] = ok ? half_at(B, (size_t)(o0 + i) * rd + k) : 0.0f;
+            }
+        }
+        if (head) {
+            const int nt = 2 * p.K + 1, nr = nh + ne;
+            for (int it = threadIdx.x; it < nr * nt; it += blockDim.x) {
+                const int i = it / nt, t = it - i * nt;
+                const bool fc1 = i < nh;
+                const int row = fc1 ? h0 + i : e0 + (i - nh);
+                const int width = fc1 ? p.H : p.E;
+                const uint16_t *tab = fc1 ? p.L.fc1_tab : p.L.l_tab;
+                const uint16_t *bias = fc1 ? p.L.b1 : p.L.bl;
+                float a = 0.0f;
+                if (t == 2 * p.K) a = bias ? half_at(bias, row) : 0.0f;
+                else if (tab) {
+                    const int e = t < p.K ? route[t] : rprv[t - p.K];
+                    if ((unsigned)e < (unsigned)p.E) a = half_at(tab, (size_t)(t < p.K ? e : p.E + e) * width + row);
+                }
+                tterm[it] = a;
+            }
+            for (int i = threadIdx.x; i < ne; i += blockDim.x) b2s[i] = p.L.b2 ? half_at(p.L.b2, e0 + i) : 0.0f;
+            __syncthreads();
+            for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+                float a = 0.0f;
+                for (int t = 0; t < nt; t++) a += tterm[i * nt + t];
+                tsum[i] = a;
+            }
+        }
+    };
+    if (!p.route_late) side();
+    stamp(p, 5);
+    grid_launch_dependents();
+    grid_wait();
+    stamp(p, 1);
+    if (p.route_late) {
+        load_route();
+        __syncthreads();
+        issue();
+        side();
+    }
+    // x = out(N-1) = base + sum_s part_in[s] (or x0): this CTA's rows kept
+    // raw, the whole vector staged as fixed point (slot: BITS chunks; head:
+    // 4-bit chunks); 1/rms of it when it is an out.  The slot vectors' loads
+    // are issued eight at a time, unconditionally, before their sum.
+    float ss = 0.0f;
+    for (int b0 = 0; b0 < p.d / 4; b0 += blockDim.x) {          // uniform over the block
+        const int i = b0 + threadIdx.x;
+        const bool in = i < p.d / 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in) {
+            v = reinterpret_cast<const float4 *>(q.base)[i];
+            if (q.part_in)
+                for (int k0 = 0; k0 < p.S; k0 += 8) {
+                    float4 t[8];
+#pragma unroll
+                    for (int u = 0; u < 8; u++)
+                        t[u] = reinterpret_cast<const float4 *>(q.part_in + (size_t)min(k0 + u, p.S - 1) * p.d)[i];
+#pragma unroll
+                    for (int u = 0; u < 8; u++)
+                        if (k0 + u < p.S) {
+                            v.x += t[u].x;
+                            v.y += t[u].y;
+                            v.z += t[u].z;
+                            v.w += t[u].w;
+                        }
+                }
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+                if (4 * i + u >= o0 && 4 * i + u < o1) xr[4 * i + u - o0] = vv[u];
+        }
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        if (head) quant4<4>(v, i, in, xf, p.d / 32, xsc, xhat);
+        else quant4<BITS>(v, i, in, xf, p.d / VALS, xsc, xhat);
+    }
+    ss = warp_sum(ss, 32);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float inv = 1.0f;
+    if (p.x_is_out) {
+        float t = 0.0f;
+        for (int w = 0; w < kCWarps; w++) t += red[w];
+        inv = 1.0f / sqrtf(t / p.d + 1e-6f);
+    }
+    stamp(p, 3);
+    // slot cluster 0 stores out(N-1)
+    if (!head && s == 0 && q.x_out)
+        for (int i = threadIdx.x; i < no; i += blockDim.x) q.x_out[o0 + i] = xr[i];
+    // shared gate/up LoRA: this CTA's partial of A x over its rows, to every
+    // peer (warp 0; lane k holds entry k)
+    if (!head && gul) {
+        __syncthreads();                                         // red reused below
+        float a = 0.0f;
+        if (lane < rg + ru)
+            for (int i = warp; i < no; i += kCWarps) a = fmaf(half_f(agu[lane * no + i]), xr[i], a);
+        red[warp * 32 + lane] = a;
+        __syncthreads();
+        if (warp == 0) {
+            // lane r sends the 32 entries to peer r and arrives once there
+            // (one release per lane, all lanes at once)
+            float v = 0.0f;
+            for (int w = 0; w < kCWarps; w++) v += red[w * 32 + lane];
+            vd[lane] = v;
+            __syncwarp();
+            if (lane < C) {
+                for (int k = 0; k < 32; k++) peer_store(peer_addr(vpart + j * 32 + k, lane), vd[k]);
+                peer_arrive(peer_addr(bar + 1, lane));
+            }
+        }
+    }
+    bar_wait(bar, p.err, p.timeout_ns);
+    if (p.debug_unset_wait && blockIdx.x == 0) {
+        // test hook: a wait for 16 bytes no copy delivers; it runs out after
+        // timeout_ns and records MOE_ETIMEOUT (the CTA carries on)
+        if (threadIdx.x == 0) bar_expect(bar + 3, 16);
+        __syncthreads();
+        bar_wait(bar + 3, p.err, p.timeout_ns);
+    }
+    stamp(p, 4);
+    if (!head) {
+        // gate/up pairs, two per warp (records g, u, g', u') -> h, pushed to
+        // every peer
+        float vxl = 0.0f;                 // lane k: entry k of the adapters' A x
+        bool vready = false;
+        auto emit = [&](int v, float g, float u) {
+            float a0 = g * inv, a1 = u * inv;
+            if (gul) {
+                if (!vready) {
+                    cbar_wait(bar + 1, p.err, p.timeout_ns);
+                    for (int r = 0; r < C; r++) vxl += vpart[r * 32 + lane];
+                    vxl *= inv;
+                    vready = true;
+                }
+                const float t = bgu[v * 32 + lane] * vxl;
+                a0 = fmaf(p.L.ss[0], lane < rg ? t : 0.0f, a0);
+                a1 = fmaf(p.L.ss[1], lane < rg ? 0.0f : t, a1);
+            }
+            const float gg = warp_sum(a0, 32), uu = warp_sum(a1, 32);
+            const float hv = silu_f(gg) * uu;
+            const int f = f0 + v;
+            if (lane < C) peer_store(peer_addr(hs + f + f / VALS, lane), hv);
+        };
+        const int np2 = np / 2 * 2;
+        for (int v = 2 * warp; v < np2; v += 2 * kCWarps) {
+            float gu[4];
+            fix_dot<BITS, 4>(wts + (size_t)v * P, p.rec_d, p.d, xf, xsc, xhat, lane, gu);
+            emit(v, gu[0], gu[1]);
+            emit(v + 1, gu[2], gu[3]);
+        }
+        for (int v = np2 + warp; v < np; v += kCWarps) {
+            float gu[2];
+            fix_dot<BITS, 2>(wts + (size_t)v * P, p.rec_d, p.d, xf, xsc, xhat, lane, gu);
+            emit(v, gu[0], gu[1]);
+        }
+        // this warp's down rows into registers while h is exchanged: rows
+        // [warp rw, (warp + 1) rw) of the CTA's, pass k lane l: row
+        // k G + l / nch, chunk l % nch
+        const int nch = p.F / VALS, G = 32 / nch;
+        const int rw = (no + kCWarps - 1) / kCWarps;
+        const int gl = lane / nch, c = lane - gl * nch;
+        const size_t cbF = code_bytes(p.F, BITS);
+        const uint8_t *down = blob + p.down_off + (size_t)o0 * p.rec_F;
+        uint4 dw[kDPass];
+        uint32_t dsb[kDPass];
+#pragma unroll
+        for (int k = 0; k < kDPass; k++) {
+            const int r = k * G + gl, i = warp * rw + r;
+            const bool okr = r < rw && i < no;
+            const uint8_t *rec = down + (size_t)(okr ? i : 0) * p.rec_F;
+            dw[k] = okr ? __ldg(reinterpret_cast<const uint4 *>(rec + (size_t)kChunk * c)) : make_uint4(0, 0, 0, 0);
+            dsb[k] = okr ? __ldg(reinterpret_cast<const unsigned int *>(rec + cbF + 4 * ((c * VALS) / kGroup))) : 0u;
+        }
+        // ... and the down adapter's A row `warp` (k < rd)
+        uint4 av[kAPass];
+        const uint16_t *Ad = nullptr;
+        if (warp < rd)
+            Ad = (shared ? p.L.sa[2]
+                         : p.L.la_d + (size_t)((unsigned)route[s] < (unsigned)p.E ? route[s] : 0) * p.L.la_ds) +
+                 (size_t)warp * p.F;
+#pragma unroll
+        for (int k = 0; k < kAPass; k++) {
+            const int f = (k * 32 + lane) * 8;
+            av[k] = Ad && f < p.F ? __ldg(reinterpret_cast<const uint4 *>(Ad + f)) : make_uint4(0, 0, 0, 0);
+        }
+        if (lane < C) peer_arrive(peer_addr(bar + 2, lane));
+        cbar_wait(bar + 2, p.err, p.timeout_ns);
+        stamp(p, 6);
+        // h as fixed point per chunk (from the padded floats)
+        for (int b0 = 0; b0 < p.F / 4; b0 += blockDim.x) {
+            const int i = b0 + threadIdx.x;
+            const bool in = i < p.F / 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (in) {
+                const int ch = (4 * i) / VALS;
+                const float *src = hs + ch * (VALS + 1) + (4 * i - ch * VALS);
+                v = make_float4(src[0], src[1], src[2], src[3]);
+            }
+            quant4<BITS>(v, i, in, hf, nch, hsc, hhat);
+        }
+        // down LoRA: vd[k] = A_d[k] h (warp k)
+        if (warp < rd) {
+            float a = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kAPass; k++) {
+                const int f = (k * 32 + lane) * 8;
+                if (f < p.F) {
+                    const uint32_t w[4] = {av[k].x, av[k].y, av[k].z, av[k].w};
+#pragma unroll
+                    for (int u = 0; u < 8; u++) {
+                        const int g = f + u;
+                        a = fmaf(half_f((uint16_t)(w[u >> 1] >> (16 * (u & 1)))), hs[g + g / VALS], a);
+                    }
+                }
+            }
+            a = warp_sum(a, 32);
+            if (lane == 0) vd[warp] = a;
+        }
+        __syncthreads();
+        // down rows: w_s (y + s_d B_d vd), the nch lanes of a row summed by
+        // shuffles
+        const bool valid = shared || (unsigned)route[s] < (unsigned)p.E;
+        const float ws = shared ? 1.0f : wk[s];
+        const float sc = shared ? p.L.ss[2] : p.L.s_d;
+#pragma unroll
+        for (int k = 0; k < kDPass; k++) {
+            if (k * G >= rw) break;                              // uniform over the warp
+            const int r = k * G + gl, i = warp * rw + r;
+            const bool okr = r < rw && i < no;
+            const uint4 w1[1] = {dw[k]};
+            int dq[1];
+            chunk_dot_fix<BITS, 1>(w1, reinterpret_cast<const uint4 *>(hf), nch, c, dq);
+            const float2 sb = sb_f(dsb[k]);
+            float y = fmaf(sb.x, (float)dq[0] * hsc[c], sb.y * hhat[c]);
+            if (okr) {
+                float l = 0.0f;
+                for (int kk = c; kk < rd; kk += nch) l = fmaf(bdn[i * q.rmax + kk], vd[kk], l);
+                y = fmaf(sc, l, y);
+            } else {
+                y = 0.0f;
+            }
+            for (int o = 1; o < nch; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+            if (c == 0 && okr) q.part[(size_t)s * p.d + o0 + i] = valid ? ws * y : 0.0f;
+        }
+    } else {
+        // fc1 rows (warp per row) -> gelu -> pushed to every peer; l rows
+        for (int v = warp; v < nh; v += kCWarps) {
+            float hd[1];
+            fix_dot<4, 1>(wts + (size_t)v * p.rec_dh, 0, p.d, xf, xsc, xhat, lane, hd);
+            const float gv = gelu_erf_f(warp_sum(hd[0], 32) * inv + tsum[v]);
+            if (lane < C) peer_store(peer_addr(hs + h0 + v, lane), gv);
+        }
+        if (lane < C) peer_arrive(peer_addr(bar + 2, lane));
+        for (int v = warp; v < ne; v += kCWarps) {
+            float hd[1];
+            fix_dot<4, 1>(wts + (size_t)(nh + v) * p.rec_dh, 0, p.d, xf, xsc, xhat, lane, hd);
+            const float a = warp_sum(hd[0], 32) * inv + tsum[nh + v];
+            if (lane == 0) zls[v] = a;
+        }
+        cbar_wait(bar + 2, p.err, p.timeout_ns);
+        stamp(p, 6);
+        // g as fixed point (4-bit chunks), then the fc2 rows: z = fc2 g + b2 + l f
+        for (int b0 = 0; b0 < p.H / 4; b0 += blockDim.x) {
+            const int i = b0 + threadIdx.x;
+            const bool in = i < p.H / 4;
+            const float4 v = in ? reinterpret_cast<const float4 *>(hs)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+            quant4<4>(v, i, in, hf, p.H / 32, hsc, hhat);
+        }
+        __syncthreads();
+        const uint8_t *w2 = wts + (size_t)(nh + ne) * p.rec_dh;
+        for (int v = warp; v < ne; v += kCWarps) {
+            float f2[1];
+            fix_dot<4, 1>(w2 + (size_t)v * p.rec_H, 0, p.H, hf, hsc, hhat, lane, f2);
+            const float a = warp_sum(f2[0], 32);
+            if (lane == 0) p.z[e0 + v] = a + b2s[v] + zls[v];
+        }
+    }
+    stamp(p, 2);
+    stamp_end(p);
+    cluster_sync();             // no peer reads or writes this CTA's shared memory after this
+}
+
+// out = base + sum_s part[s] (the last layer's outputs onto its residual).
+__global__ void __launch_bounds__(256) chain_fin_kernel(const __grid_constant__ CP p,
+                                                        const __grid_constant__ CX q) {
+    grid_launch_dependents();
+    grid_wait();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.d / 4) return;
+    float4 v = reinterpret_cast<const float4 *>(q.base)[i];
+    for (int k = 0; k < p.S; k++) {
+        const float4 t = reinterpret_cast<const float4 *>(q.part_in + (size_t)k * p.d)[i];
+        v.x += t.x;
+        v.y += t.y;
+        v.z += t.z;
+        v.w += t.w;
+    }
+    reinterpret_cast<float4 *>(p.out)[i] = v;
+}
+
 }  // namespace chain
 }  // namespace moe
 
@@ -1374,6 +1941,261 @@ static int run(const moe_stack_desc *sd, const Shapes &s, const float *x0, float
     return MOE_OK;
 }
 
+// ---------------------------------------------------------------- cluster variant (host)
+// Which variant moe_decode_step_chain runs: 0 the library's choice, 1 two
+// kernels per layer, 2 one cluster kernel per layer; and whether the cluster
+// kernel prefetches its down rows into L2 in its prologue.
+static int g_variant = 0;
+static int g_prefetch = 1;
+
+// Workspace of the cluster variant: status word | out per layer [depth][d] |
+// weighted slot outputs [depth][S][d] | head logits [depth][E] | router
+// logits [E].
+struct CWs {
+    size_t outs, part, z, zr, total;
+};
+
+static CWs cws_layout(int d, int E, int S, int depth) {
+    CWs w;
+    size_t off = 256;
+    w.outs = off;
+    off = al256(off + (size_t)depth * d * 4);
+    w.part = off;
+    off = al256(off + (size_t)depth * S * d * 4);
+    w.z = off;
+    off = al256(off + (size_t)depth * E * 4);
+    w.zr = off;
+    off = al256(off + (size_t)E * 4);
+    w.total = off;
+    return w;
+}
+
+static int c_rmax(const Shapes &s) { return std::max(s.rd_routed, s.rd_shared); }
+
+// Whether the cluster variant takes this stack (a message in *why if not).
+template <int BITS>
+static bool c_fits(const moe_stack_desc *sd, const Shapes &s, const char **why) {
+    const moe_experts_desc &e0 = sd->experts[0];
+    const int rg = e0.shared ? e0.shared_lora[0].r : 0, ru = e0.shared ? e0.shared_lora[1].r : 0;
+    if (s.heads && (s.H <= 0 || s.H % 32)) {
+        *why = "the head width must be a positive multiple of 32";
+        return false;
+    }
+    if (rg + ru > 32 || c_rmax(s) > kCWarps) {
+        *why = "adapter ranks too large";
+        return false;
+    }
+    const int nch = s.F / (128 / s.bits), no = (s.d + kCluster - 1) / kCluster;
+    const int rw = (no + kCWarps - 1) / kCWarps;
+    if (32 % nch || (rw + 32 / nch - 1) / (32 / nch) > kDPass || s.F > kAPass * 256) {
+        *why = "the down rows of a warp do not fit its registers";
+        return false;
+    }
+    const CLay Lo = c_layout(s.d, s.F, s.E, s.H, s.K, s.bits, kCluster, c_rmax(s));
+    int dev = 0, smem_max = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (Lo.total > (uint32_t)smem_max) {
+        *why = "a CTA's share of a slot does not fit shared memory";
+        return false;
+    }
+    return true;
+}
+
+template <int BITS>
+static int c_configure(int dev, uint32_t smem) {
+    static thread_local int done_dev = -1;
+    static thread_local uint32_t done_smem = 0;
+    if (done_dev == dev && done_smem >= smem) return MOE_OK;
+    int smem_max = 0;
+    cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (cudaFuncSetAttribute(chain_c_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_c_kernel<BITS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_c_kernel<BITS>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_fin_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+        return fail(MOE_ECUDA, "decode_step_chain: cluster kernel attributes");
+    done_dev = dev;
+    done_smem = smem;
+    return MOE_OK;
+}
+
+// Clusters of the layer kernel an SM set can hold at once (occupancy API).
+template <int BITS>
+static int c_clusters(int grid, uint32_t smem, int *n) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kCluster;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(n, chain_c_kernel<BITS>, &cfg) != cudaSuccess)
+        return fail(MOE_ECUDA, "decode_step_chain: cluster occupancy");
+    return MOE_OK;
+}
+
+template <int BITS>
+static int run_c(const moe_stack_desc *sd, const Shapes &s, const float *x0, float *out, int32_t *ridx,
+                 float *rw, float *rmargin, int t, uint8_t *ws, cudaStream_t st) {
+    const int C = kCluster, rmax = c_rmax(s);
+    const CLay Lo = c_layout(s.d, s.F, s.E, s.H, s.K, s.bits, C, rmax);
+    int dev = 0, smem_max = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&smem_max, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (int rc = configure<BITS>(dev, smem_max)) return rc;
+    if (int rc = c_configure<BITS>(dev, Lo.total)) return rc;
+    int ncl = 0;
+    if (int rc = c_clusters<BITS>((s.S + 1) * C, Lo.total, &ncl)) return rc;
+    if (ncl < 1)
+        return fail(MOE_EUNSUPPORTED, "decode_step_chain: no cluster of %d CTAs with %u bytes fits", C, Lo.total);
+    const CWs W = cws_layout(s.d, s.E, s.S, s.depth);
+    int32_t *err = reinterpret_cast<int32_t *>(ws);
+    if (cudaMemsetAsync(err, 0, sizeof(int32_t), st) != cudaSuccess)
+        return fail(MOE_ECUDA, "decode_step_chain: status reset");
+    float *outs = reinterpret_cast<float *>(ws + W.outs), *part = reinterpret_cast<float *>(ws + W.part);
+    float *z = reinterpret_cast<float *>(ws + W.z), *zr = reinterpret_cast<float *>(ws + W.zr);
+    const int cur = t % 3, nxt = (t + 1) % 3, prv = (t + 2) % 3;
+    const size_t ps = (size_t)s.S * s.d;
+
+    CP b{};
+    b.d = s.d;
+    b.F = s.F;
+    b.E = s.E;
+    b.K = s.K;
+    b.H = s.H;
+    b.S = s.S;
+    b.n_cta = (s.S + 1) * C;
+    b.depth = s.depth;
+    b.cur = cur;
+    b.prv = prv;
+    const BlobLayout BL = blob_layout(s.d, s.F, s.bits);
+    b.stride = sd->experts[0].expert_stride;
+    b.gu_off = (uint32_t)BL.gu_off;
+    b.down_off = (uint32_t)BL.down_off;
+    b.rec_d = (uint32_t)BL.gu_rec;
+    b.rec_F = (uint32_t)BL.down_rec;
+    b.rec_dh = (uint32_t)record_bytes(s.d, 4);
+    b.rec_H = s.H ? (uint32_t)record_bytes(s.H, 4) : 0u;
+    b.ridx = ridx;
+    b.rw = rw;
+    b.rmargin = rmargin;
+    b.err = err;
+    b.timeout_ns = sd->timeout_ns ? sd->timeout_ns : kDefaultWaitNs;
+    b.trace = sd->debug_trace;
+    int lid = 0;
+    bool first = true;
+    if (s.own0) {
+        // layer 0 routes itself on x0 (router logits, then its top-K)
+        CP p = b;
+        p.N = 0;
+        p.n_cta = sms_of_device();
+        p.launch_id = lid++;
+        p.L = layer_of(sd, 0, s);
+        p.x_in = x0;
+        const size_t sr = padded(s.d, 32) * 4 + (size_t)(s.d / 32) * 4 + 32 * 4 + 16;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(p.n_cta);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = sr;
+        cfg.stream = st;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, chain_r_kernel, p, 1, zr);
+        if (e != cudaSuccess) return fail(MOE_ECUDA, "decode_step_chain: router launch: %s", cudaGetErrorString(e));
+        CP q = b;
+        q.launch_id = lid++;
+        q.topk_z = zr;
+        q.topk_set = cur;
+        q.topk_tgt = 0;
+        if (int rc = launch(chain_topk_kernel, q, 1, 32, 0, true, st, "router top-K")) return rc;
+        first = false;
+    }
+    for (int N = 0; N < s.depth; N++) {
+        CP p = b;
+        p.N = N;
+        p.L = layer_of(sd, N, s);
+        p.head = head_runs(s, N) ? 1 : 0;
+        p.route_late = N == 0 && s.own0;
+        p.x_is_out = N > 0;
+        p.z = z + (size_t)N * s.E;
+        p.smap = sd->slot_map && !p.route_late ? sd->slot_map + (size_t)N * s.K : nullptr;
+        p.debug_unset_wait = N == 0 ? sd->debug_unset_wait : 0;
+        p.launch_id = lid++;
+        CX x{};
+        x.C = C;
+        x.rmax = rmax;
+        x.prefetch = g_prefetch;
+        x.base = N <= 1 ? x0 : outs + (size_t)(N - 2) * s.d;
+        x.part_in = N == 0 ? nullptr : part + (size_t)(N - 1) * ps;
+        x.part = part + (size_t)N * ps;
+        x.x_out = N >= 1 ? outs + (size_t)(N - 1) * s.d : nullptr;
+        if (sd->layer_ready && sd->layer_ready[N]) {
+            const cudaError_t e = cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(sd->layer_ready[N]), 0);
+            if (e != cudaSuccess)
+                return fail(MOE_ECUDA, "decode_step_chain: wait for layer %d: %s", N, cudaGetErrorString(e));
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((s.S + p.head) * C);
+        cfg.blockDim = dim3(kCThreads);
+        cfg.dynamicSmemBytes = Lo.total;
+        cfg.stream = st;
+        cudaLaunchAttribute at[2];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = C;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = first ? 1 : 2;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, chain_c_kernel<BITS>, p, x);
+        if (e != cudaSuccess) return fail(MOE_ECUDA, "decode_step_chain: layer launch: %s", cudaGetErrorString(e));
+        first = false;
+    }
+    {
+        // the last layer's outputs onto its residual
+        CP p = b;
+        p.out = out;
+        p.launch_id = lid++;
+        CX x{};
+        x.base = s.depth == 1 ? x0 : outs + (size_t)(s.depth - 2) * s.d;
+        x.part_in = part + (size_t)(s.depth - 1) * ps;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((s.d / 4 + 255) / 256);
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, chain_fin_kernel, p, x);
+        if (e != cudaSuccess) return fail(MOE_ECUDA, "decode_step_chain: output launch: %s", cudaGetErrorString(e));
+    }
+    const int n_heads = head_runs(s, s.depth - 1) ? s.depth : s.depth - 1;
+    if (n_heads > 0) {
+        CP q = b;
+        q.launch_id = lid++;
+        q.topk_set = nxt;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((n_heads + kRankWarps - 1) / kRankWarps);
+        cfg.blockDim = dim3(kRankWarps * 32);
+        cfg.stream = st;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, chain_rank_kernel, q, (const float *)z, n_heads);
+        if (e != cudaSuccess) return fail(MOE_ECUDA, "decode_step_chain: ranking launch: %s", cudaGetErrorString(e));
+    }
+    return MOE_OK;
+}
+
 }  // namespace chain
 }  // namespace moe
 
@@ -1383,7 +2205,15 @@ extern "C" size_t moe_decode_step_chain_workspace_bytes(const moe_stack_desc *sd
     if (check_decode_stack(sd) != MOE_OK) return 0;
     const chain::Shapes s = chain::shapes_of(sd);
     const int sms = chain::chain_ctas(sd);
-    return chain::ws_layout(s.d, s.F, s.E, s.H, s.S, s.depth, sms > 0 ? sms : 256).total;
+    return std::max(chain::ws_layout(s.d, s.F, s.E, s.H, s.S, s.depth, sms > 0 ? sms : 256).total,
+                    chain::cws_layout(s.d, s.E, s.S, s.depth).total);
+}
+
+extern "C" int moe_decode_step_chain_variant(int variant, int prefetch_l2) {
+    if (variant < 0 || variant > 2) return fail(MOE_EINVAL, "decode_step_chain_variant: variant %d", variant);
+    chain::g_variant = variant;
+    chain::g_prefetch = prefetch_l2 ? 1 : 0;
+    return MOE_OK;
 }
 
 extern "C" int moe_decode_step_chain_info(const moe_stack_desc *sd, moe_chain_info *info) {
@@ -1418,6 +2248,13 @@ extern "C" int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, 
         return fail(MOE_EUNSUPPORTED, "decode_step_chain: slots x F = %d x %d (or d, E) too large "
                                       "for %d SMs", s.S, s.F, n);
     uint8_t *w = static_cast<uint8_t *>(ws);
+    if (chain::g_variant == 2) {
+        const char *why = "";
+        if (!(s.bits == 4 ? chain::c_fits<4>(sd, s, &why) : chain::c_fits<2>(sd, s, &why)))
+            return fail(MOE_EUNSUPPORTED, "decode_step_chain: cluster variant: %s", why);
+        return s.bits == 4 ? chain::run_c<4>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream)
+                           : chain::run_c<2>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream);
+    }
     return s.bits == 4 ? chain::run<4>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream)
                        : chain::run<2>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream);
 }

@@ -104,6 +104,7 @@ def lib():
                 "moe_decode_step_chain_workspace_bytes": (S, [C.POINTER(StackDesc)]),
                 "moe_decode_step_chain": (I, [C.POINTER(StackDesc), P, P, P, P, P, I, P, S, P]),
                 "moe_decode_step_chain_info": (I, [C.POINTER(StackDesc), C.POINTER(ChainInfo)]),
+                "moe_decode_step_chain_variant": (I, [I, I]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -314,6 +315,13 @@ def moe_decode_step_chain(sd: StackDesc, x0, out, route_idx, route_w, route_marg
     _check(lib().moe_decode_step_chain(C.byref(sd), _ptr(x0), _ptr(out), _ptr(route_idx),
                                        _ptr(route_w), _ptr(route_margin), t, _ptr(ws), _nbytes(ws),
                                        _stream(stream)), "moe_decode_step_chain")
+
+
+def moe_decode_step_chain_variant(variant: int, prefetch_l2: bool = True) -> None:
+    """0: the library's choice, 1: two kernels per layer, 2: one cluster
+    kernel per layer (process-wide; read when a step is enqueued)."""
+    _check(lib().moe_decode_step_chain_variant(int(variant), int(bool(prefetch_l2))),
+           "moe_decode_step_chain_variant")
 
 
 def moe_decode_step_chain_info(sd: StackDesc) -> dict:

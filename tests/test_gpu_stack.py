@@ -30,21 +30,30 @@ def run_gpu(cfg, steps, fused=False, make=None):
     """Run `steps` decode steps (captured graphs from step 1 on) and record
     each step's routes and output.  make(model): another stack driver to run
     (default: DecodeStack on the path `fused` names)."""
+    from int4_expert_gemv_gb300 import moe
     from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
     dm = DeviceModel(cfg)
-    st = make(dm) if make is not None else DecodeStack(dm, fused=fused)
-    rec = []
-    for t in range(steps):
-        x0 = torch.from_numpy(synth.step_input(cfg, t)[0]).cuda()
-        st.step(x0)
-        if t == 0:
-            st.capture()
-        idx, w, mg = st.used_routes(t)
-        torch.cuda.synchronize()
-        rec.append(dict(idx=idx.cpu().numpy(), w=w.cpu().double().numpy(),
-                        margin=mg.cpu().double().numpy(), out=st.stream.cpu().double().numpy()))
-    if st.fused:
-        assert st.status() == 0
+    cluster = fused == "cluster"
+    if cluster:
+        moe.moe_decode_step_chain_variant(2)
+        fused = "chain"
+    try:
+        st = make(dm) if make is not None else DecodeStack(dm, fused=fused)
+        rec = []
+        for t in range(steps):
+            x0 = torch.from_numpy(synth.step_input(cfg, t)[0]).cuda()
+            st.step(x0)
+            if t == 0:
+                st.capture()
+            idx, w, mg = st.used_routes(t)
+            torch.cuda.synchronize()
+            rec.append(dict(idx=idx.cpu().numpy(), w=w.cpu().double().numpy(),
+                            margin=mg.cpu().double().numpy(), out=st.stream.cpu().double().numpy()))
+        if st.fused:
+            assert st.status() == 0
+    finally:
+        if cluster:
+            moe.moe_decode_step_chain_variant(0)
     del st, dm
     torch.cuda.empty_cache()
     return rec
@@ -88,7 +97,7 @@ def check_stack(cfg, steps, fused=False, make=None):
 
 
 PATHS = [pytest.param(False, id="per-call"), pytest.param(True, id="fused"),
-         pytest.param("chain", id="chain")]
+         pytest.param("chain", id="chain"), pytest.param("cluster", id="cluster")]
 
 
 @pytest.mark.parametrize("fused", PATHS)
@@ -110,6 +119,8 @@ def test_8b_stack_full_size(fused):
 @pytest.mark.parametrize("fused", PATHS)
 @pytest.mark.parametrize("name", ["wide-int4", "wide-int2"])
 def test_wide_stack_full_size(name, fused):
+    if fused == "cluster":
+        pytest.skip("a CTA's share of a wide slot does not fit shared memory (two-kernel chain)")
     check_stack(ALL[name], 2, fused)
 
 
@@ -175,6 +186,60 @@ def test_chain_bounded_wait_times_out_and_recovers():
         assert torch.equal(st.stream, ref.stream)
         assert torch.equal(st.r_idx, ref.r_idx)
     assert torch.isfinite(st.stream).all()
+
+
+def test_cluster_bounded_wait_times_out_and_recovers():
+    """The cluster form of the chained step: with the test hook on, CTA 0 of
+    layer 0 waits for bytes no copy sends; after the 50 ms limit MOE_ETIMEOUT
+    lands in the status word.  The CTA then carries on (its cluster peers'
+    waits for its h run out the same way), every CTA reaches the cluster
+    barrier and the step ends; steps run again with the hook off give the
+    same bits as a stack that never stalled."""
+    import time
+    from int4_expert_gemv_gb300 import moe
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    cfg = ALL["35b-L4"]
+    dm = DeviceModel(cfg)
+    moe.moe_decode_step_chain_variant(2)
+    try:
+        st, ref = DecodeStack(dm, fused="chain"), DecodeStack(dm, fused="chain")
+        xs = [torch.from_numpy(synth.step_input(cfg, t)[0]).cuda() for t in range(4)]
+        st.step(xs[0])                                                     # step 0: per-call
+        ref.step(xs[0])
+        st.sd.timeout_ns = 50_000_000
+        st.sd.debug_unset_wait = 1
+        t0 = time.time()
+        st.step(xs[1])
+        assert st.status() == moe.MOE_ETIMEOUT
+        assert time.time() - t0 < 10.0
+        torch.cuda.synchronize()                                           # context alive
+        st.sd.debug_unset_wait = 0
+        st.sd.timeout_ns = 0
+        st.t = 1
+        for t in (1, 2, 3):
+            st.step(xs[t])
+            ref.step(xs[t])
+            assert st.status() == moe.MOE_OK
+            assert torch.equal(st.stream, ref.stream)
+            assert torch.equal(st.r_idx, ref.r_idx)
+    finally:
+        moe.moe_decode_step_chain_variant(0)
+
+
+def test_cluster_variant_rejects_what_does_not_fit():
+    """The wide shapes' slot shares do not fit a CTA: the cluster form
+    reports MOE_EUNSUPPORTED before enqueueing anything."""
+    from int4_expert_gemv_gb300 import moe
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    cfg = replace(ALL["wide-int4"], L=1, depth=2)
+    st = DecodeStack(DeviceModel(cfg), fused="chain")
+    st.step(torch.from_numpy(synth.step_input(cfg, 0)[0]).cuda())
+    moe.moe_decode_step_chain_variant(2)
+    try:
+        with pytest.raises(RuntimeError, match="MOE_EUNSUPPORTED"):
+            st.step(torch.from_numpy(synth.step_input(cfg, 1)[0]).cuda())
+    finally:
+        moe.moe_decode_step_chain_variant(0)
 
 
 @pytest.mark.parametrize("name", ["35b", "35b-K2", "35b-K8", "8b", "tiny"])
