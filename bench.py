@@ -86,7 +86,7 @@ def peaks():
 
 def measured_traffic(cfg, path: str):
     """DRAM bytes (read + write) of one whole decode step of cfg on `path`
-    ("fused" or "chain"), scaled from the ncu capture of the 4-layer 35B-like
+    ("fused", "chain" or "cluster"), scaled from the ncu capture of the 4-layer 35B-like
     stack summarised under profiles/ (per-layer bytes x layers + the step's
     fixed launches); None for other layer shapes, or when the kernel sources
     have changed since that capture."""
@@ -98,7 +98,8 @@ def measured_traffic(cfg, path: str):
     layers = cfg.depth
     import hashlib
     import re
-    name = {"fused": "decode_step_35b_L4.md", "chain": "decode_chain_35b_L4.md"}.get(path)
+    name = {"fused": "decode_step_35b_L4.md", "chain": "decode_chain_35b_L4.md",
+            "cluster": "decode_cluster_35b_L4.md"}.get(path)
     p = os.path.join(ROOT, "profiles", name) if name else ""
     if not p or not os.path.exists(p):
         return None
