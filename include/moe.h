@@ -523,6 +523,18 @@ int moe_decode_step_chain_info(const moe_stack_desc *sd, moe_chain_info *info);
  * workspace from moe_decode_step_chain_workspace_bytes (sized for both).
  * MOE_EINVAL for another variant. */
 int moe_decode_step_chain_variant(int variant, int prefetch_l2);
+
+/* Graph cache of moe_decode_step_chain (process-wide).  A call's launches
+ * depend only on the descriptor's values, the call's pointers, t mod 3, the
+ * device and the variant, so a call not made under stream capture is
+ * recorded once into a CUDA graph (on an internal stream, thread-local
+ * capture mode) and later calls with the same key launch that graph on the
+ * caller's stream: one host launch per step instead of about two per layer.
+ * Calls with layer_ready events, debug_unset_wait or debug_trace are never
+ * cached.  max_graphs: graphs kept (least recently used dropped first;
+ * default 16); 0 disables the cache.  Every call empties the cache.
+ * MOE_EINVAL outside 0 .. 1024. */
+int moe_decode_step_chain_cache(int max_graphs);
 int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, float *out,
                           int32_t *route_idx, float *route_w, float *route_margin,
                           int t, void *ws, size_t ws_bytes, cudaStream_t stream);

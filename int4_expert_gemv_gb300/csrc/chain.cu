@@ -26,6 +26,8 @@
 #include <algorithm>
 #include <cfloat>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "internal.h"
 #include "step_common.cuh"
@@ -2196,6 +2198,130 @@ static int run_c(const moe_stack_desc *sd, const Shapes &s, const float *x0, flo
     return MOE_OK;
 }
 
+
+// ---------------------------------------------------------------- graph cache
+// A call's launches depend only on the descriptor's values, the call's
+// pointers, t mod 3, the device and the form chosen -- not on the contents
+// of any buffer.  So a call not made under stream capture is recorded once
+// into a CUDA graph (captured on an internal stream of the calling thread,
+// in thread-local capture mode) and later calls with the same key launch
+// that graph on the caller's stream: one host launch instead of two per
+// layer.  Calls with ready events or debug hooks are never cached.  At most
+// g_cache_max graphs (least recently used out first; 0 disables).
+static std::mutex g_gmu;
+static int g_cache_max = 16;
+struct GEntry {
+    std::vector<uint8_t> key;
+    cudaGraphExec_t exec;      // null: the call could not be captured (run directly)
+    unsigned long long used;
+};
+static std::vector<GEntry> g_graphs;
+static unsigned long long g_tick = 0;
+
+template <class T>
+static void put(std::vector<uint8_t> &k, const T &v) {
+    const uint8_t *b = reinterpret_cast<const uint8_t *>(&v);
+    k.insert(k.end(), b, b + sizeof(T));
+}
+
+static std::vector<uint8_t> step_key(const moe_stack_desc *sd, const Shapes &s, const float *x0,
+                                     const float *out, const int32_t *ridx, const float *rw,
+                                     const float *rmg, int t, const void *ws) {
+    std::vector<uint8_t> k;
+    k.reserve(256 + 256 * (size_t)s.n_res);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    put(k, dev);
+    put(k, g_variant);
+    put(k, g_prefetch);
+    put(k, t % 3);
+    put(k, x0);
+    put(k, out);
+    put(k, ridx);
+    put(k, rw);
+    put(k, rmg);
+    put(k, ws);
+    const int sh[] = {s.d, s.F, s.E, s.K, s.H, s.S, s.bits, s.depth, s.n_res, s.self_predict, s.own0,
+                      s.rd_routed, s.rd_shared, s.heads ? 1 : 0, sd->free_sms};
+    put(k, sh);
+    put(k, sd->experts[0].expert_stride);
+    put(k, sd->timeout_ns);
+    put(k, sd->slot_map);
+    for (int i = 0; i < s.n_res; i++) {
+        const CLayer L = layer_of(sd, i, s);
+        const void *ptrs[] = {L.pool, L.shared, L.la_d, L.lb_d, L.sa[0], L.sa[1], L.sa[2], L.sb[0], L.sb[1],
+                              L.sb[2], L.router, L.fc1x, L.fc2, L.lx, L.fc1_tab, L.b1, L.b2, L.l_tab, L.bl};
+        put(k, ptrs);
+        const size_t strides[] = {L.la_ds, L.lb_ds};
+        put(k, strides);
+        const int ranks[] = {L.r_d, L.sr[0], L.sr[1], L.sr[2]};
+        put(k, ranks);
+        const float scales[] = {L.s_d, L.ss[0], L.ss[1], L.ss[2]};
+        put(k, scales);
+    }
+    return k;
+}
+
+static cudaStream_t capture_stream() {
+    static thread_local cudaStream_t caps[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!caps[dev] && cudaStreamCreateWithFlags(&caps[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        cudaGetLastError();
+        caps[dev] = nullptr;
+    }
+    return caps[dev];
+}
+
+template <class Direct>
+static int run_cached(const std::vector<uint8_t> &key, Direct direct, cudaStream_t st) {
+    {
+        std::lock_guard<std::mutex> g(g_gmu);
+        for (GEntry &e : g_graphs)
+            if (e.key == key) {
+                e.used = ++g_tick;
+                if (!e.exec) return direct(st);
+                const cudaError_t r = cudaGraphLaunch(e.exec, st);
+                if (r != cudaSuccess) return fail(MOE_ECUDA, "decode_step_chain: graph launch: %s", cudaGetErrorString(r));
+                return MOE_OK;
+            }
+    }
+    // a new key: this call runs directly (which also sets the kernels'
+    // attributes up), then its launches are recorded for the next calls
+    if (int rc = direct(st)) return rc;
+    cudaGraphExec_t exec = nullptr;
+    cudaStream_t cap = capture_stream();
+    if (cap && cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+        const int rc = direct(cap);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t ec = cudaStreamEndCapture(cap, &graph);
+        if (rc == MOE_OK && ec == cudaSuccess && graph && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+            exec = nullptr;
+        if (graph) cudaGraphDestroy(graph);
+    }
+    cudaGetLastError();       // a failed capture leaves no sticky error (the key then runs directly)
+    {
+        std::lock_guard<std::mutex> g(g_gmu);
+        if ((int)g_graphs.size() >= g_cache_max) {
+            size_t old = 0;
+            for (size_t i = 1; i < g_graphs.size(); i++)
+                if (g_graphs[i].used < g_graphs[old].used) old = i;
+            if (g_graphs[old].exec) cudaGraphExecDestroy(g_graphs[old].exec);   // freed when it completes
+            g_graphs.erase(g_graphs.begin() + (long)old);
+        }
+        g_graphs.push_back(GEntry{key, exec, ++g_tick});
+    }
+    return MOE_OK;
+}
+
+static void clear_cache() {
+    std::lock_guard<std::mutex> g(g_gmu);
+    for (GEntry &e : g_graphs)
+        if (e.exec) cudaGraphExecDestroy(e.exec);
+    g_graphs.clear();
+}
+
 }  // namespace chain
 }  // namespace moe
 
@@ -2252,9 +2378,29 @@ extern "C" int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, 
         const char *why = "";
         if (!(s.bits == 4 ? chain::c_fits<4>(sd, s, &why) : chain::c_fits<2>(sd, s, &why)))
             return fail(MOE_EUNSUPPORTED, "decode_step_chain: cluster variant: %s", why);
-        return s.bits == 4 ? chain::run_c<4>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream)
-                           : chain::run_c<2>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream);
     }
-    return s.bits == 4 ? chain::run<4>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream)
-                       : chain::run<2>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, stream);
+    const int variant = chain::g_variant;
+    auto direct = [&](cudaStream_t st) {
+        if (variant == 2)
+            return s.bits == 4 ? chain::run_c<4>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, st)
+                               : chain::run_c<2>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, st);
+        return s.bits == 4 ? chain::run<4>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, st)
+                           : chain::run<2>(sd, s, x0, out, route_idx, route_w, route_margin, t, w, st);
+    };
+    if (chain::g_cache_max > 0 && !sd->layer_ready && !sd->debug_unset_wait && !sd->debug_trace) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone)
+            return chain::run_cached(chain::step_key(sd, s, x0, out, route_idx, route_w, route_margin, t, ws),
+                                     direct, stream);
+        cudaGetLastError();
+    }
+    return direct(stream);
+}
+
+extern "C" int moe_decode_step_chain_cache(int max_graphs) {
+    if (max_graphs < 0 || max_graphs > 1024)
+        return fail(MOE_EINVAL, "decode_step_chain_cache: %d graphs (0 .. 1024)", max_graphs);
+    chain::clear_cache();
+    chain::g_cache_max = max_graphs;
+    return MOE_OK;
 }

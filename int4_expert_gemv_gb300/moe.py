@@ -105,6 +105,7 @@ def lib():
                 "moe_decode_step_chain": (I, [C.POINTER(StackDesc), P, P, P, P, P, I, P, S, P]),
                 "moe_decode_step_chain_info": (I, [C.POINTER(StackDesc), C.POINTER(ChainInfo)]),
                 "moe_decode_step_chain_variant": (I, [I, I]),
+                "moe_decode_step_chain_cache": (I, [I]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -322,6 +323,11 @@ def moe_decode_step_chain_variant(variant: int, prefetch_l2: bool = True) -> Non
     kernel per layer (process-wide; read when a step is enqueued)."""
     _check(lib().moe_decode_step_chain_variant(int(variant), int(bool(prefetch_l2))),
            "moe_decode_step_chain_variant")
+
+
+def moe_decode_step_chain_cache(max_graphs: int) -> None:
+    """Graphs moe_decode_step_chain keeps for repeated calls (0: none)."""
+    _check(lib().moe_decode_step_chain_cache(int(max_graphs)), "moe_decode_step_chain_cache")
 
 
 def moe_decode_step_chain_info(sd: StackDesc) -> dict:

@@ -226,6 +226,36 @@ def test_cluster_bounded_wait_times_out_and_recovers():
         moe.moe_decode_step_chain_variant(0)
 
 
+def test_chain_graph_cache_gives_the_same_bits():
+    """moe_decode_step_chain replays repeated calls from its graph cache (on
+    by default): the routes and outputs of 8 steps (every t mod 3, several
+    hits per key) equal, bit for bit, those of the same calls run directly
+    (cache off), on both forms of the step."""
+    from int4_expert_gemv_gb300 import moe
+    from int4_expert_gemv_gb300.model import DecodeStack, DeviceModel
+    cfg = ALL["35b-L4"]
+    dm = DeviceModel(cfg)
+    xs = [torch.from_numpy(synth.step_input(cfg, t)[0]).cuda() for t in range(8)]
+    try:
+        for variant in (1, 2):
+            moe.moe_decode_step_chain_variant(variant)
+            res = {}
+            for cache in (16, 0):
+                moe.moe_decode_step_chain_cache(cache)
+                st = DecodeStack(dm, fused="chain")
+                res[cache] = []
+                for t in range(8):
+                    st.step(xs[t])
+                    res[cache].append((st.stream.clone(), st.r_idx.clone(), st.r_w.clone()))
+                assert st.status() == moe.MOE_OK
+            for a, b in zip(res[16], res[0]):
+                for u, v in zip(a, b):
+                    assert torch.equal(u, v)
+    finally:
+        moe.moe_decode_step_chain_variant(0)
+        moe.moe_decode_step_chain_cache(16)
+
+
 def test_cluster_variant_rejects_what_does_not_fit():
     """The wide shapes' slot shares do not fit a CTA: the cluster form
     reports MOE_EUNSUPPORTED before enqueueing anything."""
