@@ -300,3 +300,18 @@ def test_decode_step_chain_validation(m):
     need2 = L.moe_decode_step_chain_workspace_bytes(C.byref(sd2))
     assert need2 > 0
     assert L.moe_decode_step_chain(C.byref(sd2), p, p, p, p, p, 1, p, need2, None) == m.MOE_EUNSUPPORTED
+
+
+def test_chain_variant_and_cache_settings(m):
+    """The decode-chain settings validate their arguments on the host: an
+    unknown variant or a cache size outside 0 .. 1024 is MOE_EINVAL; valid
+    values are accepted (and put back to the defaults)."""
+    lib = m.lib()
+    assert lib.moe_decode_step_chain_variant(3, 1) == m.MOE_EINVAL
+    assert lib.moe_decode_step_chain_variant(-1, 1) == m.MOE_EINVAL
+    assert lib.moe_decode_step_chain_cache(-1) == m.MOE_EINVAL
+    assert lib.moe_decode_step_chain_cache(1025) == m.MOE_EINVAL
+    for v in (1, 2, 0):
+        assert lib.moe_decode_step_chain_variant(v, 1) == m.MOE_OK
+    assert lib.moe_decode_step_chain_cache(0) == m.MOE_OK
+    assert lib.moe_decode_step_chain_cache(16) == m.MOE_OK
