@@ -71,7 +71,7 @@ def parse():
                          "(h exchanged in distributed shared memory); fused: one persistent "
                          "kernel per step; per-call: the four calls per layer")
     ap.add_argument("--no-l2-prefetch", action="store_true",
-                    help="cluster path: no L2 prefetch of the next layer's weights")
+                    help="cluster path: no L2 prefetch of the down rows in the prologue")
     return ap.parse_args()
 
 
