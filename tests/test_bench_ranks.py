@@ -45,3 +45,27 @@ def test_single_rank_needs_no_collective():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_launch_counts_of_the_decode_paths():
+    """bench.py's gpu_launches claim per step, on a stand-in stack: the
+    35b stack's two-kernel chain is the layer-0 router and its top-K, A and
+    B per layer and one ranking launch (83); its cluster form is the router,
+    the top-K, one launch per layer, the output sum and the ranking (44); the
+    single self-predicting tiny layer needs no router."""
+    import sys
+    from types import SimpleNamespace
+    sys.path.insert(0, ROOT)
+    import bench
+    from int4_expert_gemv_gb300.configs import ALL, TINY
+
+    def stand_in(shared_gu_rank):
+        lora = [SimpleNamespace(r=0) for _ in range(3)]
+        shared = [SimpleNamespace(r=shared_gu_rank) for _ in range(3)]
+        ed = SimpleNamespace(lora=lora, shared_lora=shared)
+        return SimpleNamespace(chain=True, fused=True, m=SimpleNamespace(layers=[{"experts_desc": ed}]))
+
+    assert bench.kernels_per_step(ALL["35b"], stand_in(16)) == 83
+    assert bench.kernels_per_step(ALL["35b"], stand_in(16), cluster=True) == 44
+    assert bench.kernels_per_step(TINY, stand_in(0)) == 3
+    assert bench.kernels_per_step(TINY, stand_in(0), cluster=True) == 3
