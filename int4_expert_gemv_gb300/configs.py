@@ -89,6 +89,9 @@ ALL = {
     "35b-L4": replace(MOE35B, name="35b-like-d2048-E256-K4-F512-shared-L4", L=4, depth=4),
     "35b-K2": k_sweep(2),
     "35b-K8": k_sweep(8),
+    # the 35B-like stack with fp16 head matrices (per-call path only): the
+    # head-bytes side of the expert-byte share
+    "35b-fp16head": replace(MOE35B, name="35b-like-fp16-heads", head_prec="fp16"),
     "8b": MOE8B,
     "wide-int4": wide(4),
     "wide-int2": wide(2),
