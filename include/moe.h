@@ -533,6 +533,9 @@ int moe_decode_step_chain_variant(int variant, int prefetch_l2);
  * Calls with layer_ready events, debug_unset_wait or debug_trace are never
  * cached.  max_graphs: graphs kept (least recently used dropped first;
  * default 16); 0 disables the cache.  Every call empties the cache.
+ * The graphs belong to the device's current context: call
+ * moe_decode_step_chain_cache(0) before resetting the device (a graph of a
+ * destroyed context fails to launch with MOE_ECUDA).
  * MOE_EINVAL outside 0 .. 1024. */
 int moe_decode_step_chain_cache(int max_graphs);
 int moe_decode_step_chain(const moe_stack_desc *sd, const float *x0, float *out,
